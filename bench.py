@@ -1,0 +1,341 @@
+"""Benchmark of the paged MLA decode path on one GB300 (or N replicas).
+
+One step = one ``mla_decode_run`` (split-KV decode kernel + LSE merge kernel)
+over one batch of the workload, inputs resident in HBM.  Default workload:
+DeepSeek-V3-shaped decode, batch 64, 128 heads, kv_len 4096 per request,
+page size 64, bf16 cache, pages randomly permuted over the pool.
+
+Prints one JSON line.  ``value`` is microseconds per batch (device time of
+the timed steps, CUDA events on the launching stream, L2 flushed between
+steps by writing a buffer larger than L2).  ``roofline`` reports the decode
+kernel alone (timed with events recorded by the library around it) against
+the measured HBM bandwidth; ``e2e`` is the same step through the host-buffer
+entry point with the q / out / lse copies inside the timed region;
+``cpu_baseline`` is the float64 oracle on a bounded sample of the batch.
+
+``--impl reference`` times that oracle alone (the slow CPU reference of this
+method) on the same workload, metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode µs/batch, KV GB/s and % of HBM/bf16 roofline on 1 GB300"
+UNIT = "us/batch"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FLOP_PER_TOKEN_HEAD = 2 * 576 + 2 * 512          # QK^T over 576 + PV over 512
+
+
+def workload_config(x) -> dict:
+    return {"workload": f"paged MLA decode {x.name}: batch {x.batch}, heads {x.num_heads}, "
+                        f"kv_len {'mixed' if len(set(x.kv_len.tolist())) > 1 else int(x.kv_len[0])}, "
+                        f"page {x.page_size}, {x.kv_dtype} cache, kv_lora_rank 512, rope 64",
+            "batch": x.batch, "num_heads": x.num_heads, "page_size": x.page_size,
+            "total_kv_tokens": x.total_tokens, "kv_dtype": x.kv_dtype,
+            "sm_scale": x.sm_scale, "l2": "flushed between steps (256 MiB write)"}
+
+
+def algorithmic(x) -> tuple[float, float]:
+    """(bytes, flops) one batch must move / compute, pad rows not counted."""
+    tok = float(x.total_tokens)
+    kv_bytes_per_tok = 576 * (2 if x.kv_dtype == "bf16" else 1)
+    H, B = x.num_heads, x.batch
+    nbytes = (tok * kv_bytes_per_tok + B * H * 576 * 2 + B * H * 512 * 2 + B * H * 4
+              + 4 * len(x.kv_indices) + 8 * B)
+    flops = tok * H * FLOP_PER_TOKEN_HEAD
+    return nbytes, flops
+
+
+def peaks() -> tuple[float, float, float, str]:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            p = json.load(open(path))
+            hbm = float(p.get("hbm_gbs") or p.get("hbm_GBps"))
+            bf = float(p.get("bf16_tflops"))
+            bfs = float(p.get("bf16_tflops_sustained", bf))
+            return hbm, bf, bfs, "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def oracle_sample(x, budget_s: float):
+    """Float64 oracle on as many requests as fit in ~budget_s; returns (us per batch, n, secs)."""
+    from oracle import mla_oracle as O
+    order = list(range(x.batch))
+    done, t0 = 0, time.perf_counter()
+    for b in order:
+        O.mla_decode_inputs(x, requests=[b])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    secs = time.perf_counter() - t0
+    tok_done = float(x.kv_len[:done].astype(np.int64).sum())
+    us_per_batch = secs / max(tok_done, 1.0) * float(x.total_tokens) * 1e6
+    return us_per_batch, done, secs
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def run_reference(args, x) -> None:
+    """Oracle-only arm: each step is a bounded sample of the batch on host cores."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        us, n, secs = oracle_sample(x, args.ref_step_budget)
+        if i >= args.warmup:
+            per_step.append(us)
+    value = statistics.mean(per_step)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": value / 1000.0, "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(x),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(),
+                             "kind": "oracle",
+                             "sample": f"requests in ~{args.ref_step_budget:.0f}s per step, "
+                                       f"scaled to the whole batch by token count"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", default="deepseek")
+    ap.add_argument("--kernel", default="default", choices=["default", "tcgen05", "mma_sync"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--ref-step-budget", type=float, default=8.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from paged_mla_decode_02_gb300 import inputs as I
+    x = I.make_config(args.config)
+    if args.impl == "reference":
+        run_reference(args, x)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from paged_mla_decode_02_gb300 import build as B
+    from paged_mla_decode_02_gb300 import mla
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    B.build()
+    dev = torch.device("cuda", local)
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def cache(a):
+        if x.kv_dtype == "bf16":
+            return bf16(a)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev).view(torch.float8_e4m3fn)
+
+    q_nope, q_pe, ckv, kpe = bf16(x.q_nope), bf16(x.q_pe), cache(x.ckv), cache(x.kpe)
+    idx = torch.from_numpy(x.kv_indices).to(dev)
+    out = torch.empty((x.batch, x.num_heads, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((x.batch, x.num_heads), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    dec = mla.MLADecoder(x.batch, x.num_heads, args.kernel)
+    stream = torch.cuda.Stream(device=dev)
+    t_plan = time.perf_counter()
+    with torch.cuda.stream(stream):
+        dec.plan(x.kv_indptr, idx, x.kv_len, x.page_size, x.sm_scale)
+    stream.synchronize()
+    plan_us = (time.perf_counter() - t_plan) * 1e6
+    info = dec.info()
+
+    def step():
+        dec.run(q_nope, q_pe, ckv, kpe, out, lse, kv_scale=x.kv_scale, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+    dec.check_status()
+    k0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    k1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    s0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    s1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # torch creates an event lazily at its first record: create all of them
+    # here, before the library is handed their handles
+    with torch.cuda.stream(stream):
+        for e in k0 + k1 + s0 + s1:
+            e.record(stream)
+        for _ in range(args.warmup):
+            flush.zero_()
+            step()
+    stream.synchronize()
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    wall0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()
+            mla.mla_plan_set_profile_events(dec.handle, k0[i], k1[i])
+            s0[i].record(stream)
+            step()
+            s1[i].record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    mla.mla_plan_set_profile_events(dec.handle, None, None)
+    dec.check_status()
+
+    step_ms = [a.elapsed_time(b) for a, b in zip(s0, s1)]
+    kern_ms = [a.elapsed_time(b) for a, b in zip(k0, k1)]
+    dev_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([dev_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dev_ms = float(t.item())
+    us_per_batch = dev_ms * 1000.0 / args.steps / world
+
+    # end to end through the host-buffer entry point (q in, out / lse back)
+    qn_h = q_nope.cpu().pin_memory()
+    qp_h = q_pe.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    for _ in range(3):
+        mla.mla_decode_run_host(dec.handle, qn_h, qp_h, ckv, kpe, out_h, lse_h, x.kv_scale, stream)
+    e2e = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        mla.mla_decode_run_host(dec.handle, qn_h, qp_h, ckv, kpe, out_h, lse_h, x.kv_scale, stream)
+        e2e.append((time.perf_counter() - t0) * 1e6)
+    e2e_us = statistics.mean(e2e)
+
+    nbytes, flops = algorithmic(x)
+    hbm, bf, bfs, peak_src = peaks()
+    kern_us = statistics.mean(kern_ms) * 1000.0
+    achieved_gbs = nbytes / (kern_us * 1e-6) / 1e9
+    achieved_tf = flops / (kern_us * 1e-6) / 1e12
+    t_hbm = nbytes / (hbm * 1e9) * 1e6
+    t_tc = flops / (bf * 1e12) * 1e6
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    roof = {"bound": bound,
+            "achieved": achieved_gbs if bound == "hbm" else achieved_tf,
+            "peak": hbm if bound == "hbm" else bf,
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "peak_source": peak_src,
+            "traffic": None,
+            "kernel": "mla_decode (split-KV decode kernel)",
+            "kernel_us": kern_us,
+            "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+            "achieved_tflops": achieved_tf, "achieved_gbs": achieved_gbs,
+            "roofline_time_us": max(t_hbm, t_tc),
+            "frac_of_roofline_time_step": max(t_hbm, t_tc) / us_per_batch}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": us_per_batch, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": us_per_batch / 1000.0,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if x.kv_dtype == "bf16" else "fp8-e4m3 cache, bf16 mma",
+            "data": "synthetic", "config": workload_config(x),
+            "kv_gbs": float(x.total_tokens) * 576 * (2 if x.kv_dtype == "bf16" else 1)
+                      / (us_per_batch * 1e-6) / 1e9,
+            "tflops": flops / (us_per_batch * 1e-6) / 1e12,
+            "roofline": roof, "clocks": clk,
+            "e2e": {"value": e2e_us, "unit": UNIT,
+                    "h2d_bytes_per_step": int(qn_h.numel() * 2 + qp_h.numel() * 2),
+                    "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()
+                                              + lse_h.numel() * 4)},
+            "gpu_launches": 2 * args.steps,
+            "wall_s_timed": wall, "plan_us": plan_us,
+            "kernel": info["kernel"], "plan": info,
+            "step_us_p10_p50_p90": [float(np.percentile(step_ms, q) * 1000) for q in (10, 50, 90)]}
+    if not args.no_cpu_baseline and world == 1:
+        us, n, secs = oracle_sample(x, args.cpu_budget)
+        line["cpu_baseline"] = {"value": us, "unit": UNIT, "cores": os.cpu_count(),
+                                "kind": "oracle",
+                                "sample": f"{n} of {x.batch} requests ({secs:.1f}s float64 numpy), "
+                                          f"scaled to the batch by token count"}
+    print(json.dumps(line), flush=True)
+    dec.close()
+
+
+if __name__ == "__main__":
+    main()

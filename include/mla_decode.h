@@ -1,0 +1,211 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) paged MLA decode library.
+ *
+ * Operation (absorbed multi-head latent attention, decode, one query token):
+ * every token of the paged cache holds ONE latent KV head, a ckv row of width
+ * head_dim_ckv = kv_lora_rank = 512 and a kpe row of width head_dim_kpe =
+ * qk_rope_head_dim = 64.  For request b, head h:
+ *
+ *   s_i        = sm_scale * (q_nope[b,h] . ckv_i + q_pe[b,h] . kpe_i)
+ *   out[b,h,:] = sum_i softmax(s)_i * ckv_i          (width 512)
+ *   lse[b,h]   = ln sum_i exp(s_i)                    (natural log)
+ *
+ * over the kv_len[b] tokens of the request, with no causal mask.
+ *
+ * The plan/run split and the plan arguments (head_dim_ckv, head_dim_kpe,
+ * page_size, causal=False, sm_scale), the single KV head of MLA and the
+ * host-side paging arrays come from "[WIP] support flashinfer_mla"
+ * (vLLM-metax PR #113), code-review comments on the decode_wrapper.plan(...)
+ * call and on the paged_kv_indptr_cpu / paged_kv_len_arr_cpu slices.
+ * CUDA-graph capture of the run step is the concern raised in "[WIP][Kernel]
+ * Flashinfer MLA support" (vLLM PR #13630): mla_decode_run allocates nothing,
+ * never synchronises and reads no host memory, so it can be captured.
+ * A KV cache whose dtype differs from the query dtype (fp8 cache, bf16
+ * queries) is the limitation noted in "[V1][Core] FlashInfer attention backend
+ * for V1" (vLLM PR #14061), "Current limitations".
+ *
+ * Errors: every call returns a status code.  No call throws, exits or traps,
+ * and there is no silent fallback: an unsupported request is an error.
+ * The text of the last error of a plan is kept by mla_plan_last_error().
+ *
+ * Threading: a plan is not thread-safe; use one plan per host thread.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mla_plan_s* mla_plan_t;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,    /* inconsistent or malformed arguments */
+  MLA_ERR_UNSUPPORTED = 2,    /* well-formed but not supported (dims, page size, dtype) */
+  MLA_ERR_CAPACITY = 3,       /* exceeds what the plan was created for */
+  MLA_ERR_CUDA = 4,           /* a CUDA runtime call failed; see mla_plan_last_error */
+  MLA_ERR_DEVICE_TIMEOUT = 5, /* a bounded wait inside a kernel ran out */
+  MLA_ERR_DEVICE_BOUNDS = 6,  /* a kernel saw a page id outside [0, num_pages) */
+  MLA_ERR_NOT_PLANNED = 7     /* mla_decode_run before a successful mla_decode_plan */
+} mla_status_t;
+
+typedef enum {
+  MLA_DTYPE_BF16 = 0,
+  MLA_DTYPE_FP8_E4M3 = 1,     /* OCP E4M3 ("e4m3fn"), value = code * kv_scale */
+  MLA_DTYPE_FP32 = 2
+} mla_dtype_t;
+
+typedef enum {
+  MLA_KERNEL_DEFAULT = 0,     /* the tcgen05 / TMEM kernel */
+  MLA_KERNEL_TCGEN05 = 1,     /* same as DEFAULT, named explicitly */
+  MLA_KERNEL_MMA_SYNC = 2     /* warp-level mma.sync kernel (legacy tensor path, for comparison) */
+} mla_kernel_t;
+
+/* Plan statistics, filled by mla_plan_info. */
+typedef struct {
+  int32_t num_sms;            /* SMs of the plan's device */
+  int32_t num_workers;        /* persistent workers (CTA pairs for tcgen05, CTAs for mma.sync) */
+  int32_t num_units;          /* work units (contiguous tile ranges of one request) */
+  int32_t num_partial_slots;  /* split partial results written to the workspace */
+  int32_t num_merge;          /* requests combined by the merge kernel (incl. empty requests) */
+  int32_t total_tiles;        /* KV tiles (of tile_tokens tokens) over the batch */
+  int32_t batch;
+  int32_t num_heads;
+  int32_t page_size;
+  int32_t kernel;             /* mla_kernel_t actually used */
+  int32_t tile_tokens;        /* token granularity of the split (32 tcgen05, 64 mma.sync) */
+  int64_t workspace_bytes;    /* device bytes owned by the plan */
+} mla_plan_info_t;
+
+/*
+ * Create a plan on the CURRENT CUDA device.  Allocates (once, here) the
+ * work-unit buffers, the merge map and the split-KV partial workspace sized
+ * for up to max_batch requests of num_heads heads, so later plans and runs
+ * never allocate.  num_heads in 1..128.  kernel: an mla_kernel_t.
+ * On success *out receives the plan; the caller releases it with
+ * mla_plan_destroy.  Returns MLA_ERR_INVALID_ARG for bad sizes,
+ * MLA_ERR_CUDA when there is no device or an allocation fails.
+ */
+mla_status_t mla_plan_create(int max_batch, int num_heads, int kernel, mla_plan_t* out);
+
+/*
+ * Plan one decode batch (host work + one async upload on `stream`).
+ *   kv_indptr_host [batch+1] int32, HOST: CSR offsets into kv_indices, in pages;
+ *                  kv_indptr[0] = 0, non-decreasing.
+ *   kv_indices_dev [kv_indptr[batch]] int32, DEVICE: page ids.  Borrowed, not
+ *                  copied: it must stay allocated, at the same address, until the
+ *                  last run of this plan.  Its contents may change between runs.
+ *   kv_len_host    [batch] int32, HOST: tokens per request, >= 0, with
+ *                  kv_indptr[b+1]-kv_indptr[b] == ceil(kv_len[b]/page_size).
+ *                  A request with kv_len 0 gets out = 0, lse = -inf.
+ *   num_heads      must equal the plan's num_heads.
+ *   head_dim_ckv   must be 512, head_dim_kpe must be 64 (else MLA_ERR_UNSUPPORTED;
+ *                  this rejects e.g. passing the KV-head count as head_dim_ckv).
+ *   page_size      16, 32 or 64 tokens.
+ *   sm_scale       finite softmax scale applied to q.k.
+ *   stream         cudaStream_t (may be NULL = legacy default stream).
+ * The host arrays are read before the call returns.  Re-planning reuses the
+ * plan's buffers; a run already queued on `stream` sees the old plan.
+ */
+mla_status_t mla_decode_plan(mla_plan_t plan, const int32_t* kv_indptr_host,
+                             const int32_t* kv_indices_dev, const int32_t* kv_len_host,
+                             int batch, int num_heads, int head_dim_ckv, int head_dim_kpe,
+                             int page_size, float sm_scale, void* stream);
+
+/*
+ * Run the planned batch on `stream`.  All tensor arguments are DEVICE pointers
+ * to contiguous row-major arrays owned by the caller:
+ *   q_nope    [batch, num_heads, 512]   q_dtype (MLA_DTYPE_BF16 only)
+ *   q_pe      [batch, num_heads, 64]    q_dtype
+ *   ckv_cache [num_pages, page_size, 512]  kv_dtype (BF16 or FP8_E4M3), 16-byte aligned
+ *   kpe_cache [num_pages, page_size, 64]   kv_dtype, 16-byte aligned
+ *   kv_scale  per-tensor dequantisation scale of the cache (use 1.0 for bf16)
+ *   out       [batch, num_heads, 512]   out_dtype (BF16 or FP32)
+ *   lse       [batch, num_heads]        fp32, natural log
+ * Launches the decode kernel and, when some request was split, the merge
+ * kernel.  No allocation, no synchronisation, no host reads: capturable in a
+ * CUDA graph (the graph keeps the pointers; re-planning with the same plan
+ * between replays is allowed).  A page id outside [0, num_pages) found by the
+ * kernel is recorded and reported by mla_plan_check_status; that page is read
+ * as zeros.
+ */
+mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_pe,
+                            int q_dtype, const void* ckv_cache, const void* kpe_cache,
+                            int kv_dtype, float kv_scale, int num_pages, void* out,
+                            int out_dtype, float* lse, void* stream);
+
+/*
+ * One whole decode step from HOST buffers: copies q_nope / q_pe from host to
+ * plan-owned device staging buffers, runs, copies out / lse back to host and
+ * synchronises `stream`.  The KV cache stays device-resident (device
+ * pointers, as for mla_decode_run).  Pinned host memory gives the fastest
+ * copies.  The staging buffers are allocated on the first call (so this call
+ * is not graph-capturable) and kept by the plan.  Sizes and dtypes as for
+ * mla_decode_run.
+ */
+mla_status_t mla_decode_run_host(mla_plan_t plan, const void* q_nope_host,
+                                 const void* q_pe_host, int q_dtype, const void* ckv_cache,
+                                 const void* kpe_cache, int kv_dtype, float kv_scale,
+                                 int num_pages, void* out_host, int out_dtype,
+                                 float* lse_host, void* stream);
+
+/*
+ * Synchronise the device, then read and clear the plan's device error word.
+ * Returns MLA_OK, MLA_ERR_DEVICE_TIMEOUT or MLA_ERR_DEVICE_BOUNDS (the first
+ * error a kernel recorded since the last check), or MLA_ERR_CUDA.
+ */
+mla_status_t mla_plan_check_status(mla_plan_t plan);
+
+/*
+ * Profiling hook: when set (non-NULL cudaEvent_t handles created by the
+ * caller on the plan's device), every mla_decode_run records start_event on
+ * its stream immediately before the decode kernel and stop_event immediately
+ * after it (before the merge kernel), so the caller can time the decode
+ * kernel alone with cudaEventElapsedTime.  Pass NULLs to stop recording.
+ * The events are borrowed; they must outlive the runs that record them.
+ */
+mla_status_t mla_plan_set_profile_events(mla_plan_t plan, void* start_event, void* stop_event);
+
+/* Fill *info with the current plan's statistics. */
+mla_status_t mla_plan_info(mla_plan_t plan, mla_plan_info_t* info);
+
+/* Release every buffer of the plan (synchronises the device first). NULL is a no-op. */
+mla_status_t mla_plan_destroy(mla_plan_t plan);
+
+/* Static text for a status code. */
+const char* mla_status_string(mla_status_t status);
+
+/* Text of the plan's last error ("" if none).  Valid until the next call on the plan. */
+const char* mla_plan_last_error(mla_plan_t plan);
+
+/*
+ * Host-only planner, exposed for inspection and testing (no CUDA call).
+ * Validates the batch exactly as mla_decode_plan does and splits the
+ * tile_tokens-token tiles of the batch (tile_tokens 32 or 64, else
+ * MLA_ERR_UNSUPPORTED) into num_workers contiguous, balanced ranges.
+ * Outputs (caller-allocated host arrays; pass capacities):
+ *   units  [units_cap * 6] int32: per unit {req, tok_begin, tok_end,
+ *          out_slot (-1 = final output), page_base (= kv_indptr[req]), kv_len};
+ *          tok_begin is a multiple of tile_tokens, tok_end <= kv_len
+ *   worker_ptr [num_workers + 1] int32: units of worker w are
+ *          units[worker_ptr[w] .. worker_ptr[w+1])
+ *   merge  [merge_cap * 3] int32: per merged request {req, first_slot, n_slots}
+ *          (n_slots = 0 for an empty request: out = 0, lse = -inf)
+ *   counts [3] int32: {num_units, num_partial_slots, num_merge}
+ * Returns MLA_ERR_CAPACITY when units_cap or merge_cap is too small.
+ */
+mla_status_t mla_plan_partition_host(const int32_t* kv_indptr_host, const int32_t* kv_len_host,
+                                     int batch, int head_dim_ckv, int head_dim_kpe,
+                                     int page_size, float sm_scale, int num_workers,
+                                     int tile_tokens, int32_t* units, int units_cap,
+                                     int32_t* worker_ptr,
+                                     int32_t* merge, int merge_cap, int32_t* counts);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H */

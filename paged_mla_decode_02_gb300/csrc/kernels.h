@@ -1,0 +1,56 @@
+// Kernel arguments and host launchers (internal).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "mla_internal.h"
+
+namespace mla {
+
+struct DecodeArgs {
+  const void* q_nope;          // [B,H,512] bf16
+  const void* q_pe;            // [B,H,64] bf16
+  const void* ckv;             // [num_pages,P,512] bf16 or e4m3
+  const void* kpe;             // [num_pages,P,64]
+  const int32_t* kv_indices;   // page ids
+  const WorkUnit* units;
+  const int32_t* worker_ptr;   // [n_workers+1]
+  const PlanDev* params;
+  void* out;                   // [B,H,512] bf16 or fp32
+  float* lse;                  // [B,H]
+  float* o_part;               // [slots,H,512] fp32
+  float* lse_part;             // [slots,H]
+  int32_t* err;
+  int num_pages;
+  int num_heads;
+  float kv_scale;
+  int units_cap;
+  int n_workers;
+};
+
+struct MergeArgs {
+  const MergeEntry* merge;
+  const PlanDev* params;
+  const float* o_part;
+  const float* lse_part;
+  void* out;
+  float* lse;
+  int num_heads;
+  int merge_cap;
+};
+
+// Legacy warp-level tensor path (mma.sync m16n8k16): one CTA per (unit, 16-head group).
+cudaError_t launch_decode_mma(const DecodeArgs& a, bool kv_fp8, bool out_f32, cudaStream_t s);
+
+// tcgen05 / TMEM path: persistent CTA pairs, one per worker.
+struct TcMaps {
+  CUtensorMap q_nope, q_pe, ckv, kpe;
+};
+cudaError_t launch_decode_tc(const DecodeArgs& a, const TcMaps& maps, bool out_f32,
+                             cudaStream_t s);
+
+// LSE merge of split partials (and zero-fill of empty requests).
+cudaError_t launch_merge(const MergeArgs& a, bool out_f32, cudaStream_t s);
+
+}  // namespace mla
