@@ -23,7 +23,6 @@ import json
 import math
 import os
 import statistics
-import subprocess
 import sys
 import time
 
@@ -91,43 +90,52 @@ def oracle_sample(x, budget_s: float):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason sampling during the timed region."""
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """SM clock and throttle reasons sampled through NVML (read-only queries)
+    by a background thread, as fast as NVML answers, during the timed region."""
+    REASONS = {0x8: "hw_slowdown", 0x40: "hw_thermal_slowdown", 0x20: "sw_thermal_slowdown",
+               0x4: "sw_power_cap"}
 
     def __init__(self, index: int):
-        self.proc = None
+        import ctypes
+        import threading
+        self.samples, self.reasons, self.max_mhz, self.err = [], 0, None, None
+        self._stop = threading.Event()
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
-            self.proc = None
+            nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            nvml.nvmlInit_v2()
+            h = ctypes.c_void_p()
+            nvml.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(h))
+            mx = ctypes.c_uint()
+            if nvml.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:   # NVML_CLOCK_SM
+                self.max_mhz = mx.value
+            self._nvml, self._h = nvml, h
+        except Exception as e:  # no driver library: report it, do not fail the bench
+            self._nvml, self.err = None, str(e)
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+
+    def _run(self):
+        import ctypes
+        if self._nvml is None:
+            return
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            if self._nvml.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if self._nvml.nvmlDeviceGetCurrentClocksEventReasons(self._h, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(0.0005)
 
     def stop(self) -> dict:
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        out, _ = self.proc.communicate(timeout=10)
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
-            f = [v.strip() for v in line.split(",")]
-            if len(f) < 8:
-                continue
-            try:
-                sm.append(float(f[0]))
-                smax.append(float(f[1]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+        self._stop.set()
+        self._t.join(timeout=5)
+        names = sorted(n for bit, n in self.REASONS.items() if self.reasons & bit)
+        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+               "sm_max_mhz": self.max_mhz, "samples": len(self.samples), "reasons": names,
+               "source": "nvml"}
+        if self.err:
+            out["error"] = self.err
+        return out
 
 
 def dist_env():

@@ -78,6 +78,37 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P values stay below 2^8
 
+__device__ __forceinline__ float tree_max32(const float (&v)[32]) {
+  float t[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t[j] = fmaxf(v[j], v[j + 16]);
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) t[j] = fmaxf(t[j], t[j + w]);
+  return t[0];
+}
+__device__ __forceinline__ float tree_min32(const float (&v)[32]) {
+  float t[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t[j] = fminf(v[j], v[j + 16]);
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) t[j] = fminf(t[j], t[j + w]);
+  return t[0];
+}
+__device__ __forceinline__ float tree_sum32(const float (&v)[32]) {
+  float t[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t[j] = v[j] + v[j + 16];
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) t[j] = t[j] + t[j + w];
+  return t[0];
+}
+
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) {
   return base + kOffBar + 8 * i;
 }
@@ -156,114 +187,124 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
   if (warp == 0) {
-    // ================= producer =================
-    if (lane == 0) {
-      const int P = prm.page_size;
-      const int box = P < kT ? P : kT;
-      int g = 0, uidx = 0;
-      bool ok = true;
-      for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
-        const WorkUnit u = a.units[ui];
-        if (uidx > 0 && !(ok = mbar_wait(bar_addr(base, kQEmpty), (uidx - 1) & 1, abort_flag))) break;
-        mbar_arrive_expect_tx(bar_addr(base, kQFull), 4 * H * 128);
-        for (int j = 0; j < 4; ++j)
-          tma_load_2d(base + kOffQ + j * kPanelQ, &maps.q_nope, 64 * j, u.req * H,
-                      bar_addr(base, kQFull));
-        for (int tok0 = u.tok_begin; tok0 < u.tok_end; tok0 += kT, ++g) {
-          const int st = g % kStages;
-          if (!(ok = mbar_wait(bar_addr(base, kKvEmpty0 + st), ((g / kStages) & 1) ^ 1, abort_flag)))
-            break;
-          int rows[2];
-          int nbox = 0;
-          for (int t = tok0; t < tok0 + kT && t < u.tok_end; t += box) {
-            int page = a.kv_indices[u.page_base + t / P];
-            if (page < 0 || page >= a.num_pages) {
-              report_error(a.err, kErrBounds);
-              page = 0;
-            }
-            rows[nbox++] = page * P + (t % P);
+    // ================= producer (whole warp, converged) =================
+    const int P = prm.page_size;
+    const int box = P < kT ? P : kT;
+    int g = 0, uidx = 0;
+    bool ok = true;
+    for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
+      const WorkUnit u = a.units[ui];
+      if (uidx > 0 && !(ok = mbar_wait_warp(bar_addr(base, kQEmpty), (uidx - 1) & 1, abort_flag)))
+        break;
+      if (lane == 0) mbar_arrive_expect_tx(bar_addr(base, kQFull), 4 * H * 128);
+      __syncwarp();
+      if (lane < 4)
+        tma_load_2d(base + kOffQ + lane * kPanelQ, &maps.q_nope, 64 * lane, u.req * H,
+                    bar_addr(base, kQFull));
+      for (int tok0 = u.tok_begin; tok0 < u.tok_end; tok0 += kT, ++g) {
+        const int st = g % kStages;
+        if (!(ok = mbar_wait_warp(bar_addr(base, kKvEmpty0 + st), ((g / kStages) & 1) ^ 1,
+                                  abort_flag)))
+          break;
+        // lane l issues panel l % 9 of box l / 9 (a box = one page's rows of the tile)
+        const int nbox = min(kT / box, (u.tok_end - tok0 + box - 1) / box);
+        const int b = lane / 9, j = lane % 9;
+        int row = 0;
+        if (b < nbox) {
+          const int t = tok0 + b * box;
+          int page = a.kv_indices[u.page_base + t / P];
+          if (page < 0 || page >= a.num_pages) {
+            if (j == 0) report_error(a.err, kErrBounds);
+            page = 0;
           }
-          const uint32_t full = bar_addr(base, kKvFull0 + st);
-          mbar_arrive_expect_tx(full, nbox * 9 * box * 128);
-          const uint32_t dst = base + kOffKV + st * kStageBytes;
-          for (int b = 0; b < nbox; ++b) {
-            for (int j = 0; j < 8; ++j)
-              tma_load_2d(dst + j * kPanelKV + b * box * 128, &maps.ckv, 64 * j, rows[b], full);
-            tma_load_2d(dst + 8 * kPanelKV + b * box * 128, &maps.kpe, 0, rows[b], full);
-          }
+          row = page * P + (t % P);
+        }
+        const uint32_t full = bar_addr(base, kKvFull0 + st);
+        if (lane == 0) mbar_arrive_expect_tx(full, nbox * 9 * box * 128);
+        __syncwarp();
+        if (b < nbox) {
+          const uint32_t dst = base + kOffKV + st * kStageBytes + j * kPanelKV + b * box * 128;
+          if (j < 8)
+            tma_load_2d(dst, &maps.ckv, 64 * j, row, full);
+          else
+            tma_load_2d(dst, &maps.kpe, 0, row, full);
         }
       }
-      if (!ok) report_error(a.err, kErrTimeout);
-      // Drain: every copy this thread issued has landed before the CTA exits.
+    }
+    if (!ok && lane == 0) report_error(a.err, kErrTimeout);
+    // Drain: every copy this warp issued has landed before the CTA exits.
+    if (lane == 0)
       for (int k = 1; k <= kStages && k <= g; ++k) {
         const int gg = g - k;
         mbar_wait_drain(bar_addr(base, kKvFull0 + gg % kStages), (gg / kStages) & 1);
       }
-    }
+    __syncwarp();
   } else if (warp == 1) {
-    // ================= MMA issuer =================
-    if (lane == 0) {
-      constexpr uint32_t id_qk = idesc_bf16_f32(128, kT, false, false);
-      constexpr uint32_t id_pv = idesc_bf16_f32(128, 256, false, true);
-      const uint32_t p_addr = base + kOffP;
-      int g = 0, uidx = 0;
-      bool ok = true;
-      auto pv = [&](int gg, bool first, int ux) -> bool {
-        if (!mbar_wait(bar_addr(base, kPFull), gg & 1, abort_flag)) return false;
-        if (first && ux > 0 && !mbar_wait(bar_addr(base, kOFree), (ux - 1) & 1, abort_flag))
-          return false;
-        tc_fence_after();
-        const uint32_t v = base + kOffKV + (gg % kStages) * kStageBytes + 4 * half * kPanelKV;
+    // ================= MMA issuer (whole warp, converged; lane 0 issues) =================
+    constexpr uint32_t id_qk = idesc_bf16_f32(128, kT, false, false);
+    constexpr uint32_t id_pv = idesc_bf16_f32(128, 256, false, true);
+    const uint32_t issue = lane == 0;
+    const uint64_t q_desc0 = smem_desc(base + kOffQ, 16, 1024, kSw128);
+    const uint64_t kv_desc0 = smem_desc(base + kOffKV, 16, 1024, kSw128);
+    const uint64_t p_desc0 = smem_desc(base + kOffP, 16, 512, kSw64);
+    const uint64_t v_desc0 = smem_desc(base + kOffKV + 4 * half * kPanelKV, kPanelKV, 1024, kSw128);
+    int g = 0, uidx = 0;
+    bool ok = true;
+    auto pv = [&](int gg, bool first, int ux) -> bool {
+      if (!mbar_wait_warp(bar_addr(base, kPFull), gg & 1, abort_flag)) return false;
+      if (first && ux > 0 && !mbar_wait_warp(bar_addr(base, kOFree), (ux - 1) & 1, abort_flag))
+        return false;
+      tc_fence_after();
+      const uint64_t vdesc = v_desc0 + static_cast<uint64_t>(((gg % kStages) * kStageBytes) >> 4);
 #pragma unroll
-        for (int k = 0; k < kT / 16; ++k) {
-          const uint64_t ad = smem_desc(p_addr + k * 32, 16, 512, kSw64);
-          const uint64_t bd = smem_desc(v + k * 2048, kPanelKV, 1024, kSw128);
-          mma_ss(tmem + kColO, ad, bd, id_pv, (first && k == 0) ? 0u : 1u);
-        }
-        mma_commit(bar_addr(base, kKvEmpty0 + gg % kStages));
-        mma_commit(bar_addr(base, kPvDone));
-        return true;
-      };
-      for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
-        const WorkUnit u = a.units[ui];
-        const int n = (u.tok_end - u.tok_begin + kT - 1) / kT;
-        if (!(ok = mbar_wait(bar_addr(base, kQFull), uidx & 1, abort_flag) &&
-                   mbar_wait(bar_addr(base, kQTmemFull), uidx & 1, abort_flag)))
+      for (int k = 0; k < kT / 16; ++k)
+        mma_ss(tmem + kColO, p_desc0 + static_cast<uint64_t>((k * 32) >> 4),
+               vdesc + static_cast<uint64_t>((k * 2048) >> 4), id_pv, (first && k == 0) ? 0u : 1u,
+               issue);
+      mma_commit(bar_addr(base, kKvEmpty0 + gg % kStages), issue);
+      mma_commit(bar_addr(base, kPvDone), issue);
+      return true;
+    };
+    for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
+      const WorkUnit u = a.units[ui];
+      const int n = (u.tok_end - u.tok_begin + kT - 1) / kT;
+      if (!(ok = mbar_wait_warp(bar_addr(base, kQFull), uidx & 1, abort_flag) &&
+                 mbar_wait_warp(bar_addr(base, kQTmemFull), uidx & 1, abort_flag)))
+        break;
+      tc_fence_after();
+      for (int i = 0; i < n; ++i, ++g) {
+        const int st = g % kStages, sb = g & 1;
+        if (!(ok = mbar_wait_warp(bar_addr(base, kKvFull0 + st), (g / kStages) & 1, abort_flag) &&
+                   mbar_wait_warp(bar_addr(base, kSFree0 + sb), ((g >> 1) & 1) ^ 1, abort_flag)))
           break;
         tc_fence_after();
-        for (int i = 0; i < n; ++i, ++g) {
-          const int st = g % kStages, sb = g & 1;
-          if (!(ok = mbar_wait(bar_addr(base, kKvFull0 + st), (g / kStages) & 1, abort_flag) &&
-                     mbar_wait(bar_addr(base, kSFree0 + sb), ((g >> 1) & 1) ^ 1, abort_flag)))
-            break;
-          tc_fence_after();
-          const uint32_t kv = base + kOffKV + st * kStageBytes;
-          const uint32_t d = tmem + kColS + 32 * sb;
-#pragma unroll 1
-          for (int j = 0; j < 9; ++j) {
+        // descriptors differ only in their start-address field: add (offset >> 4)
+        const uint64_t bdesc = kv_desc0 + static_cast<uint64_t>((st * kStageBytes) >> 4);
+        const uint32_t d = tmem + kColS + 32 * sb;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t bd = smem_desc(kv + j * kPanelKV + kk * 32, 16, 1024, kSw128);
-              const uint32_t acc = (j | kk) != 0;
-              if (j < 4) {
-                const uint64_t ad = smem_desc(base + kOffQ + j * kPanelQ + kk * 32, 16, 1024, kSw128);
-                mma_ss(d, ad, bd, id_qk, acc);
-              } else {
-                mma_ts(d, tmem + kColQ + (j - 4) * 32 + kk * 8, bd, id_qk, acc);
-              }
-            }
-          }
-          mma_commit(bar_addr(base, kSFull0 + sb));
-          if (i == n - 1) mma_commit(bar_addr(base, kQEmpty));
-          if (i > 0 && !(ok = pv(g - 1, i == 1, uidx))) break;
-        }
-        if (ok && n > 0) ok = pv(g - 1, n == 1, uidx);
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(d, q_desc0 + static_cast<uint64_t>((j * kPanelQ + kk * 32) >> 4),
+                   bdesc + static_cast<uint64_t>((j * kPanelKV + kk * 32) >> 4), id_qk,
+                   (j | kk) != 0, issue);
+#pragma unroll
+        for (int j = 4; j < 9; ++j)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(d, tmem + kColQ + (j - 4) * 32 + kk * 8,
+                   bdesc + static_cast<uint64_t>((j * kPanelKV + kk * 32) >> 4), id_qk, 1u, issue);
+        mma_commit(bar_addr(base, kSFull0 + sb), issue);
+        if (i == n - 1) mma_commit(bar_addr(base, kQEmpty), issue);
+        if (i > 0 && !(ok = pv(g - 1, i == 1, uidx))) break;
       }
-      if (!ok) report_error(a.err, kErrTimeout);
-      // Drain: all MMAs issued by this thread complete before TMEM is freed.
-      mma_commit(bar_addr(base, kFinal));
-      mbar_wait_drain(bar_addr(base, kFinal), 0);
+      if (ok && n > 0) ok = pv(g - 1, n == 1, uidx);
     }
+    if (!ok && lane == 0) report_error(a.err, kErrTimeout);
+    // Drain: all MMAs issued by this warp complete before TMEM is freed.
+    mma_commit(bar_addr(base, kFinal), issue);
+    if (lane == 0) mbar_wait_drain(bar_addr(base, kFinal), 0);
+    __syncwarp();
   } else {
     // ================= softmax / epilogue (warps 2..5) =================
     const int quad = warp & 3;
@@ -287,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -INFINITY, lr = 0.f, lx = 0.f;
       for (int i = 0; i < n; ++i, ++g) {
         const int sb = g & 1;
-        if (!(ok = mbar_wait(bar_addr(base, kSFull0 + sb), (g >> 1) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(bar_addr(base, kSFull0 + sb), (g >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         uint32_t sr[32];
         tmem_ld32(lane_addr + kColS + 32 * sb, sr);
@@ -297,32 +338,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar_addr(base, kSFree0 + sb));
 
         const int valid = min(kT, u.tok_end - (u.tok_begin + i * kT));
-        float x[32];
-        float mx = -INFINITY;
+        // exponent of token j: s_j * c - m, one FFMA.  For c >= 0 the tile max
+        // of s_j * c is c * max s_j (c < 0: c * min s_j).
+        float sv[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          x[j] = j < valid ? __uint_as_float(sr[j]) * c : -INFINITY;
-          mx = fmaxf(mx, x[j]);
+        for (int j = 0; j < 32; ++j) sv[j] = __uint_as_float(sr[j]);
+        float mx;
+        if (valid == kT) {
+          mx = c >= 0.f ? c * tree_max32(sv) : c * tree_min32(sv);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j >= valid) sv[j] = c >= 0.f ? -INFINITY : INFINITY;
+          mx = c >= 0.f ? c * tree_max32(sv) : c * tree_min32(sv);
         }
         const bool move = mx > m + kRescaleThreshold;
         const float m_new = move ? mx : m;
         const float alpha = move ? exp2f(m - m_new) : 1.f;
-        float sx = 0.f, sr16 = 0.f;
+        float ex[32], er[32];
         uint32_t pk[16];
 #pragma unroll
+        for (int j = 0; j < 32; ++j) ex[j] = exp2f(fmaf(sv[j], c, -m_new));
+        if (valid < kT) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j >= valid) ex[j] = 0.f;        // masked tokens (also when c == 0)
+        }
+#pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float e0 = exp2f(x[2 * j] - m_new), e1 = exp2f(x[2 * j + 1] - m_new);
-          sx += e0 + e1;
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(e0, e1);
-          sr16 += __bfloat162float(b2.x) + __bfloat162float(b2.y);
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex[2 * j], ex[2 * j + 1]);
+          er[2 * j] = __low2float(b2);
+          er[2 * j + 1] = __high2float(b2);
           pk[j] = *reinterpret_cast<const uint32_t*>(&b2);
         }
+        const float sx = tree_sum32(ex), sr16 = tree_sum32(er);
         lx = lx * alpha + sx;
         lr = lr * alpha + sr16;
         m = m_new;
 
         // P buffer and O are free once PV of the previous tile completed.
-        if (i > 0 && !(ok = mbar_wait(bar_addr(base, kPvDone), (g - 1) & 1, abort_flag))) break;
+        if (i > 0 && !(ok = mbar_wait_warp(bar_addr(base, kPvDone), (g - 1) & 1, abort_flag))) break;
         tc_fence_after();
         if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
@@ -364,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // ---- epilogue ----
-      if (!(ok = mbar_wait(bar_addr(base, kPvDone), (g - 1) & 1, abort_flag))) break;
+      if (!(ok = mbar_wait_warp(bar_addr(base, kPvDone), (g - 1) & 1, abort_flag))) break;
       tc_fence_after();
       const bool partial = u.out_slot >= 0;
       const size_t orow = partial ? static_cast<size_t>(u.out_slot) * H + r

@@ -21,7 +21,7 @@ from paged_mla_decode_02_gb300 import mla
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ["mma_sync"]
+KERNELS = ["tcgen05", "mma_sync"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -82,6 +82,16 @@ def test_small_shapes(kernel, lens, heads, P):
 def test_sharp_softmax(kernel):
     # keys x3 as in the long-context workload: scores spread over ~+-15 sigma
     x = I.make_inputs("sharp", [3000, 129], 16, 64, seed=3, key_scale=3.0)
+    _check_all(x, kernel)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("sm_scale", [0.0, -0.05, 1.0 / 24.0])
+def test_degenerate_and_negative_scales(kernel, sm_scale):
+    # sm_scale 0: uniform weights (out = mean of the ckv rows, lse = ln L);
+    # a negative scale flips the ordering of the scores
+    x = I.make_inputs("scale", [45, 100, 7], 32, 16, seed=12, sm_scale=sm_scale, poison=True,
+                      slack_pages=2)
     _check_all(x, kernel)
 
 
