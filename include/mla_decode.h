@@ -76,7 +76,7 @@ typedef struct {
   int32_t num_heads;
   int32_t page_size;
   int32_t kernel;             /* mla_kernel_t actually used */
-  int32_t tile_tokens;        /* token granularity of the split (32 tcgen05, 64 mma.sync) */
+  int32_t tile_tokens;        /* token granularity of the split (128 tcgen05, 64 mma.sync) */
   int64_t workspace_bytes;    /* device bytes owned by the plan */
 } mla_plan_info_t;
 
@@ -184,7 +184,7 @@ const char* mla_plan_last_error(mla_plan_t plan);
 /*
  * Host-only planner, exposed for inspection and testing (no CUDA call).
  * Validates the batch exactly as mla_decode_plan does and splits the
- * tile_tokens-token tiles of the batch (tile_tokens 32 or 64, else
+ * tile_tokens-token tiles of the batch (tile_tokens 64 or 128, else
  * MLA_ERR_UNSUPPORTED) into num_workers contiguous, balanced ranges.
  * Outputs (caller-allocated host arrays; pass capacities):
  *   units  [units_cap * 6] int32: per unit {req, tok_begin, tok_end,

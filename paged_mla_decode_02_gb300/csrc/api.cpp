@@ -322,13 +322,13 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
                   "the tcgen05 kernel takes bf16 caches; use MLA_KERNEL_MMA_SYNC for fp8");
     TcMaps maps;
     const int H = plan->num_heads;
+    const int P = plan->params.page_size;
     const uint64_t qrows = static_cast<uint64_t>(plan->params.batch) * H;
-    const uint64_t kvrows = static_cast<uint64_t>(num_pages) * plan->params.page_size;
-    const uint32_t kv_box = plan->params.page_size < kTileTc ? plan->params.page_size : kTileTc;
+    const uint64_t kvrows = static_cast<uint64_t>(num_pages) * P;
     if (!encode_2d(&maps.q_nope, q_nope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qrows, kDCkv, H, 64) ||
-        !encode_2d(&maps.q_pe, q_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qrows, kDKpe, H, 64) ||
-        !encode_2d(&maps.ckv, ckv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDCkv, kv_box, 64) ||
-        !encode_2d(&maps.kpe, kpe_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDKpe, kv_box, 64))
+        !encode_2d(&maps.ckv_k, ckv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDCkv, P, 64) ||
+        !encode_2d(&maps.kpe_k, kpe_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDKpe, P, 64) ||
+        !encode_2d(&maps.ckv_v, ckv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDCkv, 16, 64))
       return fail(plan, MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     e = launch_decode_tc(a, maps, out_f32, s);
   }

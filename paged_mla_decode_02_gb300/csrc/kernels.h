@@ -45,7 +45,10 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, bool kv_fp8, bool out_f32, cu
 
 // tcgen05 / TMEM path: persistent CTA pairs, one per worker.
 struct TcMaps {
-  CUtensorMap q_nope, q_pe, ckv, kpe;
+  CUtensorMap q_nope;   // [B*H, 512] bf16, box 64 x H
+  CUtensorMap ckv_k;    // [pages*P, 512] bf16, box 64 x P (one page of a K panel)
+  CUtensorMap kpe_k;    // [pages*P, 64] bf16, box 64 x P
+  CUtensorMap ckv_v;    // [pages*P, 512] bf16, box 64 x 16 (a V chunk panel)
 };
 cudaError_t launch_decode_tc(const DecodeArgs& a, const TcMaps& maps, bool out_f32,
                              cudaStream_t s);

@@ -11,11 +11,11 @@ constexpr int kD = kDCkv + kDKpe;   // 576: contraction width of the scores
 constexpr int kMaxHeads = 128;
 
 // Token granularity of the split-KV partition for each kernel: a work unit
-// starts on a multiple of it.  Every supported page size (16, 32, 64) is
-// compatible with both (a tile never straddles a page partially except at
-// the end of a request).
+// starts on a multiple of it.  Every supported page size (16, 32, 64)
+// divides both, so a tile is a whole number of pages (the last page of a
+// request may be partially filled).
 constexpr int kTileMma = 64;        // mma.sync kernel: 64-token tiles
-constexpr int kTileTc = 32;         // tcgen05 kernel: 32-token tiles
+constexpr int kTileTc = 128;        // tcgen05 kernel: 128-token tiles
 
 // One contiguous token range of one request, processed by one worker.
 struct WorkUnit {

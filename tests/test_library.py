@@ -95,7 +95,7 @@ def _check_partition(lens, P, W, T):
     return units, merge
 
 
-@pytest.mark.parametrize("T", [32, 64])
+@pytest.mark.parametrize("T", [64, 128])
 @pytest.mark.parametrize("P", [16, 32, 64])
 def test_partition_random_batches(lib, T, P):
     rng = np.random.Generator(np.random.PCG64(7))
@@ -108,14 +108,14 @@ def test_partition_random_batches(lib, T, P):
 
 
 def test_partition_named_shapes(lib):
-    _check_partition([33, 70], 16, 76, 32)
-    _check_partition([4096] * 64, 64, 76, 32)
-    _check_partition([131072], 64, 76, 32)
-    _check_partition([0, 0, 5], 16, 3, 32)
+    _check_partition([33, 70], 16, 76, 128)
+    _check_partition([4096] * 64, 64, 76, 128)
+    _check_partition([131072], 64, 76, 128)
+    _check_partition([0, 0, 5], 16, 3, 128)
 
 
 def test_partition_long_request_split_over_all_workers(lib):
-    units, merge = _check_partition([131072], 64, 76, 32)
+    units, merge = _check_partition([131072], 64, 76, 128)
     assert len(units) == 76 and merge.shape[0] == 1 and merge[0, 2] == 76
 
 
@@ -125,11 +125,11 @@ def test_partition_long_request_split_over_all_workers(lib):
     (dict(page_size=8), mla.ERR_UNSUPPORTED),
     (dict(sm_scale=math.inf), mla.ERR_INVALID_ARG),
     (dict(sm_scale=math.nan), mla.ERR_INVALID_ARG),
-    (dict(tile_tokens=48), mla.ERR_UNSUPPORTED),
+    (dict(tile_tokens=32), mla.ERR_UNSUPPORTED),
 ])
 def test_partition_rejects_bad_arguments(lib, bad, status):
     indptr, lens = _batch([33, 70], 16)
-    kw = dict(head_dim_ckv=512, head_dim_kpe=64, page_size=16, sm_scale=0.1, tile_tokens=32)
+    kw = dict(head_dim_ckv=512, head_dim_kpe=64, page_size=16, sm_scale=0.1, tile_tokens=128)
     kw.update(bad)
     with pytest.raises(mla.MLAError) as ei:
         mla.mla_plan_partition_host(indptr, lens, 4, kw["tile_tokens"], kw["page_size"],
@@ -142,12 +142,12 @@ def test_partition_rejects_inconsistent_paging(lib):
     bad = indptr.copy()
     bad[1] += 1                                  # request 0 claims 4 pages for 33 tokens
     with pytest.raises(mla.MLAError) as ei:
-        mla.mla_plan_partition_host(bad, lens, 4, 32, 16)
+        mla.mla_plan_partition_host(bad, lens, 4, 128, 16)
     assert ei.value.status == mla.ERR_INVALID_ARG
     with pytest.raises(mla.MLAError) as ei:
-        mla.mla_plan_partition_host(indptr, np.array([33, -1], np.int32), 4, 32, 16)
+        mla.mla_plan_partition_host(indptr, np.array([33, -1], np.int32), 4, 128, 16)
     assert ei.value.status == mla.ERR_INVALID_ARG
     nz = indptr.copy()
     nz[0] = 1
     with pytest.raises(mla.MLAError):
-        mla.mla_plan_partition_host(nz, lens, 4, 32, 16)
+        mla.mla_plan_partition_host(nz, lens, 4, 128, 16)
