@@ -78,7 +78,7 @@ int workers_for(int kernel, int num_sms, int num_heads) {
     const int w = 2 * num_sms / head_groups;
     return w < 1 ? 1 : w;
   }
-  return num_sms / 2 < 1 ? 1 : num_sms / 2;   // one CTA pair per worker
+  return num_sms / 2 < 1 ? 1 : num_sms / 2;   // one 2-CTA cluster per worker
 }
 
 void release(mla_plan_t p) {
@@ -172,6 +172,15 @@ mla_status_t mla_plan_create(int max_batch, int num_heads, int kernel, mla_plan_
     return MLA_ERR_CUDA;
   }
   p->n_workers = workers_for(p->kernel, p->num_sms, num_heads);
+  if (p->kernel == MLA_KERNEL_TCGEN05) {
+    int resident = 0;
+    if ((e = decode_tc_max_workers(&resident)) != cudaSuccess || resident < 1) {
+      delete p;
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+    if (resident < p->n_workers) p->n_workers = resident;
+  }
   p->units_cap = max_units(p->n_workers, max_batch);
   p->slots_cap = max_slots(p->n_workers, max_batch);
   p->merge_cap = max_batch;

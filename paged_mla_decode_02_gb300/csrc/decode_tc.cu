@@ -11,40 +11,44 @@
 // O = P[H x T] . ckv[T x 512].
 //
 // Work decomposition.  A work unit (a token range of one request, from the
-// host planner) is processed by a PAIR of CTAs; CTA half h in {0, 1} owns the
-// output dims [256h, 256h + 256).  128 heads x 512 fp32 accumulators would
-// fill all 512 TMEM columns of an SM, so each CTA keeps O[:, its 256 dims]
-// in TMEM and both compute the full score tile S.  The grid is persistent:
-// one CTA pair per worker, each walking its units.
+// host planner) is processed by a cluster of two CTAs.  CTA `half` owns the
+// output dims [256 half, 256 half + 256): 128 heads x 512 fp32 accumulators
+// would fill all 512 TMEM columns of one SM.  The unit's 128-token tiles
+// alternate between the two CTAs: the owner of tile g (g odd or even) loads
+// its K, computes S = Q K^T and the softmax, and sends P (bf16) with the
+// tile's reference max and row sums to the other CTA through distributed
+// shared memory.  Both CTAs then accumulate P . V over their own 256 dims.
+// So every score tile is computed once, and each SM issues half the score
+// MMAs and half the softmax of a design where both CTAs compute S.
+// The grid is persistent: one cluster per worker, walking its units.
 //
-// Tiles are 128 tokens, so every score MMA is M=128 x N=128 x K=16 (a
-// tcgen05.mma instruction costs about as much for N=32 as for N=128, so
-// wide tiles keep the tensor pipe busy).  Per CTA (384 threads):
-//   warp 0      K producer: TMA loads of Q dims 0..319 (per unit) and of
-//               the 9 K panels (64 dims x 128 tokens, 16 KB) of every tile,
-//               gathered page by page through kv_indices into a 5-slot ring,
-//               after a contiguous L2 prefetch of the next tile's pages;
-//   warp 1      allocates TMEM; lane 0 issues the QK(t) MMAs, panel by
-//               panel, into S;
-//   warp 11     lane 0 issues the PV(t) MMAs, chunk by chunk, into O (two
-//               issuing warps keep the tensor pipe fed: a single warp can
-//               issue a tcgen05.mma only every ~80-100 cycles);
-//   warp 2      V producer: TMA loads of this CTA's 256 dims of ckv for PV,
-//               16 tokens (8 KB) at a time into a 4-slot ring (a second
-//               read of rows the K producer fetched shortly before, served
-//               from L2); rows past the end of a request are zeroed;
-//   warps 3..10 softmax / epilogue, two warps per 32 head rows (TMEM lane
-//               quadrant): each owns 64 of the 128 tokens of a tile (one P
-//               panel) and 128 of the 256 output dims.  S is drained from
-//               TMEM to registers at once (so QK(t+1) can start; each warp
-//               reads all 128 scores of its rows for the row max), online
-//               softmax in the exp2 domain with lazy
-//               rescaling (the reference max moves only when a tile's max
-//               exceeds it by more than 2^8), P to shared memory in bf16,
-//               O rescale in TMEM when needed, Q dims 320..575 into TMEM for
-//               the next unit, and the epilogue O / l, lse.
+// Per CTA (384 threads, 12 warps):
+//   warp 0      K producer (own tiles): TMA loads of Q dims 0..319 (per
+//               unit) and of the 9 K panels (64 dims x 128 tokens) of the
+//               tile, page by page through kv_indices, into a 2-slot ring;
+//   warp 1      allocates TMEM; lane 0 issues the QK MMAs (M=128 heads,
+//               N=128 tokens, K=16) of own tiles into S;
+//   warp 2      V producer (every tile): this CTA's 256 dims of ckv,
+//               16 tokens (8 KB) at a time into a 5-slot ring; rows past the
+//               end of a request are zeroed; also a contiguous L2 prefetch of
+//               the pages of the tile two ahead;
+//   warps 3..10 softmax: two warps per 32 head rows (TMEM lane quadrant),
+//               each owning 64 tokens of a tile (one P panel) and 128 of the
+//               256 output dims.  For an own tile: drain S, row max over the
+//               tile, lazy-rescaled exp2 (the reference max moves only when
+//               a tile's max exceeds it by more than 2^8), P to local and
+//               remote shared memory.  For every tile, in order: take its
+//               reference (own, or received), rescale O in TMEM when the
+//               reference moved, update the row sums, release it to PV.
+//               Then the epilogue O / l, lse;
+//   warp 11     lane 0 issues the PV MMAs (M=128, N=256 dims, K=16 tokens).
 // TMEM columns: O [0, 256) | S [256, 384) | Q dims 320..575 as bf16 pairs
 // [384, 512).
+//
+// Reference max of tile g (both CTAs use the same value): the owner takes
+// the lazy update of max(M[g-2], M[g-3]), the two latest references it has
+// already applied, so neither CTA's softmax waits on the other's.  O and the
+// row sums are kept relative to the reference of the last applied tile.
 //
 // Every wait is bounded (2 s); on expiry the kernel records
 // MLA_ERR_DEVICE_TIMEOUT, drains its own copies and MMAs, frees TMEM and
@@ -63,32 +67,47 @@ using namespace tc;
 
 constexpr int kT = kTileTc;                 // 128 tokens per tile
 constexpr int kThreads = 384;
-constexpr int kPvWarp = 11;
 constexpr int kSoftmaxWarps = 8;
+constexpr int kPvWarp = 11;
 constexpr int kPanel = 128 * 128;           // 128 rows x 128 B (one 64-dim panel)
-constexpr int kKSlots = 5;
-constexpr int kVSlots = 4;
-constexpr int kVChunkTok = 16;
-constexpr int kVPanel = kVChunkTok * 128;   // 2 KB: 16 rows x 64 dims
-constexpr int kVSlot = 4 * kVPanel;         // 8 KB: 16 rows x 256 dims
+constexpr int kKSlots = 3;
+constexpr int kVSlots = 3;
+constexpr int kVChunkTok = 32;              // tokens per V chunk: two PV MMAs
+constexpr int kVBox = 16;                   // rows per V copy (every page holds >= 16)
+constexpr int kVPanel = kVChunkTok * 128;   // 4 KB: 32 rows x 64 dims
+constexpr int kVSlot = 4 * kVPanel;         // 16 KB: 32 rows x 256 dims
 constexpr int kQSmemPanels = 5;             // Q dims 0..319 in shared memory
+// A tile's row info, per softmax warp: 32 heads x {ref max, lx, lr, -} (16 B);
+// laid out [token half][head] so each warp's block is contiguous.
+constexpr int kInfoRow = 16;
+constexpr int kInfoBytes = 2 * 128 * kInfoRow;
+constexpr int kRecvBytes = 2 * kPanel + kInfoBytes;   // P (both token halves) + info
 
 // shared memory map (offsets from the 1024-byte aligned base)
 constexpr int kOffQ = 0;
-constexpr int kOffP = kOffQ + kQSmemPanels * kPanel;   // P [128 x 128] bf16: 2 panels
+constexpr int kOffP = kOffQ + kQSmemPanels * kPanel;   // P [128 x 128] bf16 (2 panels)
 constexpr int kOffK = kOffP + 2 * kPanel;
 constexpr int kOffV = kOffK + kKSlots * kPanel;
-constexpr int kOffBar = kOffV + kVSlots * kVSlot;
+constexpr int kOffInfo = kOffV + kVSlots * kVSlot;     // received row info (the peer's tiles)
+constexpr int kOffInfoOut = kOffInfo + kInfoBytes;     // row info of own tiles, to send
+constexpr int kOffXchg = kOffInfoOut + kInfoBytes;     // 128 x (lx, lr) x 2 halves
+constexpr int kOffBar = kOffXchg + 128 * 16;
 constexpr int kBarBytes = 512;
 constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kOffBar % 8 == 0, "barrier alignment");
 
 enum Bar {
   kQFull = 0, kQTmemFull, kQEmpty,
   kKFull0, kKEmpty0 = kKFull0 + kKSlots,
   kVFull0 = kKEmpty0 + kKSlots, kVEmpty0 = kVFull0 + kVSlots, kVTail0 = kVEmpty0 + kVSlots,
-  kSFull = kVTail0 + kVSlots, kSFree, kPFull, kPvDone, kOFree, kFinal, kFinalPv,
-  kXchg0, kNumBars = kXchg0 + 4   // per TMEM lane quadrant: the two softmax warps' row sums
+  kSFull = kVTail0 + kVSlots, kSFree,
+  kPFree0,          // 2, by tile parity: both CTAs' PV of the tile done (P buffer reusable)
+  kPRecv = kPFree0 + 2,   // the peer's P and info for a tile it owns have landed
+  kPReady0,         // 2, by tile parity: tile released to PV (O rescaled, P in place)
+  kPvDone0 = kPReady0 + 2,   // 2, by tile parity: this CTA's PV of the tile completed
+  kOFree = kPvDone0 + 2, kFinal, kFinalPv,
+  kXchg0, kNumBars = kXchg0 + 4
 };
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
 
@@ -153,6 +172,8 @@ __device__ __forceinline__ void load_q_tmem(const DecodeArgs& a, int req, int r,
   tmem_st_wait();
 }
 
+__device__ __forceinline__ int tiles_of(const WorkUnit& u) { return (u.tok_end - u.tok_begin + kT - 1) / kT; }
+
 template <bool kOutF32>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ TcMaps maps) {
@@ -164,7 +185,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + kNumBars * 8 + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int worker = blockIdx.x >> 1, half = blockIdx.x & 1;
+  const int worker = blockIdx.x >> 1;
+  const int half = static_cast<int>(cluster_ctarank());   // == blockIdx.x & 1
+  const uint32_t peer = static_cast<uint32_t>(half ^ 1);
   const PlanDev prm = *a.params;
   const int H = a.num_heads;
   const int P = prm.page_size;
@@ -174,11 +197,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- setup ----
   if (threadIdx.x == 0) {
     *abort_flag = 0;
-    for (int i = 0; i < kNumBars; ++i)
-      mbar_init(bar_addr(base, i),
-                (i == kQTmemFull || i == kPFull || i == kOFree || i == kSFree) ? kSoftmaxWarps
-                : i >= kXchg0                                                   ? 2
-                                                                                : 1);
+    for (int i = 0; i < kNumBars; ++i) {
+      uint32_t cnt = 1;
+      if (i == kQTmemFull || i == kSFree || i == kPReady0 || i == kPReady0 + 1 || i == kOFree)
+        cnt = kSoftmaxWarps;
+      if (i == kPFree0 || i == kPFree0 + 1 || i >= kXchg0) cnt = 2;
+      mbar_init(bar_addr(base, i), cnt);
+    }
     fence_barrier_init();
   }
   if (warp >= 3 && warp < kPvWarp && H < 128) {
@@ -200,13 +225,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&maps.ckv_v);
   }
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();   // both CTAs' barriers initialised before any remote operation
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(tmem_slot);
 
   if (warp == 0) {
-    // ================= K producer =================
-    int kc = 0, uidx = 0;
+    // ================= K producer (own tiles) =================
+    int kc = 0, g = 0, uidx = 0;
     bool ok = true;
     for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
       const WorkUnit u = a.units[ui];
@@ -217,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane < kQSmemPanels)
         tma_load_2d(base + kOffQ + lane * kPanel, &maps.q_nope, 64 * lane, u.req * H,
                     bar_addr(base, kQFull));
-      for (int tok0 = u.tok_begin; tok0 < u.tok_end && ok; tok0 += kT) {
+      for (int tok0 = u.tok_begin; tok0 < u.tok_end && ok; tok0 += kT, ++g) {
+        if ((g & 1) != half) continue;
         // lane b < nbox owns page b of this tile (a box of P rows)
         const int nbox = (min(tok0 + kT, u.tok_end) - tok0 + P - 1) / P;
         int row = 0;
@@ -228,29 +254,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             page = 0;
           }
           row = page * P;
-        }
-        {
-          // The panels of a page are 128-byte slices of every 1 KB cache row;
-          // fetched panel by panel, DRAM would open each row eight times.
-          // Prefetch the next tile's pages whole (contiguous) into L2 instead,
-          // so the panel copies below hit L2.
-          int nu = ui, nt = tok0 + kT;
-          if (nt >= u.tok_end) {
-            nu = ui + 1;
-            nt = nu < u1 ? a.units[nu].tok_begin : 0;
-          }
-          if (nu < u1) {
-            const WorkUnit v = a.units[nu];
-            const int nb = (min(nt + kT, v.tok_end) - nt + P - 1) / P;
-            if (lane < nb) {
-              const int page = a.kv_indices[v.page_base + nt / P + lane];
-              if (page >= 0 && page < a.num_pages) {
-                const size_t slot_row = static_cast<size_t>(page) * P;
-                bulk_prefetch_l2(static_cast<const char*>(a.ckv) + slot_row * kDCkv * 2, P * kDCkv * 2);
-                bulk_prefetch_l2(static_cast<const char*>(a.kpe) + slot_row * kDKpe * 2, P * kDKpe * 2);
-              }
-            }
-          }
         }
         for (int j = 0; j < 9; ++j, ++kc) {
           const int slot = kc % kKSlots;
@@ -276,33 +279,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(bar_addr(base, kKFull0 + (kc - k) % kKSlots), ((kc - k) / kKSlots) & 1);
     __syncwarp();
   } else if (warp == 2) {
-    // ================= V producer (this CTA's 256 dims of ckv) =================
-    int vc = 0;
-    bool ok = true;
-    for (int ui = u0; ui < u1 && ok; ++ui) {
-      const WorkUnit u = a.units[ui];
-      for (int t = u.tok_begin; t < u.tok_end && ok; t += kVChunkTok, ++vc) {
-        const int slot = vc % kVSlots;
-        if (!(ok = mbar_wait_warp(bar_addr(base, kVEmpty0 + slot), ((vc / kVSlots) & 1) ^ 1,
-                                  abort_flag)))
-          break;
-        int page = a.kv_indices[u.page_base + t / P];
+    // ================= V producer (this CTA's 256 dims of ckv, every tile) =================
+    // The page ids of a tile are read once (lane b: page b), one tile ahead,
+    // so no chunk waits on a dependent load of kv_indices.
+    auto tile_pages = [&](int ui, int i) -> int {
+      const WorkUnit v = a.units[ui];
+      const int tok0 = v.tok_begin + i * kT;
+      const int nb = (min(tok0 + kT, v.tok_end) - tok0 + P - 1) / P;
+      int page = 0;
+      if (lane < nb) {
+        page = a.kv_indices[v.page_base + tok0 / P + lane];
         if (page < 0 || page >= a.num_pages) {
-          if (lane == 0) report_error(a.err, kErrBounds);
+          report_error(a.err, kErrBounds);
           page = 0;
         }
-        const int row = page * P + (t % P);
+      }
+      return page;
+    };
+    int vc = 0, vslot = 0;
+    uint32_t vphase = 0;   // parity of the current pass over the ring
+    bool ok = true;
+    int pg_cur = u0 < u1 ? tile_pages(u0, 0) : 0;
+    for (int ui = u0, i = 0; ui < u1 && ok;) {
+      const WorkUnit u = a.units[ui];
+      const int tok0 = u.tok_begin + i * kT;
+      // next tile in the flattened sequence of this worker's tiles
+      int ui2 = ui, i2 = i + 1;
+      if (i2 >= tiles_of(u)) {
+        ++ui2;
+        i2 = 0;
+      }
+      const int pg_next = ui2 < u1 ? tile_pages(ui2, i2) : 0;
+      for (int t = tok0; t < min(tok0 + kT, u.tok_end) && ok; t += kVChunkTok, ++vc) {
+        const int slot = vslot;
+        const uint32_t ph = vphase;
+        if (++vslot == kVSlots) {
+          vslot = 0;
+          vphase ^= 1;
+        }
+        if (!(ok = mbar_wait_warp(bar_addr(base, kVEmpty0 + slot), ph ^ 1, abort_flag))) break;
+        // lane l copies box (l >> 2) (16 rows) of panel (l & 3) (64 dims)
         const int rows = min(kVChunkTok, u.tok_end - t);
+        const int nbox = rows > kVBox ? 2 : 1;
+        const int bh = (lane >> 2) & 1;
+        const int tb = t + kVBox * bh;
+        const int page = __shfl_sync(0xffffffffu, pg_cur, min(tb, u.tok_end - 1) - tok0 < kT
+                                                               ? (min(tb, u.tok_end - 1) - tok0) / P
+                                                               : 0);
         const uint32_t full = bar_addr(base, kVFull0 + slot);
         const uint32_t dst = base + kOffV + slot * kVSlot;
-        if (lane == 0) mbar_arrive_expect_tx(full, kVSlot);
+        if (lane == 0) mbar_arrive_expect_tx(full, 4 * nbox * kVBox * 128);
         __syncwarp();
-        if (lane < 4) tma_load_2d(dst + lane * kVPanel, &maps.ckv_v, 256 * half + 64 * lane, row, full);
+        if (lane < 4 * nbox)
+          tma_load_2d(dst + (lane & 3) * kVPanel + bh * kVBox * 128, &maps.ckv_v,
+                      256 * half + 64 * (lane & 3), page * P + (tb % P), full);
         if (rows < kVChunkTok) {
           // Last chunk of a request: rows past kv_len may hold anything (even
           // NaN), and P = 0 there does not cancel NaN.  Wait for the copy,
           // zero those rows, then release the chunk through kVTail.
-          if (!(ok = mbar_wait_warp(full, (vc / kVSlots) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait_warp(full, ph, abort_flag))) break;
           for (int q = lane; q < (kVChunkTok - rows) * 32; q += 32) {
             const int rr = rows + q / 32, rem = q % 32;
             *reinterpret_cast<uint4*>(sm + kOffV + slot * kVSlot + (rem >> 3) * kVPanel + rr * 128 +
@@ -313,6 +348,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(bar_addr(base, kVTail0 + slot));
         }
       }
+      if (!ok) break;
+      if (ui2 < u1) {
+        // Warm L2 with the next tile's pages, whole contiguous rows (the panel
+        // copies slice every 1 KB row into 128-byte pieces, which DRAM serves
+        // poorly); both CTAs' copies of that tile then hit L2.
+        const WorkUnit v = a.units[ui2];
+        const int nt = v.tok_begin + i2 * kT;
+        const int nb = (min(nt + kT, v.tok_end) - nt + P - 1) / P;
+        if (lane < nb) {
+          const size_t srow = static_cast<size_t>(pg_next) * P;
+          bulk_prefetch_l2(static_cast<const char*>(a.ckv) + srow * kDCkv * 2, P * kDCkv * 2);
+          bulk_prefetch_l2(static_cast<const char*>(a.kpe) + srow * kDKpe * 2, P * kDKpe * 2);
+        }
+      }
+      pg_cur = pg_next;
+      ui = ui2;
+      i = i2;
     }
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
     if (lane == 0)
@@ -320,28 +372,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(bar_addr(base, kVFull0 + (vc - k) % kVSlots), ((vc - k) / kVSlots) & 1);
     __syncwarp();
   } else if (warp == 1) {
-    // ================= QK issuer (whole warp converged; lane 0 issues) =================
+    // ================= QK issuer (own tiles; whole warp converged, lane 0 issues) =================
     constexpr uint32_t id_qk = idesc_bf16_f32(128, kT, false, false);
     const uint32_t issue = lane == 0;
     const uint64_t q_desc0 = smem_desc(base + kOffQ, 16, 1024, kSw128);
     const uint64_t k_desc0 = smem_desc(base + kOffK, 16, 1024, kSw128);
-    int kc = 0, g = 0, uidx = 0;
+    int g = 0, gl = 0, uidx = 0, kslot = 0;
+    uint32_t kphase = 0;
     bool ok = true;
     for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
       const WorkUnit u = a.units[ui];
-      const int n = (u.tok_end - u.tok_begin + kT - 1) / kT;
+      const int n = tiles_of(u);
       if (!(ok = mbar_wait_warp(bar_addr(base, kQFull), uidx & 1, abort_flag) &&
                  mbar_wait_warp(bar_addr(base, kQTmemFull), uidx & 1, abort_flag)))
         break;
       tc_fence_after();
       for (int i = 0; i < n && ok; ++i, ++g) {
+        if ((g & 1) != half) continue;
         // S is single-buffered: the softmax drains it to registers right away.
-        if (!(ok = mbar_wait_warp(bar_addr(base, kSFree), (g & 1) ^ 1, abort_flag))) break;
-        for (int j = 0; j < 9; ++j, ++kc) {
-          const int slot = kc % kKSlots;
-          if (!(ok = mbar_wait_warp(bar_addr(base, kKFull0 + slot), (kc / kKSlots) & 1, abort_flag)))
-            break;
-          tc_fence_after();
+        if (!(ok = mbar_wait_warp(bar_addr(base, kSFree), (gl & 1) ^ 1, abort_flag))) break;
+        tc_fence_after();
+        for (int j = 0; j < 9; ++j) {
+          const int slot = kslot;
+          const uint32_t ph = kphase;
+          if (++kslot == kKSlots) {
+            kslot = 0;
+            kphase ^= 1;
+          }
+          if (!(ok = mbar_wait_warp(bar_addr(base, kKFull0 + slot), ph, abort_flag))) break;
           const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((slot * kPanel) >> 4);
           if (j < kQSmemPanels) {
             const uint64_t adesc = q_desc0 + static_cast<uint64_t>((j * kPanel) >> 4);
@@ -359,8 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         mma_commit(bar_addr(base, kSFull), issue);
-        if (i == n - 1) mma_commit(bar_addr(base, kQEmpty), issue);
+        ++gl;
       }
+      if (!ok) break;
+      mma_commit(bar_addr(base, kQEmpty), issue);   // Q of this unit no longer read
     }
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
     // Drain: all MMAs issued by this warp complete before TMEM is freed.
@@ -368,45 +428,57 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_wait_drain(bar_addr(base, kFinal), 0);
     __syncwarp();
   } else if (warp == kPvWarp) {
-    // ================= PV issuer (whole warp converged; lane 0 issues) =================
+    // ================= PV issuer (every tile; lane 0 issues) =================
     constexpr uint32_t id_pv = idesc_bf16_f32(128, 256, false, true);
     const uint32_t issue = lane == 0;
     const uint64_t p_desc0 = smem_desc(base + kOffP, 16, 1024, kSw128);
     const uint64_t v_desc0 = smem_desc(base + kOffV, kVPanel, 1024, kSw128);
-    int vc = 0, g = 0, uidx = 0;
+    int g = 0, uidx = 0, vslot = 0;
+    uint32_t vphase = 0;
     uint32_t tail_par = 0;   // per V slot: parity of its next tail-chunk release
     bool ok = true;
     for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
       const WorkUnit u = a.units[ui];
-      const int n = (u.tok_end - u.tok_begin + kT - 1) / kT;
+      const int n = tiles_of(u);
       for (int i = 0; i < n && ok; ++i, ++g) {
         const int valid = min(kT, u.tok_end - (u.tok_begin + i * kT));
         const int nch = (valid + kVChunkTok - 1) / kVChunkTok;
-        if (!(ok = mbar_wait_warp(bar_addr(base, kPFull), g & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(bar_addr(base, kPReady0 + (g & 1)), (g >> 1) & 1, abort_flag)))
+          break;
         // the first PV of a unit overwrites O: the previous epilogue must be done
         if (i == 0 && uidx > 0 &&
             !(ok = mbar_wait_warp(bar_addr(base, kOFree), (uidx - 1) & 1, abort_flag)))
           break;
-        for (int c = 0; c < nch; ++c, ++vc) {
-          const int slot = vc % kVSlots;
+        tc_fence_after();
+        for (int c = 0; c < nch; ++c) {
+          const int slot = vslot;
+          const uint32_t ph = vphase;
+          if (++vslot == kVSlots) {
+            vslot = 0;
+            vphase ^= 1;
+          }
           if (c == nch - 1 && (valid % kVChunkTok) != 0) {
             if (!(ok = mbar_wait_warp(bar_addr(base, kVTail0 + slot), (tail_par >> slot) & 1,
                                       abort_flag)))
               break;
             tail_par ^= 1u << slot;
-          } else if (!(ok = mbar_wait_warp(bar_addr(base, kVFull0 + slot), (vc / kVSlots) & 1,
-                                           abort_flag))) {
+          } else if (!(ok = mbar_wait_warp(bar_addr(base, kVFull0 + slot), ph, abort_flag))) {
             break;
           }
-          tc_fence_after();
-          mma_ss(tmem + kColO,
-                 p_desc0 + static_cast<uint64_t>(((c >> 2) * kPanel + (c & 3) * 32) >> 4),
-                 v_desc0 + static_cast<uint64_t>((slot * kVSlot) >> 4), id_pv,
-                 (i == 0 && c == 0) ? 0u : 1u, issue);
+#pragma unroll
+          for (int kk = 0; kk < kVChunkTok / 16; ++kk) {
+            const int tok = kVChunkTok * c + 16 * kk;   // first token of this MMA's K slice
+            mma_ss(tmem + kColO,
+                   p_desc0 + static_cast<uint64_t>(((tok >> 6) * kPanel + (tok & 63) * 2) >> 4),
+                   v_desc0 + static_cast<uint64_t>((slot * kVSlot + kk * 16 * 128) >> 4), id_pv,
+                   (i == 0 && c == 0 && kk == 0) ? 0u : 1u, issue);
+          }
           mma_commit(bar_addr(base, kVEmpty0 + slot), issue);
         }
         if (!ok) break;
-        mma_commit(bar_addr(base, kPvDone), issue);
+        mma_commit(bar_addr(base, kPvDone0 + (g & 1)), issue);
+        // P buffer g & 1 is reusable once both CTAs' PV of this tile is done
+        mma_commit_mc(bar_addr(base, kPFree0 + (g & 1)), static_cast<uint16_t>(0x3), issue);
       }
     }
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
@@ -422,9 +494,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const float c = prm.sm_scale * kLog2e;
     const float pad = c >= 0.f ? -INFINITY : INFINITY;   // neutral for the max of s * c
-    unsigned char* p_row = sm + kOffP + hc * kPanel + (r >> 3) * 1024 + (r & 7) * 128;
+    // P of tile g lives in buffer g & 1 in both CTAs; this row's chunk area:
+    const uint32_t p_off = hc * kPanel + (r >> 3) * 1024 + (r & 7) * 128;
     const int pswz = r & 7;
-    int g = 0, uidx = 0;
+    const uint32_t info_off = (hc * 128 + r) * kInfoRow;
+    const uint32_t recv_bar_remote = map_to_rank(bar_addr(base, kPRecv), peer);
+    int g = 0, gl = 0, nrecv = 0, uidx = 0;
     bool ok = true;
     if (u0 < u1) {
       load_q_tmem(a, a.units[u0].req, r, hc, lane_addr);
@@ -434,93 +509,131 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
       const WorkUnit u = a.units[ui];
-      const int n = (u.tok_end - u.tok_begin + kT - 1) / kT;
-      float m = -INFINITY, lr = 0.f, lx = 0.f;       // lr, lx: sums over this warp's tokens
-      for (int i = 0; i < n; ++i, ++g) {
-        if (!(ok = mbar_wait_warp(bar_addr(base, kSFull), g & 1, abort_flag))) break;
-        tc_fence_after();
-        const int valid = min(kT, u.tok_end - (u.tok_begin + i * kT));
-        float s[64];
-        float other;   // max (or min) over the partner warp's 64 tokens
-        {
-          uint32_t v[32];
-          tmem_ld32(lane_addr + kColS + 64 * hc, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(v[j]);
-          tmem_ld32(lane_addr + kColS + 64 * hc + 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(v[j]);
-          const int ob = 64 * (1 - hc);
-          float t[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) t[j] = pad;
-#pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            tmem_ld32(lane_addr + kColS + ob + 32 * q, v);
+      const int n = tiles_of(u);
+      const int g0 = g;
+      // references: m_last = of the last applied tile, m_prev = the one before
+      float m_last = -INFINITY, m_prev = -INFINITY;
+      float lx = 0.f, lr = 0.f;                        // this warp's token half
+      // the own tile computed but not yet applied
+      float own_m = -INFINITY, own_lx = 0.f, own_lr = 0.f;
+      for (int i = 0; i <= n && ok; ++i) {
+        const bool own_now = i < n && ((g0 + i) & 1) == half;
+        uint32_t pk[32];
+        if (own_now) {
+          // ---------- own tile g0 + i: scores -> P (registers) ----------
+          const int gg = g0 + i;
+          if (!(ok = mbar_wait_warp(bar_addr(base, kSFull), gl & 1, abort_flag))) break;
+          tc_fence_after();
+          const int valid = min(kT, u.tok_end - (u.tok_begin + i * kT));
+          float s[64];
+          float other;   // max (or min) over the partner warp's 64 tokens
+          {
+            uint32_t v[32];
+            tmem_ld32(lane_addr + kColS + 64 * hc, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float y = ob + 32 * q + j < valid ? __uint_as_float(v[j]) : pad;
-              t[j & 15] = c >= 0.f ? fmaxf(t[j & 15], y) : fminf(t[j & 15], y);
+            for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(v[j]);
+            tmem_ld32(lane_addr + kColS + 64 * hc + 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(v[j]);
+            const int ob = 64 * (1 - hc);
+            float t[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) t[j] = pad;
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+              tmem_ld32(lane_addr + kColS + ob + 32 * q, v);
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float y = ob + 32 * q + j < valid ? __uint_as_float(v[j]) : pad;
+                t[j & 15] = c >= 0.f ? fmaxf(t[j & 15], y) : fminf(t[j & 15], y);
+              }
             }
+            other = c >= 0.f ? tree_max(t) : tree_min(t);
           }
-          other = c >= 0.f ? tree_max(t) : tree_min(t);
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_addr(base, kSFree));
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_addr(base, kSFree));
+          ++gl;
 
-        // exponent of token j: s_j * c - m (one FFMA); for c >= 0 the row max
-        // of s_j * c is c * max s_j, for c < 0 it is c * min s_j.
-        const int vb = 64 * hc;                      // first token of this warp's half
-        float mx;
-        {
-          float t[32];
+          const int vb = 64 * hc;                      // first token of this warp's half
+          float mx;
+          {
+            float t[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float lo = vb + j < valid ? s[j] : pad;
-            const float hi = vb + 32 + j < valid ? s[32 + j] : pad;
-            t[j] = c >= 0.f ? fmaxf(lo, hi) : fminf(lo, hi);
+            for (int j = 0; j < 32; ++j) {
+              const float lo = vb + j < valid ? s[j] : pad;
+              const float hi = vb + 32 + j < valid ? s[32 + j] : pad;
+              t[j] = c >= 0.f ? fmaxf(lo, hi) : fminf(lo, hi);
+            }
+            const float own = c >= 0.f ? tree_max(t) : tree_min(t);
+            mx = c * (c >= 0.f ? fmaxf(own, other) : fminf(own, other));
           }
-          const float own = c >= 0.f ? tree_max(t) : tree_min(t);
-          mx = c * (c >= 0.f ? fmaxf(own, other) : fminf(own, other));
-        }
-        const bool move = mx > m + kRescaleThreshold;
-        const float m_new = move ? mx : m;
-        const float alpha = move ? exp2f(m - m_new) : 1.f;
-        uint32_t pk[32];
-        float sx = 0.f, srd = 0.f;
+          // lazy reference: the latest two applied references, moved only when
+          // this tile's max exceeds them by more than the threshold
+          const float m_known = fmaxf(m_last, m_prev);
+          const float m_new = mx > m_known + kRescaleThreshold ? mx : m_known;
+          float sx = 0.f, srd = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float ex[16], er[16];
-          if (valid == kT) {
+          for (int q = 0; q < 4; ++q) {
+            float ex[16], er[16];
+            if (valid == kT) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) ex[j] = exp2f(fmaf(s[16 * q + j], c, -m_new));
-          } else {
+              for (int j = 0; j < 16; ++j) ex[j] = exp2f(fmaf(s[16 * q + j], c, -m_new));
+            } else {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)   // masked tokens: 0 (also when c == 0)
-              ex[j] = vb + 16 * q + j < valid ? exp2f(fmaf(s[16 * q + j], c, -m_new)) : 0.f;
+              for (int j = 0; j < 16; ++j)   // masked tokens: 0 (also when c == 0)
+                ex[j] = vb + 16 * q + j < valid ? exp2f(fmaf(s[16 * q + j], c, -m_new)) : 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex[2 * j], ex[2 * j + 1]);
+              er[2 * j] = __low2float(b2);
+              er[2 * j + 1] = __high2float(b2);
+              pk[8 * q + j] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            sx += tree_sum(ex);
+            srd += tree_sum(er);
           }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex[2 * j], ex[2 * j + 1]);
-            er[2 * j] = __low2float(b2);
-            er[2 * j + 1] = __high2float(b2);
-            pk[8 * q + j] = *reinterpret_cast<const uint32_t*>(&b2);
-          }
-          sx += tree_sum(ex);
-          srd += tree_sum(er);
-        }
-        lx = lx * alpha + sx;
-        lr = lr * alpha + srd;
-        m = m_new;
+          own_m = m_new;
+          own_lx = sx;
+          own_lr = srd;
 
-        // P buffer and O are free once PV of the previous tile completed.
-        if (g > 0 && !(ok = mbar_wait_warp(bar_addr(base, kPvDone), (g - 1) & 1, abort_flag))) break;
-        tc_fence_after();
-        if (i > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        }
+        if (i > 0) {
+        // ---------- apply tile t = g0 + i - 1 (own or received), release it to PV ----------
+        const int t = g0 + i - 1;
+        float mt, tlx, tlr;
+        if ((t & 1) == half) {
+          mt = own_m;
+          tlx = own_lx;
+          tlr = own_lr;
+        } else {
+          if (warp == 3 && lane == 0) mbar_arrive_expect_tx(bar_addr(base, kPRecv), kRecvBytes);
+          if (!(ok = mbar_wait_warp(bar_addr(base, kPRecv), nrecv & 1, abort_flag))) break;
+          ++nrecv;
+          const float* info = reinterpret_cast<const float*>(sm + kOffInfo + info_off);
+          mt = info[0];
+          tlx = info[1];
+          tlr = info[2];
+          fence_proxy_async_smem();   // P written through the peer is read by the MMA next
+        }
+        // Stay at most two tiles ahead of PV (PV(t-2) complete): with one
+        // kPvDone barrier per tile parity, every wait below is then less
+        // than two phases away, so its parity is unambiguous.
+        if (t >= 2 && !(ok = mbar_wait_warp(bar_addr(base, kPvDone0 + (t & 1)), ((t - 2) >> 1) & 1,
+                                            abort_flag)))
+          break;
+        const bool first = t == g0;
+        const float alpha = first ? 0.f : exp2f(m_last - mt);
+        if (!first && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O holds P . V of earlier tiles relative to m_last: move it to mt
+          if (!(ok = mbar_wait_warp(bar_addr(base, kPvDone0 + ((t - 1) & 1)), ((t - 1) >> 1) & 1,
+                                    abort_flag)))
+            break;
+          tc_fence_after();
 #pragma unroll 1
           for (int cc = 4 * hc; cc < 4 * hc + 4; ++cc) {
             uint32_t o[32];
@@ -532,38 +645,74 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st_wait();
         }
-        // P row r, this warp's panel: 16-byte chunk ch holds tokens 8ch .. 8ch+7
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(p_row + ((ch ^ pswz) << 4)) =
-              make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-        fence_proxy_async_smem();
+        lx = first ? tlx : lx * alpha + tlx;
+        lr = first ? tlr : lr * alpha + tlr;
+        m_prev = m_last;
+        m_last = mt;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_addr(base, kPFull));
-        if (i == n - 1 && ui + 1 < u1) {
-          // Q of the next unit: every QK of this unit has completed (S was read)
-          load_q_tmem(a, a.units[ui + 1].req, r, hc, lane_addr);
-          tc_fence_before();
+        if (lane == 0) mbar_arrive(bar_addr(base, kPReady0 + (t & 1)));
+        }
+        if (own_now) {
+          // ---------- own tile g0 + i: P to this CTA and the peer ----------
+          // (after tile g0 + i - 1 was released above: its PV, in both CTAs,
+          // is what frees the P buffers)
+          const int gg = g0 + i;
+          // The P buffer (one, in each CTA) is free once both CTAs' PV of the
+          // previous tile is done.
+          if (gg >= 1 && !(ok = mbar_wait_warp(bar_addr(base, kPFree0 + ((gg - 1) & 1)),
+                                               ((gg - 1) >> 1) & 1, abort_flag)))
+            break;
+          const uint32_t prow = kOffP + p_off;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<uint4*>(sm + prow + ((ch ^ pswz) << 4)) =
+                make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          *reinterpret_cast<float4*>(sm + kOffInfoOut + info_off) =
+              make_float4(own_m, own_lx, own_lr, 0.f);
+          // This warp's rows are contiguous: P rows 32 quad .. 32 quad + 31 of
+          // panel hc (4 KB) and its 32 info rows (512 B).  One bulk copy each
+          // carries them to the peer (the TMA engine moves distributed shared
+          // memory much faster than per-thread remote stores).
+          fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_addr(base, kQTmemFull));
+          if (lane == 0) {
+            const uint32_t pblk = kOffP + hc * kPanel + quad * 32 * 128;
+            const uint32_t iblk = (hc * 128 + quad * 32) * kInfoRow;
+            bulk_copy_to_peer(map_to_rank(base + pblk, peer), base + pblk, 32 * 128, recv_bar_remote);
+            bulk_copy_to_peer(map_to_rank(base + kOffInfo + iblk, peer), base + kOffInfoOut + iblk,
+                              32 * kInfoRow, recv_bar_remote);
+          }
+          fence_proxy_async_smem();
         }
       }
       if (!ok) break;
+      g = g0 + n;
+      if (ui + 1 < u1) {
+        // Q of the next unit: every own QK of this unit has been drained, and
+        // the QK warp has finished the unit (so it consumed this unit's
+        // kQTmemFull phase before the next one is signalled)
+        if (!(ok = mbar_wait_warp(bar_addr(base, kQEmpty), uidx & 1, abort_flag))) break;
+        load_q_tmem(a, a.units[ui + 1].req, r, hc, lane_addr);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_addr(base, kQTmemFull));
+      }
       // ---- epilogue ----
-      if (!(ok = mbar_wait_warp(bar_addr(base, kPvDone), (g - 1) & 1, abort_flag))) break;
+      if (!(ok = mbar_wait_warp(bar_addr(base, kPvDone0 + ((g - 1) & 1)), ((g - 1) >> 1) & 1,
+                                abort_flag)))
+        break;
       tc_fence_after();
-      // Combine the two warps' row sums through their P rows (P is idle now).
-      // Two phases of kXchg0 + quad per unit: "both written", "both read".
-      float* xch = reinterpret_cast<float*>(p_row);
-      xch[0] = lx;
-      xch[1] = lr;
+      // Combine the two warps' row sums through shared memory; two phases of
+      // kXchg0 + quad per unit.
+      float* xch = reinterpret_cast<float*>(sm + kOffXchg + r * 16);
+      xch[2 * hc] = lx;
+      xch[2 * hc + 1] = lr;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(base, kXchg0 + quad));
       if (!(ok = mbar_wait_warp(bar_addr(base, kXchg0 + quad), 0, abort_flag))) break;
-      const float* pxch = reinterpret_cast<const float*>(p_row + (hc ? -kPanel : kPanel));
-      const float lx_all = lx + pxch[0];
-      const float lr_all = lr + pxch[1];
+      const float lx_all = xch[0] + xch[2];
+      const float lr_all = xch[1] + xch[3];
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(base, kXchg0 + quad));
       if (!(ok = mbar_wait_warp(bar_addr(base, kXchg0 + quad), 1, abort_flag))) break;
@@ -605,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(base, kOFree));
       if (half == 0 && hc == 0 && r < H)
-        (partial ? a.lse_part : a.lse)[orow] = (m + log2f(lx_all)) * kLn2;
+        (partial ? a.lse_part : a.lse)[orow] = (m_last + log2f(lx_all)) * kLn2;
     }
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
   }
@@ -616,22 +765,65 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  cluster_sync_all();   // no CTA leaves while its peer may still address its shared memory
+}
+
+template <bool kOutF32>
+cudaError_t set_attributes() {
+  static bool attr_set = false;   // set once, before any stream capture
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<kOutF32>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return cudaSuccess;
 }
 
 template <bool kOutF32>
 cudaError_t launch_impl(const DecodeArgs& a, const TcMaps& maps, cudaStream_t s) {
   auto* k = decode_tc_kernel<kOutF32>;
-  static bool attr_set = false;   // set once, before any stream capture
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  k<<<2 * a.n_workers, kThreads, kSmemBytes, s>>>(a, maps);
-  return cudaGetLastError();
+  cudaError_t e = set_attributes<kOutF32>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * a.n_workers);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, a, maps);
 }
 
 }  // namespace
+
+cudaError_t decode_tc_max_workers(int* workers) {
+  *workers = 0;
+  cudaError_t e = set_attributes<true>();
+  if (e == cudaSuccess) e = set_attributes<false>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, decode_tc_kernel<false>, &cfg);
+  if (e != cudaSuccess) return e;
+  *workers = clusters;
+  return cudaSuccess;
+}
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, const TcMaps& maps, bool out_f32, cudaStream_t s) {
   return out_f32 ? launch_impl<true>(a, maps, s) : launch_impl<false>(a, maps, s);

@@ -52,6 +52,9 @@ struct TcMaps {
 };
 cudaError_t launch_decode_tc(const DecodeArgs& a, const TcMaps& maps, bool out_f32,
                              cudaStream_t s);
+// Clusters of two CTAs of the tcgen05 kernel that can be resident at once
+// (the persistent grid uses at most that many workers).
+cudaError_t decode_tc_max_workers(int* workers);
 
 // LSE merge of split partials (and zero-fill of empty requests).
 cudaError_t launch_merge(const MergeArgs& a, bool out_f32, cudaStream_t s);
