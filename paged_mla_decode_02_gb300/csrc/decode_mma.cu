@@ -277,8 +277,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
   for (int j = 0; j < 16; ++j) {
     const int d = warp * 128 + j * 8 + 2 * (lane & 3);
     if (partial) {
-      if (g0 < H) *reinterpret_cast<float2*>(a.o_part + row0 * kDCkv + d) = make_float2(o[j][0] * inv0, o[j][1] * inv0);
-      if (g1 < H) *reinterpret_cast<float2*>(a.o_part + row1 * kDCkv + d) = make_float2(o[j][2] * inv1, o[j][3] * inv1);
+      if (g0 < H)
+        *reinterpret_cast<float2*>(a.o_part + part_offset(u.out_slot, g0, d, H)) =
+            make_float2(o[j][0] * inv0, o[j][1] * inv0);
+      if (g1 < H)
+        *reinterpret_cast<float2*>(a.o_part + part_offset(u.out_slot, g1, d, H)) =
+            make_float2(o[j][2] * inv1, o[j][3] * inv1);
     } else if (kOutF32) {
       float* out = static_cast<float*>(a.out);
       if (g0 < H) *reinterpret_cast<float2*>(out + row0 * kDCkv + d) = make_float2(o[j][0] * inv0, o[j][1] * inv0);

@@ -25,13 +25,12 @@
 // Per CTA (384 threads, 12 warps):
 //   warp 0      K producer (own tiles): TMA loads of Q dims 0..319 (per
 //               unit) and of the 9 K panels (64 dims x 128 tokens) of the
-//               tile, page by page through kv_indices, into a 2-slot ring;
+//               tile, page by page through kv_indices, into a 3-slot ring;
 //   warp 1      allocates TMEM; lane 0 issues the QK MMAs (M=128 heads,
 //               N=128 tokens, K=16) of own tiles into S;
 //   warp 2      V producer (every tile): this CTA's 256 dims of ckv,
-//               16 tokens (8 KB) at a time into a 5-slot ring; rows past the
-//               end of a request are zeroed; also a contiguous L2 prefetch of
-//               the pages of the tile two ahead;
+//               32 tokens (16 KB) at a time into a 3-slot ring; rows past the
+//               end of a request are zeroed;
 //   warps 3..10 softmax: two warps per 32 head rows (TMEM lane quadrant),
 //               each owning 64 tokens of a tile (one P panel) and 128 of the
 //               256 output dims.  For an own tile: drain S, row max over the
@@ -91,7 +90,8 @@ constexpr int kOffV = kOffK + kKSlots * kPanel;
 constexpr int kOffInfo = kOffV + kVSlots * kVSlot;     // received row info (the peer's tiles)
 constexpr int kOffInfoOut = kOffInfo + kInfoBytes;     // row info of own tiles, to send
 constexpr int kOffXchg = kOffInfoOut + kInfoBytes;     // 128 x (lx, lr) x 2 halves
-constexpr int kOffBar = kOffXchg + 128 * 16;
+constexpr int kOffMaxX = kOffXchg + 128 * 16;          // [own tile parity][half][128] row maxima
+constexpr int kOffBar = kOffMaxX + 2 * 2 * 128 * 4;
 constexpr int kBarBytes = 512;
 constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;   // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -107,7 +107,8 @@ enum Bar {
   kPReady0,         // 2, by tile parity: tile released to PV (O rescaled, P in place)
   kPvDone0 = kPReady0 + 2,   // 2, by tile parity: this CTA's PV of the tile completed
   kOFree = kPvDone0 + 2, kFinal, kFinalPv,
-  kXchg0, kNumBars = kXchg0 + 4
+  kXchg0, kMaxX0 = kXchg0 + 4,   // 4, per lane quadrant: the two warps' row maxima posted
+  kNumBars = kMaxX0 + 4
 };
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
 
@@ -201,7 +202,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t cnt = 1;
       if (i == kQTmemFull || i == kSFree || i == kPReady0 || i == kPReady0 + 1 || i == kOFree)
         cnt = kSoftmaxWarps;
-      if (i == kPFree0 || i == kPFree0 + 1 || i >= kXchg0) cnt = 2;
+      if (i == kPFree0 || i == kPFree0 + 1 || i >= kXchg0) cnt = 2;   // kXchg*, kMaxX*
       mbar_init(bar_addr(base, i), cnt);
     }
     fence_barrier_init();
@@ -349,19 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      if (ui2 < u1) {
-        // Warm L2 with the next tile's pages, whole contiguous rows (the panel
-        // copies slice every 1 KB row into 128-byte pieces, which DRAM serves
-        // poorly); both CTAs' copies of that tile then hit L2.
-        const WorkUnit v = a.units[ui2];
-        const int nt = v.tok_begin + i2 * kT;
-        const int nb = (min(nt + kT, v.tok_end) - nt + P - 1) / P;
-        if (lane < nb) {
-          const size_t srow = static_cast<size_t>(pg_next) * P;
-          bulk_prefetch_l2(static_cast<const char*>(a.ckv) + srow * kDCkv * 2, P * kDCkv * 2);
-          bulk_prefetch_l2(static_cast<const char*>(a.kpe) + srow * kDKpe * 2, P * kDKpe * 2);
-        }
-      }
       pg_cur = pg_next;
       ui = ui2;
       i = i2;
@@ -474,6 +462,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                    (i == 0 && c == 0 && kk == 0) ? 0u : 1u, issue);
           }
           mma_commit(bar_addr(base, kVEmpty0 + slot), issue);
+          // P panel 0 (tokens 0..63) is no longer read after chunk 1: the
+          // next tile's owner may overwrite it in both CTAs
         }
         if (!ok) break;
         mma_commit(bar_addr(base, kPvDone0 + (g & 1)), issue);
@@ -525,52 +515,50 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait_warp(bar_addr(base, kSFull), gl & 1, abort_flag))) break;
           tc_fence_after();
           const int valid = min(kT, u.tok_end - (u.tok_begin + i * kT));
+          const int vb = 64 * hc;                      // first token of this warp's half
           float s[64];
-          float other;   // max (or min) over the partner warp's 64 tokens
           {
-            uint32_t v[32];
-            tmem_ld32(lane_addr + kColS + 64 * hc, v);
+            uint32_t v0[32], v1[32];
+            tmem_ld32(lane_addr + kColS + vb, v0);
+            tmem_ld32(lane_addr + kColS + vb + 32, v1);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) s[j] = __uint_as_float(v[j]);
-            tmem_ld32(lane_addr + kColS + 64 * hc + 32, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) s[32 + j] = __uint_as_float(v[j]);
-            const int ob = 64 * (1 - hc);
-            float t[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) t[j] = pad;
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-              tmem_ld32(lane_addr + kColS + ob + 32 * q, v);
-              tmem_ld_wait();
-#pragma unroll
-              for (int j = 0; j < 32; ++j) {
-                const float y = ob + 32 * q + j < valid ? __uint_as_float(v[j]) : pad;
-                t[j & 15] = c >= 0.f ? fmaxf(t[j & 15], y) : fminf(t[j & 15], y);
-              }
+            for (int j = 0; j < 32; ++j) {
+              s[j] = __uint_as_float(v0[j]);
+              s[32 + j] = __uint_as_float(v1[j]);
             }
-            other = c >= 0.f ? tree_max(t) : tree_min(t);
           }
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_addr(base, kSFree));
           ++gl;
 
-          const int vb = 64 * hc;                      // first token of this warp's half
-          float mx;
+          // max (min when c < 0) of s over this warp's valid tokens, then
+          // combined with the partner warp's half of the row
+          float hmx;
           {
             float t[32];
+            if (valid >= vb + 64) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float lo = vb + j < valid ? s[j] : pad;
-              const float hi = vb + 32 + j < valid ? s[32 + j] : pad;
-              t[j] = c >= 0.f ? fmaxf(lo, hi) : fminf(lo, hi);
+              for (int j = 0; j < 32; ++j) t[j] = c >= 0.f ? fmaxf(s[j], s[32 + j]) : fminf(s[j], s[32 + j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) {
+                const float lo = vb + j < valid ? s[j] : pad;
+                const float hi = vb + 32 + j < valid ? s[32 + j] : pad;
+                t[j] = c >= 0.f ? fmaxf(lo, hi) : fminf(lo, hi);
+              }
             }
-            const float own = c >= 0.f ? tree_max(t) : tree_min(t);
-            mx = c * (c >= 0.f ? fmaxf(own, other) : fminf(own, other));
+            hmx = c >= 0.f ? tree_max(t) : tree_min(t);
           }
+          float* mx_slot = reinterpret_cast<float*>(sm + kOffMaxX) + ((gl & 1) * 2 + hc) * 128 + r;
+          *mx_slot = hmx;
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_addr(base, kMaxX0 + quad));
+          // phase k of this barrier: both warps of the quadrant posted own tile k
+          if (!(ok = mbar_wait_warp(bar_addr(base, kMaxX0 + quad), (gl - 1) & 1, abort_flag))) break;
+          const float other = mx_slot[(1 - 2 * hc) * 128];
+          const float mx = c * (c >= 0.f ? fmaxf(hmx, other) : fminf(hmx, other));
           // lazy reference: the latest two applied references, moved only when
           // this tile's max exceeds them by more than the threshold
           const float m_known = fmaxf(m_last, m_prev);
@@ -579,20 +567,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             float ex[16], er[16];
-            if (valid == kT) {
+            if (valid >= vb + 64) {
 #pragma unroll
-              for (int j = 0; j < 16; ++j) ex[j] = exp2f(fmaf(s[16 * q + j], c, -m_new));
+              for (int j = 0; j < 16; ++j) ex[j] = fast_exp2(fmaf(s[16 * q + j], c, -m_new));
             } else {
 #pragma unroll
               for (int j = 0; j < 16; ++j)   // masked tokens: 0 (also when c == 0)
-                ex[j] = vb + 16 * q + j < valid ? exp2f(fmaf(s[16 * q + j], c, -m_new)) : 0.f;
+                ex[j] = vb + 16 * q + j < valid ? fast_exp2(fmaf(s[16 * q + j], c, -m_new)) : 0.f;
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               const __nv_bfloat162 b2 = __floats2bfloat162_rn(ex[2 * j], ex[2 * j + 1]);
-              er[2 * j] = __low2float(b2);
-              er[2 * j + 1] = __high2float(b2);
-              pk[8 * q + j] = *reinterpret_cast<const uint32_t*>(&b2);
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(&b2);
+              er[2 * j] = __uint_as_float(w << 16);
+              er[2 * j + 1] = __uint_as_float(w & 0xffff0000u);
+              pk[8 * q + j] = w;
             }
             sx += tree_sum(ex);
             srd += tree_sum(er);
@@ -717,35 +706,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar_addr(base, kXchg0 + quad));
       if (!(ok = mbar_wait_warp(bar_addr(base, kXchg0 + quad), 1, abort_flag))) break;
       const bool partial = u.out_slot >= 0;
-      const size_t orow = partial ? static_cast<size_t>(u.out_slot) * H + r
-                                  : static_cast<size_t>(u.req) * H + r;
+      // rows of out are 32-byte aligned when out is (the ABI asks for 16)
+      const bool out32 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
+      const size_t orow = static_cast<size_t>(u.req) * H + r;
       const float inv = (r < H) ? a.kv_scale / lr_all : 0.f;
 #pragma unroll 1
       for (int cc = 4 * hc; cc < 4 * hc + 4; ++cc) {
         uint32_t o[32];
         tmem_ld32(lane_addr + kColO + 32 * cc, o);
         tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * inv);
         if (r < H) {
           const int d0 = 256 * half + 32 * cc;
-          if (partial || kOutF32) {
-            float* dst = (partial ? a.o_part : static_cast<float*>(a.out)) + orow * kDCkv + d0;
+          if (partial) {
+            // lanes hold consecutive heads: each store is 512 contiguous bytes
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              reinterpret_cast<float4*>(dst)[j] =
-                  make_float4(__uint_as_float(o[4 * j]) * inv, __uint_as_float(o[4 * j + 1]) * inv,
-                              __uint_as_float(o[4 * j + 2]) * inv, __uint_as_float(o[4 * j + 3]) * inv);
+              *reinterpret_cast<uint4*>(a.o_part + part_offset(u.out_slot, r, d0 + 4 * j, H)) =
+                  make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+          } else if (kOutF32) {
+            float* dst = static_cast<float*>(a.out) + orow * kDCkv + d0;
+            if (out32) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) st_global_v8(dst + 8 * j, &o[8 * j]);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                reinterpret_cast<uint4*>(dst)[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            }
           } else {
             __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + orow * kDCkv + d0;
+            uint32_t w[16];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              uint32_t w[4];
+            for (int e = 0; e < 16; ++e) {
+              const __nv_bfloat162 b2 =
+                  __floats2bfloat162_rn(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
+              w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+            }
+            if (out32) {
+              st_global_v8(dst, &w[0]);
+              st_global_v8(dst + 16, &w[8]);
+            } else {
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 b2 = __floats2bfloat162_rn(
-                    __uint_as_float(o[8 * j + 2 * e]) * inv, __uint_as_float(o[8 * j + 2 * e + 1]) * inv);
-                w[e] = *reinterpret_cast<const uint32_t*>(&b2);
-              }
-              reinterpret_cast<uint4*>(dst)[j] = make_uint4(w[0], w[1], w[2], w[3]);
+              for (int j = 0; j < 4; ++j)
+                reinterpret_cast<uint4*>(dst)[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
             }
           }
         }
@@ -754,7 +759,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(base, kOFree));
       if (half == 0 && hc == 0 && r < H)
-        (partial ? a.lse_part : a.lse)[orow] = (m_last + log2f(lx_all)) * kLn2;
+        (partial ? a.lse_part + static_cast<size_t>(u.out_slot) * H + r : a.lse + orow)[0] =
+            (m_last + log2f(lx_all)) * kLn2;
     }
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
   }

@@ -19,7 +19,7 @@ struct DecodeArgs {
   const PlanDev* params;
   void* out;                   // [B,H,512] bf16 or fp32
   float* lse;                  // [B,H]
-  float* o_part;               // [slots,H,512] fp32
+  float* o_part;               // partial outputs, fp32, layout of part_offset()
   float* lse_part;             // [slots,H]
   int32_t* err;
   int num_pages;
@@ -28,6 +28,16 @@ struct DecodeArgs {
   int units_cap;
   int n_workers;
 };
+
+// Element (slot, head h, dim d) of the fp32 partial outputs.  Dims are
+// grouped by four and the heads of a group are adjacent:
+//   [slot][d / 4][h][d % 4]
+// so a warp holding 32 consecutive heads x 4 dims stores (or the merge
+// loads) 512 contiguous bytes, where a [slot][h][d] layout would touch 32
+// separate rows per instruction.
+__host__ __device__ inline size_t part_offset(int slot, int h, int d, int H) {
+  return ((static_cast<size_t>(slot) * (kDCkv / 4) + d / 4) * H + h) * 4 + (d & 3);
+}
 
 struct MergeArgs {
   const MergeEntry* merge;

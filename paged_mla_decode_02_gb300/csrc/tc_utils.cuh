@@ -299,6 +299,21 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 // Stores into another CTA's shared memory whose completion is counted, in
 // bytes, on an mbarrier of that CTA (remote addresses from map_to_rank).
+// 2^x on the special function unit (approximate; results below 2^-126
+// flush to zero, 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 32-byte global store (eight 32-bit words; the address is 32-byte aligned).
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
+
 __device__ __forceinline__ void st_async_v4(uint32_t raddr, uint4 v, uint32_t rbar) {
   asm volatile(
       "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::
