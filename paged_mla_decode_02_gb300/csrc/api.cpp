@@ -128,6 +128,25 @@ bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int ele
   return r == CUDA_SUCCESS;
 }
 
+// 3-D view of a row-major [rows, 512] bf16 matrix as 64-element panels:
+// (element within panel, row, panel) with strides (2 B, 1024 B, 128 B); a box
+// (64, box_rows, box_panels) lands in shared memory panel by panel, each
+// panel box_rows x 128 bytes with the 128-byte swizzle -- the layout the MMA
+// reads -- in one copy instead of one per panel.
+bool encode_panels_3d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows,
+                      uint32_t box_panels) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {64, rows, kDCkv / 64};
+  cuuint64_t strides[2] = {kDCkv * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, box_panels};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 extern "C" {
@@ -337,7 +356,7 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
     if (!encode_2d(&maps.q_nope, q_nope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qrows, kDCkv, H, 64) ||
         !encode_2d(&maps.ckv_k, ckv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDCkv, P, 64) ||
         !encode_2d(&maps.kpe_k, kpe_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDKpe, P, 64) ||
-        !encode_2d(&maps.ckv_v, ckv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDCkv, 16, 64))
+        !encode_panels_3d(&maps.ckv_v, ckv_cache, kvrows, P >= 32 ? 32 : 16, 4))
       return fail(plan, MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     e = launch_decode_tc(a, maps, out_f32, s);
   }

@@ -72,7 +72,6 @@ constexpr int kPanel = 128 * 128;           // 128 rows x 128 B (one 64-dim pane
 constexpr int kKSlots = 3;
 constexpr int kVSlots = 3;
 constexpr int kVChunkTok = 32;              // tokens per V chunk: two PV MMAs
-constexpr int kVBox = 16;                   // rows per V copy (every page holds >= 16)
 constexpr int kVPanel = kVChunkTok * 128;   // 4 KB: 32 rows x 64 dims
 constexpr int kVSlot = 4 * kVPanel;         // 16 KB: 32 rows x 256 dims
 constexpr int kQSmemPanels = 5;             // Q dims 0..319 in shared memory
@@ -319,30 +318,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           vphase ^= 1;
         }
         if (!(ok = mbar_wait_warp(bar_addr(base, kVEmpty0 + slot), ph ^ 1, abort_flag))) break;
-        // lane l copies box (l >> 2) (16 rows) of panel (l & 3) (64 dims)
+        // One 3-D copy per page run of the chunk brings this CTA's 4 panels:
+        // pages of >= 32 rows give one 32-row copy (panels 4 KB apart), 16-row
+        // pages two 16-row copies (panels 2 KB apart, second copy 8 KB in).
         const int rows = min(kVChunkTok, u.tok_end - t);
-        const int nbox = rows > kVBox ? 2 : 1;
-        const int bh = (lane >> 2) & 1;
-        const int tb = t + kVBox * bh;
-        const int page = __shfl_sync(0xffffffffu, pg_cur, min(tb, u.tok_end - 1) - tok0 < kT
-                                                               ? (min(tb, u.tok_end - 1) - tok0) / P
-                                                               : 0);
+        const int vbox = P >= kVChunkTok ? kVChunkTok : 16;
+        const int ncopy = (rows + vbox - 1) / vbox;
         const uint32_t full = bar_addr(base, kVFull0 + slot);
         const uint32_t dst = base + kOffV + slot * kVSlot;
-        if (lane == 0) mbar_arrive_expect_tx(full, 4 * nbox * kVBox * 128);
+        if (lane == 0) mbar_arrive_expect_tx(full, ncopy * vbox * 4 * 128);
         __syncwarp();
-        if (lane < 4 * nbox)
-          tma_load_2d(dst + (lane & 3) * kVPanel + bh * kVBox * 128, &maps.ckv_v,
-                      256 * half + 64 * (lane & 3), page * P + (tb % P), full);
+        // lane c < ncopy issues copy c (lanes past it mirror the last one for the shuffle)
+        const int tb = t + vbox * min(lane, ncopy - 1);
+        const int page = __shfl_sync(0xffffffffu, pg_cur, (tb - tok0) / P);
+        if (lane < ncopy)
+          tma_load_3d(dst + lane * vbox * 4 * 128, &maps.ckv_v, 0, page * P + (tb % P), 4 * half, full);
         if (rows < kVChunkTok) {
           // Last chunk of a request: rows past kv_len may hold anything (even
           // NaN), and P = 0 there does not cancel NaN.  Wait for the copy,
           // zero those rows, then release the chunk through kVTail.
           if (!(ok = mbar_wait_warp(full, ph, abort_flag))) break;
           for (int q = lane; q < (kVChunkTok - rows) * 32; q += 32) {
-            const int rr = rows + q / 32, rem = q % 32;
-            *reinterpret_cast<uint4*>(sm + kOffV + slot * kVSlot + (rem >> 3) * kVPanel + rr * 128 +
-                                      (rem & 7) * 16) = make_uint4(0, 0, 0, 0);
+            const int rr = rows + q / 32, pnl = (q % 32) >> 3, c16 = q & 7;
+            const int off = vbox == kVChunkTok
+                                ? pnl * kVPanel + rr * 128
+                                : (rr >> 4) * (kVSlot / 2) + pnl * (kVPanel / 2) + (rr & 15) * 128;
+            *reinterpret_cast<uint4*>(sm + kOffV + slot * kVSlot + off + c16 * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -420,7 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t id_pv = idesc_bf16_f32(128, 256, false, true);
     const uint32_t issue = lane == 0;
     const uint64_t p_desc0 = smem_desc(base + kOffP, 16, 1024, kSw128);
-    const uint64_t v_desc0 = smem_desc(base + kOffV, kVPanel, 1024, kSw128);
+    // V chunk layout (see the V producer): panels 4 KB apart and the two
+    // 16-token slices 2 KB apart, or for 16-row pages 2 KB and 8 KB
+    const bool v32 = P >= kVChunkTok;
+    const uint64_t v_desc0 = smem_desc(base + kOffV, v32 ? kVPanel : kVPanel / 2, 1024, kSw128);
+    const uint32_t v_kstep = v32 ? 16 * 128 : kVSlot / 2;
     int g = 0, uidx = 0, vslot = 0;
     uint32_t vphase = 0;
     uint32_t tail_par = 0;   // per V slot: parity of its next tail-chunk release
@@ -458,7 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int tok = kVChunkTok * c + 16 * kk;   // first token of this MMA's K slice
             mma_ss(tmem + kColO,
                    p_desc0 + static_cast<uint64_t>(((tok >> 6) * kPanel + (tok & 63) * 2) >> 4),
-                   v_desc0 + static_cast<uint64_t>((slot * kVSlot + kk * 16 * 128) >> 4), id_pv,
+                   v_desc0 + static_cast<uint64_t>((slot * kVSlot + kk * v_kstep) >> 4), id_pv,
                    (i == 0 && c == 0 && kk == 0) ? 0u : 1u, issue);
           }
           mma_commit(bar_addr(base, kVEmpty0 + slot), issue);

@@ -58,7 +58,7 @@ struct TcMaps {
   CUtensorMap q_nope;   // [B*H, 512] bf16, box 64 x H
   CUtensorMap ckv_k;    // [pages*P, 512] bf16, box 64 x P (one page of a K panel)
   CUtensorMap kpe_k;    // [pages*P, 64] bf16, box 64 x P
-  CUtensorMap ckv_v;    // [pages*P, 512] bf16, box 64 x 16 (a V chunk panel)
+  CUtensorMap ckv_v;    // (64, pages*P, 8 panels) view of ckv, box 64 x min(P, 32) x 4 panels
 };
 cudaError_t launch_decode_tc(const DecodeArgs& a, const TcMaps& maps, bool out_f32,
                              cudaStream_t s);
