@@ -331,7 +331,9 @@ def main() -> None:
                     "h2d_bytes_per_step": int(qn_h.numel() * 2 + qp_h.numel() * 2),
                     "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()
                                               + lse_h.numel() * 4)},
-            "gpu_launches": 2 * args.steps,
+            # tcgen05: one kernel per step (split requests merged in its epilogue);
+            # mma.sync: decode + merge
+            "gpu_launches": (1 if info["kernel"] == mla.KERNEL_TCGEN05 else 2) * args.steps,
             "wall_s_timed": wall, "plan_us": plan_us,
             "kernel": info["kernel"], "plan": info,
             "step_us_p10_p50_p90": [float(np.percentile(step_ms, q) * 1000) for q in (10, 50, 90)]}

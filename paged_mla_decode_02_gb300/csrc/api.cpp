@@ -39,7 +39,8 @@ struct mla_plan_s {
   cudaEvent_t upload_done = nullptr; // the pinned blob may be rewritten once this fired
 
   float* d_o_part = nullptr;         // [slots_cap, H, 512]
-  float* d_lse_part = nullptr;       // [slots_cap, H]
+  float* d_lse_part = nullptr;       // [slots_cap, 2, H]
+  int32_t* d_counters = nullptr;     // [max_batch, 4]: split-request counts (tcgen05)
   int32_t* d_err = nullptr;
 
   // Staging of mla_decode_run_host (allocated on first use).
@@ -87,6 +88,7 @@ void release(mla_plan_t p) {
   if (p->upload_done) cudaEventDestroy(p->upload_done);
   if (p->d_o_part) cudaFree(p->d_o_part);
   if (p->d_lse_part) cudaFree(p->d_lse_part);
+  if (p->d_counters) cudaFree(p->d_counters);
   if (p->d_err) cudaFree(p->d_err);
   if (p->d_q) cudaFree(p->d_q);
   if (p->d_res) cudaFree(p->d_res);
@@ -209,12 +211,15 @@ mla_status_t mla_plan_create(int max_batch, int num_heads, int kernel, mla_plan_
   p->off_merge = align16(p->off_wptr + sizeof(int32_t) * (p->n_workers + 1));
   p->blob_bytes = align16(p->off_merge + sizeof(MergeEntry) * p->merge_cap);
   const size_t o_bytes = sizeof(float) * static_cast<size_t>(p->slots_cap) * num_heads * kDCkv;
-  const size_t l_bytes = sizeof(float) * static_cast<size_t>(p->slots_cap) * num_heads;
+  const size_t l_bytes = sizeof(float) * static_cast<size_t>(p->slots_cap) * 2 * num_heads;
+  const size_t c_bytes = sizeof(int32_t) * static_cast<size_t>(max_batch) * 4;
   if ((e = cudaMalloc(&p->d_blob, p->blob_bytes)) != cudaSuccess ||
       (e = cudaMallocHost(&p->h_blob, p->blob_bytes)) != cudaSuccess ||
       (e = cudaEventCreateWithFlags(&p->upload_done, cudaEventDisableTiming)) != cudaSuccess ||
       (e = cudaMalloc(reinterpret_cast<void**>(&p->d_o_part), o_bytes)) != cudaSuccess ||
       (e = cudaMalloc(reinterpret_cast<void**>(&p->d_lse_part), l_bytes)) != cudaSuccess ||
+      (e = cudaMalloc(reinterpret_cast<void**>(&p->d_counters), c_bytes)) != cudaSuccess ||
+      (e = cudaMemset(p->d_counters, 0, c_bytes)) != cudaSuccess ||
       (e = cudaMalloc(reinterpret_cast<void**>(&p->d_err), sizeof(int32_t))) != cudaSuccess ||
       (e = cudaMemset(p->d_err, 0, sizeof(int32_t))) != cudaSuccess ||
       (e = cudaMemset(p->d_blob, 0, p->blob_bytes)) != cudaSuccess) {
@@ -282,6 +287,11 @@ mla_status_t mla_decode_plan(mla_plan_t plan, const int32_t* kv_indptr_host,
   if ((e = cudaMemcpyAsync(plan->d_blob, plan->h_blob, plan->blob_bytes, cudaMemcpyHostToDevice,
                            s)) != cudaSuccess)
     return cuda_fail(plan, e, "plan upload");
+  // The tcgen05 kernel leaves its arrival counters at zero; a launch that
+  // stopped on a device error may not have, so every plan starts from zero.
+  if ((e = cudaMemsetAsync(plan->d_counters, 0, sizeof(int32_t) * 4 * plan->max_batch, s)) !=
+      cudaSuccess)
+    return cuda_fail(plan, e, "counter reset");
   if ((e = cudaEventRecord(plan->upload_done, s)) != cudaSuccess)
     return cuda_fail(plan, e, "cudaEventRecord");
 
@@ -332,6 +342,8 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
   a.lse = lse;
   a.o_part = plan->d_o_part;
   a.lse_part = plan->d_lse_part;
+  a.merge = reinterpret_cast<const MergeEntry*>(blob + plan->off_merge);
+  a.counters = plan->d_counters;
   a.err = plan->d_err;
   a.num_pages = num_pages;
   a.num_heads = plan->num_heads;
@@ -364,6 +376,8 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
   if (plan->prof_stop && (e = cudaEventRecord(plan->prof_stop, s)) != cudaSuccess)
     return cuda_fail(plan, e, "cudaEventRecord");
 
+  // The tcgen05 kernel combines split requests and fills empty ones itself.
+  if (plan->kernel != MLA_KERNEL_MMA_SYNC) return MLA_OK;
   MergeArgs m{};
   m.merge = reinterpret_cast<const MergeEntry*>(blob + plan->off_merge);
   m.params = a.params;

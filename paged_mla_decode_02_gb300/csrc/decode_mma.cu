@@ -294,9 +294,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
     }
   }
   if (warp == 0 && (lane & 3) == 0) {
-    float* dst = partial ? a.lse_part : a.lse;
-    if (g0 < H) dst[row0] = lse0;
-    if (g1 < H) dst[row1] = lse1;
+    if (partial) {
+      if (g0 < H) a.lse_part[lse_part_offset(u.out_slot, 0, g0, H)] = lse0;
+      if (g1 < H) a.lse_part[lse_part_offset(u.out_slot, 0, g1, H)] = lse1;
+    } else {
+      if (g0 < H) a.lse[row0] = lse0;
+      if (g1 < H) a.lse[row1] = lse1;
+    }
   }
 }
 

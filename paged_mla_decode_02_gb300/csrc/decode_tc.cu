@@ -107,7 +107,8 @@ enum Bar {
   kPvDone0 = kPReady0 + 2,   // 2, by tile parity: this CTA's PV of the tile completed
   kOFree = kPvDone0 + 2, kFinal, kFinalPv,
   kXchg0, kMaxX0 = kXchg0 + 4,   // 4, per lane quadrant: the two warps' row maxima posted
-  kNumBars = kMaxX0 + 4
+  kMergeB = kMaxX0 + 4,   // split unit: merge-or-publish decided (flag in shared memory)
+  kNumBars
 };
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
 
@@ -117,6 +118,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P values stay below 2^8
+constexpr int kMergeRegs = 8;               // split request slots whose weights stay in registers
 
 __device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
 
@@ -174,6 +176,42 @@ __device__ __forceinline__ void load_q_tmem(const DecodeArgs& a, int req, int r,
 
 __device__ __forceinline__ int tiles_of(const WorkUnit& u) { return (u.tok_end - u.tok_begin + kT - 1) / kT; }
 
+// 32 consecutive dims of one output row: 32-byte stores when out is 32-byte
+// aligned (rows then are too), else 16-byte stores.
+template <bool kOutF32>
+__device__ __forceinline__ void store_out_row32(void* out, size_t orow, int d0, const float (&v)[32],
+                                                bool out32) {
+  uint32_t w[32];
+  if (kOutF32) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(v[j]);
+    float* dst = static_cast<float*>(out) + orow * kDCkv + d0;
+    if (out32) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) st_global_v8(dst + 8 * j, &w[8 * j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        reinterpret_cast<uint4*>(dst)[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * e], v[2 * e + 1]);
+      w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(out) + orow * kDCkv + d0;
+    if (out32) {
+      st_global_v8(dst, &w[0]);
+      st_global_v8(dst + 16, &w[8]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        reinterpret_cast<uint4*>(dst)[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    }
+  }
+}
+
 template <bool kOutF32>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ TcMaps maps) {
@@ -201,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t cnt = 1;
       if (i == kQTmemFull || i == kSFree || i == kPReady0 || i == kPReady0 + 1 || i == kOFree)
         cnt = kSoftmaxWarps;
-      if (i == kPFree0 || i == kPFree0 + 1 || i >= kXchg0) cnt = 2;   // kXchg*, kMaxX*
+      if (i == kPFree0 || i == kPFree0 + 1 || (i >= kXchg0 && i < kMergeB)) cnt = 2;   // kXchg*, kMaxX*
       mbar_init(bar_addr(base, i), cnt);
     }
     fence_barrier_init();
@@ -430,17 +468,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t vphase = 0;
     uint32_t tail_par = 0;   // per V slot: parity of its next tail-chunk release
     bool ok = true;
+    const volatile int* merge_flag = reinterpret_cast<const volatile int*>(sm + kOffBar + kNumBars * 8 + 8);
+    // After unit v's epilogue released O (kOFree): if v is a split unit that
+    // does not merge, its stored share becomes visible GPU-wide and is counted
+    // as published (the fence orders the softmax warps' stores, seen through
+    // the barrier, before the count).
+    auto publish = [&](const WorkUnit& v) {
+      if (v.n_slots > 0 && *merge_flag == 0 && lane == 0) {
+        __threadfence();
+        atomicAdd(a.counters + 4 * v.req + 2 + half, 1);
+      }
+    };
     for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
       const WorkUnit u = a.units[ui];
       const int n = tiles_of(u);
+      // the first PV of a unit overwrites O: the previous epilogue must be done
+      if (uidx > 0) {
+        if (!(ok = mbar_wait_warp(bar_addr(base, kOFree), (uidx - 1) & 1, abort_flag))) break;
+        publish(a.units[ui - 1]);
+      }
       for (int i = 0; i < n && ok; ++i, ++g) {
         const int valid = min(kT, u.tok_end - (u.tok_begin + i * kT));
         const int nch = (valid + kVChunkTok - 1) / kVChunkTok;
         if (!(ok = mbar_wait_warp(bar_addr(base, kPReady0 + (g & 1)), (g >> 1) & 1, abort_flag)))
-          break;
-        // the first PV of a unit overwrites O: the previous epilogue must be done
-        if (i == 0 && uidx > 0 &&
-            !(ok = mbar_wait_warp(bar_addr(base, kOFree), (uidx - 1) & 1, abort_flag)))
           break;
         tc_fence_after();
         for (int c = 0; c < nch; ++c) {
@@ -476,6 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit_mc(bar_addr(base, kPFree0 + (g & 1)), static_cast<uint16_t>(0x3), issue);
       }
     }
+    if (ok && uidx > 0) {   // the last unit's share
+      if ((ok = mbar_wait_warp(bar_addr(base, kOFree), (uidx - 1) & 1, abort_flag)))
+        publish(a.units[u1 - 1]);
+    }
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
     mma_commit(bar_addr(base, kFinalPv), issue);
     if (lane == 0) mbar_wait_drain(bar_addr(base, kFinalPv), 0);
@@ -494,8 +548,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pswz = r & 7;
     const uint32_t info_off = (hc * 128 + r) * kInfoRow;
     const uint32_t recv_bar_remote = map_to_rank(bar_addr(base, kPRecv), peer);
-    int g = 0, gl = 0, nrecv = 0, uidx = 0;
+    int g = 0, gl = 0, nrecv = 0, uidx = 0, nsplit = 0;
     bool ok = true;
+    volatile int* merge_flag = reinterpret_cast<volatile int*>(sm + kOffBar + kNumBars * 8 + 8);
+    // Requests without tokens: out = 0, lse = -inf (merge entries with no
+    // slots, dealt round-robin over the workers).
+    if (worker < prm.n_workers && r < H) {
+      for (int e = worker; e < prm.n_merge; e += prm.n_workers) {
+        const MergeEntry me = a.merge[e];
+        if (me.n_slots != 0) continue;
+        const size_t orow = static_cast<size_t>(me.req) * H + r;
+        const int d0 = 256 * half + 128 * hc;
+        uint4* dst = kOutF32 ? reinterpret_cast<uint4*>(static_cast<float*>(a.out) + orow * kDCkv + d0)
+                             : reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDCkv + d0);
+#pragma unroll 4
+        for (int j = 0; j < (kOutF32 ? 32 : 16); ++j) dst[j] = make_uint4(0, 0, 0, 0);
+        if (half == 0 && hc == 0) a.lse[orow] = -INFINITY;
+      }
+    }
     if (u0 < u1) {
       load_q_tmem(a, a.units[u0].req, r, hc, lane_addr);
       tc_fence_before();
@@ -506,6 +576,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const WorkUnit u = a.units[ui];
       const int n = tiles_of(u);
       const int g0 = g;
+      // split request: the unit counts itself one tile before its last (near
+      // its end, so the last to count is about the last to finish); the result
+      // is first needed a tile later, which hides the atomic's latency
+      int end_count = 0;
+      const int i_count = max(n - 2, 0);
       // references: m_last = of the last applied tile, m_prev = the one before
       float m_last = -INFINITY, m_prev = -INFINITY;
       float lx = 0.f, lr = 0.f;                        // this warp's token half
@@ -513,6 +588,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       float own_m = -INFINITY, own_lx = 0.f, own_lr = 0.f;
       for (int i = 0; i <= n && ok; ++i) {
         const bool own_now = i < n && ((g0 + i) & 1) == half;
+        if (u.n_slots > 0 && warp == 3 && lane == 0) {
+          if (i == i_count) end_count = atomicAdd(a.counters + 4 * u.req + half, 1);
+          if (i == i_count + 1 && end_count == u.n_slots - 1) {
+            // this unit will merge: bring the other units' shares of this CTA
+            // half (contiguous 32 x H x 32 bytes per slot) into L2 meanwhile
+            for (int k = u.slot0; k < u.slot0 + u.n_slots; ++k) {
+              if (k == u.out_slot) continue;
+              const char* src = reinterpret_cast<const char*>(a.o_part + part_offset(k, 0, 256 * half, H));
+              for (int off = 0; off < 32 * H * 32; off += 32768)
+                bulk_prefetch_l2(src + off, min(32768, 32 * H * 32 - off));
+            }
+          }
+        }
         uint32_t pk[32];
         if (own_now) {
           // ---------- own tile g0 + i: scores -> P (registers) ----------
@@ -710,62 +798,160 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_addr(base, kXchg0 + quad));
       if (!(ok = mbar_wait_warp(bar_addr(base, kXchg0 + quad), 1, abort_flag))) break;
-      const bool partial = u.out_slot >= 0;
+      // A split request is combined by its unit that counted last (warp 3
+      // lane 0 holds that count): the others publish their
+      // share (partial O and lse of each CTA half), the last one waits for
+      // them -- they counted first, so they are running and wait on nothing
+      // of this unit -- and merges them with its own O straight from TMEM.
+      const bool split = u.n_slots > 0;
+      bool last = false;
+      if (split) {
+        if (warp == 3 && lane == 0) {
+          const bool me_last = end_count == u.n_slots - 1;
+          if (me_last) {
+            int32_t* cnt = a.counters + 4 * u.req;
+            if (!wait_count_acquire(cnt + 2 + half, u.n_slots - 1, abort_flag)) {
+              report_error(a.err, kErrTimeout);
+            } else {
+              cnt[half] = 0;       // every unit counted and published: clean for the next launch
+              cnt[2 + half] = 0;
+            }
+          }
+          *merge_flag = me_last;
+          mbar_arrive(bar_addr(base, kMergeB));
+        }
+        if (!(ok = mbar_wait_warp(bar_addr(base, kMergeB), nsplit & 1, abort_flag))) break;
+        ++nsplit;
+        last = *merge_flag != 0;
+      }
       // rows of out are 32-byte aligned when out is (the ABI asks for 16)
       const bool out32 = (reinterpret_cast<uintptr_t>(a.out) & 31) == 0;
       const size_t orow = static_cast<size_t>(u.req) * H + r;
+      const float lse_own = (m_last + log2f(lx_all)) * kLn2;
       const float inv = (r < H) ? a.kv_scale / lr_all : 0.f;
-#pragma unroll 1
-      for (int cc = 4 * hc; cc < 4 * hc + 4; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(lane_addr + kColO + 32 * cc, o);
-        tmem_ld_wait();
+      if (last) {
+        // Slots are combined in slot order, this unit's own slot (from TMEM,
+        // O * inv: bit-identical to the share it would have stored) in its
+        // place, so the result does not depend on which unit merges.
+        // The published shares are visible here: warp 3 saw their counts with
+        // an acquire load and released that to these warps through kMergeB;
+        // they are read from L2 (.cg), past this SM's L1.
+        const int rr = r < H ? r : H - 1;
+        const int ns = u.n_slots, own = u.out_slot - u.slot0;
+        auto slot_lse = [&](int k) {   // k: index within the request's slots
+          return k == own ? lse_own : __ldcg(a.lse_part + lse_part_offset(u.slot0 + k, half, rr, H));
+        };
+        // the first kMergeRegs slot lse values are loaded together (static
+        // indices keep them in registers); more slots are re-read
+        float lk[kMergeRegs];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * inv);
-        if (r < H) {
-          const int d0 = 256 * half + 32 * cc;
-          if (partial) {
-            // lanes hold consecutive heads: each store is 512 contiguous bytes
+        for (int k = 0; k < kMergeRegs; ++k) lk[k] = k < ns ? slot_lse(k) : -INFINITY;
+        float M = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kMergeRegs; ++k) M = fmaxf(M, lk[k]);
+        for (int k = kMergeRegs; k < ns; ++k) M = fmaxf(M, slot_lse(k));
+        float W = 0.f;
+#pragma unroll
+        for (int k = 0; k < kMergeRegs; ++k) W += k < ns ? __expf(lk[k] - M) : 0.f;
+        for (int k = kMergeRegs; k < ns; ++k) W += __expf(slot_lse(k) - M);
+        const float winv = 1.f / W;
+        auto weight = [&](int k) { return __expf(slot_lse(k) - M) * winv; };
+        if (ns == 2) {
+          // the common split in two: the other share's loads and the TMEM
+          // load of each chunk are in flight together
+          const int other = u.slot0 + (1 - own);
+          const float w0 = __expf(lk[0] - M) * winv, w1 = __expf(lk[1] - M) * winv;
+#pragma unroll 1
+          for (int cc = 4 * hc; cc < 4 * hc + 4; ++cc) {
+            const int d0 = 256 * half + 32 * cc;
+            uint32_t o[32];
+            tmem_ld32(lane_addr + kColO + 32 * cc, o);   // in flight with the loads below
+            float4 q[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-              *reinterpret_cast<uint4*>(a.o_part + part_offset(u.out_slot, r, d0 + 4 * j, H)) =
-                  make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-          } else if (kOutF32) {
-            float* dst = static_cast<float*>(a.out) + orow * kDCkv + d0;
-            if (out32) {
+              q[j] = __ldcg(reinterpret_cast<const float4*>(a.o_part + part_offset(other, rr, d0 + 4 * j, H)));
+            tmem_ld_wait();
+            float acc[32];
 #pragma unroll
-              for (int j = 0; j < 4; ++j) st_global_v8(dst + 8 * j, &o[8 * j]);
-            } else {
+            for (int j = 0; j < 8; ++j) {
+              const float vo[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                reinterpret_cast<uint4*>(dst)[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+              for (int e = 0; e < 4; ++e) {
+                const float mine = __uint_as_float(o[4 * j + e]) * inv;
+                acc[4 * j + e] = own == 0 ? fmaf(w1, vo[e], w0 * mine) : fmaf(w1, mine, w0 * vo[e]);
+              }
             }
-          } else {
-            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + orow * kDCkv + d0;
-            uint32_t w[16];
+            if (r < H) store_out_row32<kOutF32>(a.out, orow, d0, acc, out32);
+          }
+        } else {
+#pragma unroll 1
+          for (int cc = 4 * hc; cc < 4 * hc + 4; ++cc) {
+            const int d0 = 256 * half + 32 * cc;
+            float acc[32];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const __nv_bfloat162 b2 =
-                  __floats2bfloat162_rn(__uint_as_float(o[2 * e]), __uint_as_float(o[2 * e + 1]));
-              w[e] = *reinterpret_cast<const uint32_t*>(&b2);
+            for (int j = 0; j < 32; ++j) acc[j] = 0.f;
+#pragma unroll 1
+            for (int k = 0; k < ns; ++k) {
+              const float w = weight(k);
+              float v[32];
+              if (k == own) {
+                uint32_t o[32];
+                tmem_ld32(lane_addr + kColO + 32 * cc, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(o[j]) * inv;
+              } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                  const float4 q = __ldcg(reinterpret_cast<const float4*>(
+                      a.o_part + part_offset(u.slot0 + k, rr, d0 + 4 * j, H)));
+                  v[4 * j] = q.x;
+                  v[4 * j + 1] = q.y;
+                  v[4 * j + 2] = q.z;
+                  v[4 * j + 3] = q.w;
+                }
+              }
+#pragma unroll
+              for (int j = 0; j < 32; ++j) acc[j] = fmaf(w, v[j], acc[j]);
             }
-            if (out32) {
-              st_global_v8(dst, &w[0]);
-              st_global_v8(dst + 16, &w[8]);
-            } else {
+            if (r < H) store_out_row32<kOutF32>(a.out, orow, d0, acc, out32);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_addr(base, kOFree));
+        if (half == 0 && hc == 0 && r < H) a.lse[orow] = M + __logf(W);
+      } else {
+#pragma unroll 1
+        for (int cc = 4 * hc; cc < 4 * hc + 4; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(lane_addr + kColO + 32 * cc, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * inv);
+          if (r < H) {
+            const int d0 = 256 * half + 32 * cc;
+            if (split) {
+              // lanes hold consecutive heads: each store covers 1 KB of contiguous memory
 #pragma unroll
               for (int j = 0; j < 4; ++j)
-                reinterpret_cast<uint4*>(dst)[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                st_global_v8(a.o_part + part_offset(u.out_slot, r, d0 + 8 * j, H), &o[8 * j]);
+            } else {
+              float v[32];
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(o[j]);
+              store_out_row32<kOutF32>(a.out, orow, d0, v, out32);
             }
           }
         }
+        if (split && hc == 0 && r < H) a.lse_part[lse_part_offset(u.out_slot, half, r, H)] = lse_own;
+        // O may be overwritten now; for a split unit this also hands the
+        // stored share to the PV warp, which publishes it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_addr(base, kOFree));
+        if (!split && half == 0 && hc == 0 && r < H) a.lse[orow] = lse_own;
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(base, kOFree));
-      if (half == 0 && hc == 0 && r < H)
-        (partial ? a.lse_part + static_cast<size_t>(u.out_slot) * H + r : a.lse + orow)[0] =
-            (m_last + log2f(lx_all)) * kLn2;
     }
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
   }

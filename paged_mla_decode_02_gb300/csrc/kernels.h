@@ -20,7 +20,10 @@ struct DecodeArgs {
   void* out;                   // [B,H,512] bf16 or fp32
   float* lse;                  // [B,H]
   float* o_part;               // partial outputs, fp32, layout of part_offset()
-  float* lse_part;             // [slots,H]
+  float* lse_part;             // [slots][2][H]: one copy per CTA half (lse_part_offset)
+  const MergeEntry* merge;     // split and empty requests
+  int32_t* counters;           // [max_batch][4]: per CTA half, units started and
+                               // shares published; zero between launches
   int32_t* err;
   int num_pages;
   int num_heads;
@@ -30,13 +33,19 @@ struct DecodeArgs {
 };
 
 // Element (slot, head h, dim d) of the fp32 partial outputs.  Dims are
-// grouped by four and the heads of a group are adjacent:
-//   [slot][d / 4][h][d % 4]
-// so a warp holding 32 consecutive heads x 4 dims stores (or the merge
-// loads) 512 contiguous bytes, where a [slot][h][d] layout would touch 32
-// separate rows per instruction.
+// grouped by eight and the heads of a group are adjacent:
+//   [slot][d / 8][h][d % 8]
+// so a warp holding 32 consecutive heads x 8 dims stores (or loads) 1 KB of
+// contiguous memory with 32-byte accesses, where a [slot][h][d] layout would
+// touch 32 separate rows per instruction.
 __host__ __device__ inline size_t part_offset(int slot, int h, int d, int H) {
-  return ((static_cast<size_t>(slot) * (kDCkv / 4) + d / 4) * H + h) * 4 + (d & 3);
+  return ((static_cast<size_t>(slot) * (kDCkv / 8) + d / 8) * H + h) * 8 + (d & 7);
+}
+
+// Log-sum-exp of partial slot `slot`, head h: the tcgen05 kernel's two CTA
+// halves each keep a copy (half 0's is the one the merge kernel reads).
+__host__ __device__ inline size_t lse_part_offset(int slot, int half, int h, int H) {
+  return (static_cast<size_t>(slot) * 2 + half) * H + h;
 }
 
 struct MergeArgs {
@@ -66,7 +75,8 @@ cudaError_t launch_decode_tc(const DecodeArgs& a, const TcMaps& maps, bool out_f
 // (the persistent grid uses at most that many workers).
 cudaError_t decode_tc_max_workers(int* workers);
 
-// LSE merge of split partials (and zero-fill of empty requests).
+// LSE merge of split partials (and zero-fill of empty requests); the mma.sync
+// path only -- the tcgen05 kernel merges in its own epilogue.
 cudaError_t launch_merge(const MergeArgs& a, bool out_f32, cudaStream_t s);
 
 }  // namespace mla

@@ -35,9 +35,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
   if (t < H) {
     float M = -INFINITY, wsum = 0.f;
     for (int i = 0; i < me.n_slots; ++i)
-      M = fmaxf(M, a.lse_part[static_cast<size_t>(me.first_slot + i) * H + t]);
+      M = fmaxf(M, a.lse_part[lse_part_offset(me.first_slot + i, 0, t, H)]);
     for (int i = 0; i < me.n_slots; ++i)
-      wsum += __expf(a.lse_part[static_cast<size_t>(me.first_slot + i) * H + t] - M);
+      wsum += __expf(a.lse_part[lse_part_offset(me.first_slot + i, 0, t, H)] - M);
     s_max[t] = M;
     s_inv[t] = me.n_slots > 0 ? 1.f / wsum : 0.f;
     if (dq == 0) a.lse[static_cast<size_t>(me.req) * H + t] = me.n_slots > 0 ? M + __logf(wsum) : -INFINITY;
@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
     for (int k = 0; k < kItems; ++k) {
       if (dk[k] >= 0) {
         o[k] = *reinterpret_cast<const float4*>(a.o_part + part_offset(slot, hk[k], dk[k], H));
-        l[k] = a.lse_part[static_cast<size_t>(slot) * H + hk[k]];
+        l[k] = a.lse_part[lse_part_offset(slot, 0, hk[k], H)];
       }
     }
 #pragma unroll

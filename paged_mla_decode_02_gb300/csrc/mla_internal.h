@@ -25,8 +25,10 @@ struct WorkUnit {
   int32_t out_slot;    // -1: the unit covers the whole request -> final out/lse
   int32_t page_base;   // kv_indptr[req]: first entry of the request in kv_indices
   int32_t kv_len;      // tokens of the request
+  int32_t slot0;       // split request: its first partial slot (its units use
+  int32_t n_slots;     //   slot0 .. slot0 + n_slots - 1); 0, 0 otherwise
 };
-static_assert(sizeof(WorkUnit) == 24, "WorkUnit layout");
+static_assert(sizeof(WorkUnit) == 32, "WorkUnit layout");
 
 // A request whose partial results (slots first_slot .. first_slot+n_slots-1)
 // the merge kernel combines; n_slots == 0 marks an empty request.

@@ -102,6 +102,8 @@ void partition_batch(const int32_t* kv_indptr, const int32_t* kv_len, int batch,
       u.out_slot = -1;
       u.page_base = kv_indptr[req];
       u.kv_len = kv_len[req];
+      u.slot0 = 0;
+      u.n_slots = 0;
       out->units.push_back(u);
       quota -= take;
       tile += take;
@@ -129,10 +131,14 @@ void partition_batch(const int32_t* kv_indptr, const int32_t* kv_len, int batch,
   }
   // Units of one request are consecutive in the unit list (the walk above is
   // in tile order), so the k-th unit of request b takes slot first_slot + k.
-  std::vector<int> next(batch, 0);
-  for (const MergeEntry& m : out->merge) next[m.req] = m.first_slot;
+  std::vector<int> first(batch, 0), next(batch, 0);
+  for (const MergeEntry& m : out->merge) first[m.req] = next[m.req] = m.first_slot;
   for (WorkUnit& u : out->units)
-    if (n_units[u.req] >= 2) u.out_slot = next[u.req]++;
+    if (n_units[u.req] >= 2) {
+      u.out_slot = next[u.req]++;
+      u.slot0 = first[u.req];
+      u.n_slots = n_units[u.req];
+    }
   out->n_slots = slot;
 }
 

@@ -308,6 +308,24 @@ __device__ __forceinline__ void cluster_sync_all() {
 }
 // Stores into another CTA's shared memory whose completion is counted, in
 // bytes, on an mbarrier of that CTA (remote addresses from map_to_rank).
+// Spin (bounded, with a short sleep) until the GPU-scope value at p reaches
+// target; the load that sees it has acquire semantics.  False on timeout or
+// when another warp of the CTA gave up.
+__device__ __forceinline__ bool wait_count_acquire(const int* p, int target, volatile int* abort_flag) {
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      return false;
+    }
+    __nanosleep(256);
+  }
+}
+
 // 2^x on the special function unit (approximate; results below 2^-126
 // flush to zero, 2^-inf = 0).
 __device__ __forceinline__ float fast_exp2(float x) {

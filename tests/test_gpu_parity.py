@@ -263,3 +263,26 @@ def test_full_size_config_sampled(kernel, cfg):
     assert np.isfinite(out).all() and np.isfinite(lse).all()
     del d
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("cfg, lens, heads, P", [
+    ("split_many", [4000, 1, 777], 128, 16),   # a request spread over dozens of units
+    ("deepseek", None, None, None),            # every request split in two
+])
+def test_split_requests_deterministic(kernel, cfg, lens, heads, P):
+    # Split requests are combined by whichever unit finishes last; the result
+    # must not depend on which one that is: repeated runs are bit-identical.
+    x = _config(cfg) if lens is None else I.make_inputs(cfg, lens, heads, P, seed=13)
+    d = to_device(x)
+    dec = mla.MLADecoder(x.batch, x.num_heads, kernel)
+    o0, l0 = run_decode(x, d, kernel, torch.float32, decoder=dec)
+    for _ in range(3):
+        o1, l1 = run_decode(x, d, kernel, torch.float32, decoder=dec)
+        assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    dec.close()
+    reqs = _sample(x, 3) if x.batch > 8 else list(range(x.batch))
+    ref_out, ref_lse = O.mla_decode_inputs(x, requests=reqs)
+    assert_parity(o0[reqs], l0[reqs], ref_out, ref_lse, f"{cfg} {reqs}")
+    del d
+    torch.cuda.empty_cache()
