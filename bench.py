@@ -73,6 +73,32 @@ def peaks() -> tuple[float, float, float, str]:
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
 
 
+PROFILE = os.path.join(ROOT, "profiles", "decode_tc_deepseek.md")
+KERNEL_SOURCES = ["decode_tc.cu", "tc_utils.cuh", "device_utils.cuh", "kernels.h", "mla_internal.h"]
+
+
+def profiled_traffic(workload: str) -> float | None:
+    """DRAM bytes per launch of the tcgen05 kernel from the committed ncu
+    summary, or None when the summary is for another workload or the kernel
+    sources changed since it was taken (hash recorded beside the figure)."""
+    import hashlib
+    if workload != "deepseek" or not os.path.exists(PROFILE):
+        return None
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(f.encode())
+        with open(os.path.join(ROOT, "paged_mla_decode_02_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    vals = {}
+    for line in open(PROFILE):
+        if ":" in line and line.split(":", 1)[0] in ("source_sha256", "dram_bytes_per_launch"):
+            k, v = line.split(":", 1)
+            vals[k] = v.strip()
+    if vals.get("source_sha256") != h.hexdigest() or "dram_bytes_per_launch" not in vals:
+        return None
+    return float(vals["dram_bytes_per_launch"])
+
+
 def oracle_sample(x, budget_s: float):
     """Float64 oracle on as many requests as fit in ~budget_s; returns (us per batch, n, secs)."""
     from oracle import mla_oracle as O
@@ -307,7 +333,9 @@ def main() -> None:
             "peak": hbm if bound == "hbm" else bf,
             "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
             "peak_source": peak_src,
-            "traffic": None,
+            "traffic": (profiled_traffic(args.config)
+                        if info["kernel"] == mla.KERNEL_TCGEN05 else None),
+            "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
             "kernel": "mla_decode (split-KV decode kernel)",
             "kernel_us": kern_us,
             "algorithmic_bytes": nbytes, "algorithmic_flops": flops,

@@ -70,7 +70,7 @@ typedef struct {
   int32_t num_workers;        /* persistent workers (CTA pairs for tcgen05, CTAs for mma.sync) */
   int32_t num_units;          /* work units (contiguous tile ranges of one request) */
   int32_t num_partial_slots;  /* split partial results written to the workspace */
-  int32_t num_merge;          /* requests combined by the merge kernel (incl. empty requests) */
+  int32_t num_merge;          /* split and empty requests (merged / zero-filled) */
   int32_t total_tiles;        /* KV tiles (of tile_tokens tokens) over the batch */
   int32_t batch;
   int32_t num_heads;
@@ -82,7 +82,8 @@ typedef struct {
 
 /*
  * Create a plan on the CURRENT CUDA device.  Allocates (once, here) the
- * work-unit buffers, the merge map and the split-KV partial workspace sized
+ * work-unit buffers, the merge map, the split-request counters and the
+ * split-KV partial workspace sized
  * for up to max_batch requests of num_heads heads, so later plans and runs
  * never allocate.  num_heads in 1..128.  kernel: an mla_kernel_t.
  * On success *out receives the plan; the caller releases it with
@@ -125,8 +126,12 @@ mla_status_t mla_decode_plan(mla_plan_t plan, const int32_t* kv_indptr_host,
  *   kv_scale  per-tensor dequantisation scale of the cache (use 1.0 for bf16)
  *   out       [batch, num_heads, 512]   out_dtype (BF16 or FP32)
  *   lse       [batch, num_heads]        fp32, natural log
- * Launches the decode kernel and, when some request was split, the merge
- * kernel.  No allocation, no synchronisation, no host reads: capturable in a
+ * Launches the decode kernel; with the tcgen05 kernel that is the only launch
+ * (a request split across workers is combined by log-sum-exp in the epilogue
+ * of its last-finishing unit, requests with kv_len 0 are filled by the same
+ * kernel), with the mma.sync kernel a merge kernel follows.  The combination
+ * order is fixed, so repeated runs give bit-identical results.
+ * No allocation, no synchronisation, no host reads: capturable in a
  * CUDA graph (the graph keeps the pointers; re-planning with the same plan
  * between replays is allowed).  A page id outside [0, num_pages) found by the
  * kernel is recorded and reported by mla_plan_check_status; that page is read
@@ -163,7 +168,7 @@ mla_status_t mla_plan_check_status(mla_plan_t plan);
  * Profiling hook: when set (non-NULL cudaEvent_t handles created by the
  * caller on the plan's device), every mla_decode_run records start_event on
  * its stream immediately before the decode kernel and stop_event immediately
- * after it (before the merge kernel), so the caller can time the decode
+ * after it (before the mma.sync path's merge kernel), so the caller can time the decode
  * kernel alone with cudaEventElapsedTime.  Pass NULLs to stop recording.
  * The events are borrowed; they must outlive the runs that record them.
  */
