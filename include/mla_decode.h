@@ -158,6 +158,43 @@ mla_status_t mla_decode_run_host(mla_plan_t plan, const void* q_nope_host,
                                  float* lse_host, void* stream);
 
 /*
+ * Plan + run one batch without any allocation, for callers that may not
+ * allocate device memory after start-up (e.g. a serving process whose
+ * allocator owns all memory).  The pages have no counterpart to this call; it
+ * is an engineering variant of mla_decode_plan + mla_decode_run on the
+ * tcgen05 kernel.
+ *   Everything besides the caller's tensors -- work units, split partials,
+ *   split-request counters, the device status word -- lives in one fixed
+ *   48 MiB scratch array inside the library; the work-unit list is built in
+ *   static host memory.  Nothing is allocated (no cudaMalloc, no pinned host
+ *   memory, no heap allocation on success).
+ *   Limits: batch <= 4096 (else MLA_ERR_CAPACITY, before any device work); the
+ *   batch's partials and work units must fit the scratch (else
+ *   MLA_ERR_CAPACITY; with 128 heads they take about 38 MiB at most on a
+ *   152-SM GPU).  bf16 q and caches only; head dims 512 / 64.
+ *   Arguments as for mla_decode_plan / mla_decode_run (kv_indptr_host and
+ *   kv_len_host on the host, everything else on the device; kv_indices_dev is
+ *   only read by this call's kernel).
+ *   The first call on a device does the setup (looks up the scratch address,
+ *   queries the SM count and kernel residency); make it before any work that
+ *   must not see those calls.
+ *   Each call zeroes, on `stream`, the counters and the status word the
+ *   kernel expects at zero, uploads its work units and launches one kernel;
+ *   it returns without waiting unless check_status is nonzero, in which case
+ *   it synchronises `stream` and returns MLA_ERR_DEVICE_BOUNDS /
+ *   MLA_ERR_DEVICE_TIMEOUT if the kernel recorded one.
+ *   The scratch and the host staging are shared by all calls in the process:
+ *   calls that overlap (other streams, other host threads) race and corrupt
+ *   each other.  Issue them one after another on one stream.
+ */
+mla_status_t mla_decode_noalloc(const int32_t* kv_indptr_host, const int32_t* kv_indices_dev,
+                                const int32_t* kv_len_host, int batch, int num_heads,
+                                int page_size, float sm_scale, const void* q_nope,
+                                const void* q_pe, const void* ckv_cache, const void* kpe_cache,
+                                float kv_scale, int num_pages, void* out, int out_dtype,
+                                float* lse, int check_status, void* stream);
+
+/*
  * Synchronise the device, then read and clear the plan's device error word.
  * Returns MLA_OK, MLA_ERR_DEVICE_TIMEOUT or MLA_ERR_DEVICE_BOUNDS (the first
  * error a kernel recorded since the last check), or MLA_ERR_CUDA.

@@ -151,6 +151,21 @@ bool encode_panels_3d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t 
 
 }  // namespace
 
+// The tcgen05 kernel's tensor maps for one batch (also used by the entry point
+// that works from static scratch memory).
+bool mla::encode_tc_maps(TcMaps* maps, const void* q_nope, const void* ckv_cache, const void* kpe_cache,
+                    int batch, int num_heads, int page_size, int num_pages) {
+  const uint64_t qrows = static_cast<uint64_t>(batch) * num_heads;
+  const uint64_t kvrows = static_cast<uint64_t>(num_pages) * page_size;
+  return encode_2d(&maps->q_nope, q_nope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qrows, kDCkv,
+                   num_heads, 64) &&
+         encode_2d(&maps->ckv_k, ckv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDCkv,
+                   page_size, 64) &&
+         encode_2d(&maps->kpe_k, kpe_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDKpe,
+                   page_size, 64) &&
+         encode_panels_3d(&maps->ckv_v, ckv_cache, kvrows, page_size >= 32 ? 32 : 16, 4);
+}
+
 extern "C" {
 
 const char* mla_status_string(mla_status_t s) {

@@ -71,6 +71,10 @@ struct TcMaps {
 };
 cudaError_t launch_decode_tc(const DecodeArgs& a, const TcMaps& maps, bool out_f32,
                              cudaStream_t s);
+// Host: the tensor maps launch_decode_tc takes, for one batch (false when the
+// driver's encoder is unavailable or rejects an argument).
+bool encode_tc_maps(TcMaps* maps, const void* q_nope, const void* ckv_cache, const void* kpe_cache,
+                    int batch, int num_heads, int page_size, int num_pages);
 // Clusters of two CTAs of the tcgen05 kernel that can be resident at once
 // (the persistent grid uses at most that many workers).
 cudaError_t decode_tc_max_workers(int* workers);

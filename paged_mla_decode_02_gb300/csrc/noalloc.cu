@@ -1,0 +1,240 @@
+// Paged MLA decode from fixed scratch memory: a call that allocates nothing.
+//
+// Who needs it.  A serving process commonly reserves nearly all device memory
+// when it starts -- the KV-cache pool plus a caching allocator that accounts
+// for every byte -- and from then on a library that calls cudaMalloc on its
+// own either fails (the memory is taken), escapes that accounting, or stalls
+// the device (cudaFree waits for all work on it).  Such callers cannot own a
+// plan object, whose buffers are allocated.  This entry point keeps everything
+// the decode needs besides the caller's tensors -- the work-unit list, the
+// split partials, the split-request counters and the device status word -- in
+// one fixed array that is part of the library image, and assembles the
+// work-unit list in static host memory.  It runs the same tcgen05 kernel as
+// mla_decode_run.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <string>
+
+#include "kernels.h"
+#include "planner.h"
+
+namespace mla {
+namespace {
+
+constexpr size_t kScratchBytes = size_t(48) << 20;   // device scratch: 48 MiB
+constexpr int kMaxBatch = 4096;                       // requests per call
+constexpr int kMaxWorkers = 512;
+constexpr int kMaxUnits = kMaxWorkers + kMaxBatch;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+struct DeviceSetup {
+  bool done;
+  unsigned char* scratch;   // device address of g_scratch on that device
+  int n_workers;
+};
+DeviceSetup g_setup[kMaxDevices];
+
+// host staging: PlanDev | units | worker_ptr | merge entries (16-byte aligned parts)
+constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+constexpr size_t kHostBlobBytes =
+    align_up(sizeof(PlanDev), 16) + align_up(sizeof(WorkUnit) * kMaxUnits, 16) +
+    align_up(sizeof(int32_t) * (kMaxWorkers + 1), 16) + sizeof(MergeEntry) * kMaxBatch;
+alignas(16) unsigned char g_host_blob[kHostBlobBytes];
+
+// The planner's partition rule (equal tile shares per worker, units cut at
+// request boundaries, consecutive slots for the units of a split request),
+// written into fixed arrays.  Returns the number of units.
+int partition_fixed(const int32_t* indptr, const int32_t* len, int batch, int n_workers,
+                    WorkUnit* units, int32_t* wptr, MergeEntry* merge, int* n_merge,
+                    int* n_slots) {
+  auto tiles_of_req = [&](int b) { return (len[b] + kTileTc - 1) / kTileTc; };
+  long long total = 0;
+  for (int b = 0; b < batch; ++b) total += tiles_of_req(b);
+  const long long base = total / n_workers, extra = total % n_workers;
+  int nu = 0, req = 0, tile = 0;
+  while (req < batch && tiles_of_req(req) == 0) ++req;
+  for (int w = 0; w < n_workers; ++w) {
+    wptr[w] = nu;
+    long long quota = base + (w < extra ? 1 : 0);
+    while (quota > 0 && req < batch) {
+      const int take = static_cast<int>(std::min<long long>(quota, tiles_of_req(req) - tile));
+      WorkUnit& u = units[nu++];
+      u.req = req;
+      u.tok_begin = tile * kTileTc;
+      u.tok_end = std::min((tile + take) * kTileTc, len[req]);
+      u.out_slot = -1;
+      u.page_base = indptr[req];
+      u.kv_len = len[req];
+      u.slot0 = 0;
+      u.n_slots = 0;
+      quota -= take;
+      tile += take;
+      if (tile == tiles_of_req(req)) {
+        tile = 0;
+        ++req;
+        while (req < batch && tiles_of_req(req) == 0) ++req;
+      }
+    }
+  }
+  wptr[n_workers] = nu;
+  // units of one request are consecutive: a run of two or more is a split request
+  int slot = 0, nm = 0, i = 0;
+  for (int b = 0; b < batch; ++b) {
+    if (tiles_of_req(b) == 0) {
+      merge[nm++] = MergeEntry{b, 0, 0};
+      continue;
+    }
+    int j = i;
+    while (j < nu && units[j].req == b) ++j;
+    if (j - i >= 2) {
+      for (int k = i; k < j; ++k) {
+        units[k].out_slot = slot + (k - i);
+        units[k].slot0 = slot;
+        units[k].n_slots = j - i;
+      }
+      merge[nm++] = MergeEntry{b, slot, j - i};
+      slot += j - i;
+    }
+    i = j;
+  }
+  *n_merge = nm;
+  *n_slots = slot;
+  return nu;
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" mla_status_t mla_decode_noalloc(
+    const int32_t* kv_indptr_host, const int32_t* kv_indices_dev, const int32_t* kv_len_host,
+    int batch, int num_heads, int page_size, float sm_scale, const void* q_nope, const void* q_pe,
+    const void* ckv_cache, const void* kpe_cache, float kv_scale, int num_pages, void* out,
+    int out_dtype, float* lse, int check_status, void* stream) {
+  // ---- arguments (host only; nothing touches the device before they pass) ----
+  std::string why;
+  if (!kv_indptr_host || !kv_len_host || batch < 0) return MLA_ERR_INVALID_ARG;
+  if (batch > kMaxBatch) return MLA_ERR_CAPACITY;
+  mla_status_t st = validate_batch(kv_indptr_host, kv_len_host, batch, kDCkv, kDKpe, page_size,
+                                   sm_scale, &why);
+  if (st != MLA_OK) return st;
+  if (num_heads < 1 || num_heads > kMaxHeads) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != MLA_DTYPE_BF16 && out_dtype != MLA_DTYPE_FP32) return MLA_ERR_UNSUPPORTED;
+  if (!q_nope || !q_pe || !ckv_cache || !kpe_cache || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (kv_indptr_host[batch] > 0 && !kv_indices_dev) return MLA_ERR_INVALID_ARG;
+  if (num_pages < 1 || !std::isfinite(kv_scale) || kv_scale <= 0.f) return MLA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ckv_cache) | reinterpret_cast<uintptr_t>(kpe_cache) |
+       reinterpret_cast<uintptr_t>(q_nope) | reinterpret_cast<uintptr_t>(q_pe) |
+       reinterpret_cast<uintptr_t>(out)) & 15)
+    return MLA_ERR_INVALID_ARG;
+
+  // ---- once per device: scratch address and worker count ----
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  DeviceSetup& su = g_setup[dev];
+  if (!su.done) {
+    void* ptr = nullptr;
+    int sms = 0, resident = 0;
+    if ((e = cudaGetSymbolAddress(&ptr, g_scratch)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess ||
+        (e = decode_tc_max_workers(&resident)) != cudaSuccess || resident < 1) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+    int nw = sms / 2 < 1 ? 1 : sms / 2;
+    if (nw > resident) nw = resident;
+    if (nw > kMaxWorkers) nw = kMaxWorkers;
+    su.scratch = static_cast<unsigned char*>(ptr);
+    su.n_workers = nw;
+    su.done = true;
+  }
+
+  // ---- partition into static host memory ----
+  const size_t off_units = align_up(sizeof(PlanDev), 16);
+  WorkUnit* units = reinterpret_cast<WorkUnit*>(g_host_blob + off_units);
+  // worker offsets and merge entries follow the units, whose count is known
+  // only after the partition: staged separately, then placed
+  int32_t wptr_tmp[kMaxWorkers + 1];
+  static MergeEntry merge_stage[kMaxBatch];
+  int n_merge = 0, n_slots = 0;
+  const int n_units = partition_fixed(kv_indptr_host, kv_len_host, batch, su.n_workers, units,
+                                      wptr_tmp, merge_stage, &n_merge, &n_slots);
+  const size_t off_wptr = align_up(off_units + sizeof(WorkUnit) * n_units, 16);
+  const size_t off_merge = align_up(off_wptr + sizeof(int32_t) * (su.n_workers + 1), 16);
+  const size_t blob_bytes = off_merge + sizeof(MergeEntry) * n_merge;
+  std::memcpy(g_host_blob + off_wptr, wptr_tmp, sizeof(int32_t) * (su.n_workers + 1));
+  std::memcpy(g_host_blob + off_merge, merge_stage, sizeof(MergeEntry) * n_merge);
+  PlanDev prm{};
+  prm.n_units = n_units;
+  prm.n_merge = n_merge;
+  prm.n_workers = su.n_workers;
+  prm.batch = batch;
+  prm.num_heads = num_heads;
+  prm.page_size = page_size;
+  prm.sm_scale = sm_scale;
+  prm.n_slots = n_slots;
+  std::memcpy(g_host_blob, &prm, sizeof(prm));
+
+  // ---- scratch layout for this call ----
+  const size_t off_opart = align_up(blob_bytes, 256);
+  const size_t off_lpart =
+      align_up(off_opart + sizeof(float) * static_cast<size_t>(n_slots) * num_heads * kDCkv, 256);
+  const size_t off_cnt =
+      align_up(off_lpart + sizeof(float) * static_cast<size_t>(n_slots) * 2 * num_heads, 256);
+  const size_t off_err = off_cnt + sizeof(int32_t) * 4 * static_cast<size_t>(batch);
+  const size_t need = off_err + sizeof(int32_t);
+  if (need > kScratchBytes) return MLA_ERR_CAPACITY;
+
+  // ---- upload, zero what must start at zero, launch ----
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned char* sc = su.scratch;
+  if ((e = cudaMemcpyAsync(sc, g_host_blob, blob_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+      (e = cudaMemsetAsync(sc + off_cnt, 0, need - off_cnt, s)) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  TcMaps maps;
+  if (!encode_tc_maps(&maps, q_nope, ckv_cache, kpe_cache, batch, num_heads, page_size, num_pages))
+    return MLA_ERR_CUDA;
+  DecodeArgs a{};
+  a.q_nope = q_nope;
+  a.q_pe = q_pe;
+  a.ckv = ckv_cache;
+  a.kpe = kpe_cache;
+  a.kv_indices = kv_indices_dev;
+  a.units = reinterpret_cast<const WorkUnit*>(sc + off_units);
+  a.worker_ptr = reinterpret_cast<const int32_t*>(sc + off_wptr);
+  a.params = reinterpret_cast<const PlanDev*>(sc);
+  a.out = out;
+  a.lse = lse;
+  a.o_part = reinterpret_cast<float*>(sc + off_opart);
+  a.lse_part = reinterpret_cast<float*>(sc + off_lpart);
+  a.merge = reinterpret_cast<const MergeEntry*>(sc + off_merge);
+  a.counters = reinterpret_cast<int32_t*>(sc + off_cnt);
+  a.err = reinterpret_cast<int32_t*>(sc + off_err);
+  a.num_pages = num_pages;
+  a.num_heads = num_heads;
+  a.kv_scale = kv_scale;
+  a.units_cap = n_units;
+  a.n_workers = su.n_workers;
+  if ((e = launch_decode_tc(a, maps, out_dtype == MLA_DTYPE_FP32, s)) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  if (!check_status) return MLA_OK;
+  int32_t err = 0;
+  if ((e = cudaMemcpyAsync(&err, a.err, sizeof(err), cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(s)) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  return err ? static_cast<mla_status_t>(err) : MLA_OK;
+}

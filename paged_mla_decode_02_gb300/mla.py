@@ -31,7 +31,8 @@ KERNELS = {"default": KERNEL_DEFAULT, "tcgen05": KERNEL_TCGEN05, "mma_sync": KER
 
 EXPORTED = ("mla_plan_create", "mla_decode_plan", "mla_decode_run", "mla_decode_run_host",
             "mla_plan_check_status", "mla_plan_info", "mla_plan_destroy", "mla_status_string",
-            "mla_plan_last_error", "mla_plan_partition_host", "mla_plan_set_profile_events")
+            "mla_plan_last_error", "mla_plan_partition_host", "mla_plan_set_profile_events",
+            "mla_decode_noalloc")
 
 
 class MLAError(RuntimeError):
@@ -93,6 +94,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_plan_partition_host.argtypes = [_I32P, _I32P, c_int, c_int, c_int, c_int, c_float,
                                             c_int, c_int, _I32P, c_int, _I32P, _I32P, c_int,
                                             _I32P]
+    lib.mla_decode_noalloc.restype = c_int
+    lib.mla_decode_noalloc.argtypes = [_I32P, _VP, _I32P, c_int, c_int, c_int, c_float, _VP, _VP,
+                                       _VP, _VP, c_float, c_int, _VP, c_int, _VP, c_int, _VP]
     _lib = lib
     return lib
 
@@ -193,6 +197,34 @@ def mla_decode_run(plan, q_nope, q_pe, ckv_cache, kpe_cache, out, lse, kv_scale:
                             float(kv_scale), num_pages, _ptr(out), _dtype_code(out, "out"),
                             _ptr(lse), _stream_handle(stream))
     _check(st, plan, "mla_decode_run")
+
+
+def mla_decode_noalloc(kv_indptr, kv_indices, kv_len, page_size: int, sm_scale: float, q_nope,
+                       q_pe, ckv_cache, kpe_cache, out, lse, kv_scale: float = 1.0,
+                       check_status: bool = True, stream=None) -> None:
+    """Plan + run one batch from the library's fixed scratch memory: the call
+    allocates no device memory (out / lse are the caller's tensors).  Calls
+    must not overlap; see mla_decode.h for the limits."""
+    lib = load_library()
+    indptr = _i32_host(kv_indptr)
+    lens = _i32_host(kv_len)
+    batch = lens.shape[0]
+    if indptr.shape[0] != batch + 1:
+        raise ValueError("kv_indptr must have batch + 1 entries")
+    for name, t in (("q_nope", q_nope), ("q_pe", q_pe), ("ckv_cache", ckv_cache),
+                    ("kpe_cache", kpe_cache), ("out", out), ("lse", lse)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if _dtype_code(q_nope, "q_nope") != DTYPE_BF16 or _dtype_code(ckv_cache, "ckv_cache") != DTYPE_BF16:
+        raise ValueError("mla_decode_noalloc takes bf16 queries and caches")
+    idx_ptr = _ptr(kv_indices) if kv_indices is not None and kv_indices.numel() > 0 else None
+    st = lib.mla_decode_noalloc(indptr.ctypes.data_as(_I32P), idx_ptr, lens.ctypes.data_as(_I32P),
+                                batch, int(q_nope.shape[1]), int(page_size), float(sm_scale),
+                                _ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(kpe_cache),
+                                float(kv_scale), int(ckv_cache.shape[0]), _ptr(out),
+                                _dtype_code(out, "out"), _ptr(lse), int(bool(check_status)),
+                                _stream_handle(stream))
+    _check(st, None, "mla_decode_noalloc")
 
 
 def mla_decode_run_host(plan, q_nope_host, q_pe_host, ckv_cache, kpe_cache, out_host, lse_host,
