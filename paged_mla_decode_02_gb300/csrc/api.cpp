@@ -39,8 +39,8 @@ struct mla_plan_s {
   cudaEvent_t upload_done = nullptr; // the pinned blob may be rewritten once this fired
 
   float* d_o_part = nullptr;         // [slots_cap, H, 512]
-  float* d_lse_part = nullptr;       // [slots_cap, 2, H]
-  int32_t* d_counters = nullptr;     // [max_batch, 4]: split-request counts (tcgen05)
+  float* d_lse_part = nullptr;       // [slots_cap, 4, H]
+  int32_t* d_counters = nullptr;     // [max_batch, 8]: split-request counts (tcgen05)
   int32_t* d_err = nullptr;
 
   // Staging of mla_decode_run_host (allocated on first use).
@@ -163,7 +163,7 @@ bool mla::encode_tc_maps(TcMaps* maps, const void* q_nope, const void* ckv_cache
                    page_size, 64) &&
          encode_2d(&maps->kpe_k, kpe_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDKpe,
                    page_size, 64) &&
-         encode_panels_3d(&maps->ckv_v, ckv_cache, kvrows, page_size >= 32 ? 32 : 16, 4);
+         encode_panels_3d(&maps->ckv_v, ckv_cache, kvrows, page_size >= 32 ? 32 : 16, 8 / kTcCluster);
 }
 
 extern "C" {
@@ -226,8 +226,8 @@ mla_status_t mla_plan_create(int max_batch, int num_heads, int kernel, mla_plan_
   p->off_merge = align16(p->off_wptr + sizeof(int32_t) * (p->n_workers + 1));
   p->blob_bytes = align16(p->off_merge + sizeof(MergeEntry) * p->merge_cap);
   const size_t o_bytes = sizeof(float) * static_cast<size_t>(p->slots_cap) * num_heads * kDCkv;
-  const size_t l_bytes = sizeof(float) * static_cast<size_t>(p->slots_cap) * 2 * num_heads;
-  const size_t c_bytes = sizeof(int32_t) * static_cast<size_t>(max_batch) * 4;
+  const size_t l_bytes = sizeof(float) * static_cast<size_t>(p->slots_cap) * kLsePartCopies * num_heads;
+  const size_t c_bytes = sizeof(int32_t) * static_cast<size_t>(max_batch) * 8;
   if ((e = cudaMalloc(&p->d_blob, p->blob_bytes)) != cudaSuccess ||
       (e = cudaMallocHost(&p->h_blob, p->blob_bytes)) != cudaSuccess ||
       (e = cudaEventCreateWithFlags(&p->upload_done, cudaEventDisableTiming)) != cudaSuccess ||
@@ -304,7 +304,7 @@ mla_status_t mla_decode_plan(mla_plan_t plan, const int32_t* kv_indptr_host,
     return cuda_fail(plan, e, "plan upload");
   // The tcgen05 kernel leaves its arrival counters at zero; a launch that
   // stopped on a device error may not have, so every plan starts from zero.
-  if ((e = cudaMemsetAsync(plan->d_counters, 0, sizeof(int32_t) * 4 * plan->max_batch, s)) !=
+  if ((e = cudaMemsetAsync(plan->d_counters, 0, sizeof(int32_t) * 8 * plan->max_batch, s)) !=
       cudaSuccess)
     return cuda_fail(plan, e, "counter reset");
   if ((e = cudaEventRecord(plan->upload_done, s)) != cudaSuccess)
@@ -383,7 +383,7 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
     if (!encode_2d(&maps.q_nope, q_nope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qrows, kDCkv, H, 64) ||
         !encode_2d(&maps.ckv_k, ckv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDCkv, P, 64) ||
         !encode_2d(&maps.kpe_k, kpe_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDKpe, P, 64) ||
-        !encode_panels_3d(&maps.ckv_v, ckv_cache, kvrows, P >= 32 ? 32 : 16, 4))
+        !encode_panels_3d(&maps.ckv_v, ckv_cache, kvrows, P >= 32 ? 32 : 16, 8 / kTcCluster))
       return fail(plan, MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     e = launch_decode_tc(a, maps, out_f32, s);
   }

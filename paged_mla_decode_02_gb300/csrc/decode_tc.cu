@@ -11,18 +11,18 @@
 // O = P[H x T] . ckv[T x 512].
 //
 // Work decomposition.  A work unit (a token range of one request, from the
-// host planner) is processed by a cluster of two CTAs.  CTA `half` owns the
-// output dims [256 half, 256 half + 256): 128 heads x 512 fp32 accumulators
-// would fill all 512 TMEM columns of one SM.  The unit's 128-token tiles
-// alternate between the two CTAs: the owner of tile g (g odd or even) loads
-// its K, computes S = Q K^T and the softmax, and sends P (bf16) with the
-// tile's reference max and row sums to the other CTA through distributed
-// shared memory.  Both CTAs then accumulate P . V over their own 256 dims.
-// So every score tile is computed once, and each SM issues half the score
-// MMAs and half the softmax of a design where both CTAs compute S.
-// The grid is persistent: one cluster per worker, walking its units.
+// host planner) is processed by a cluster of C CTAs (C = kTcCluster = 2; the
+// same source builds C = 4).  CTA `rank` owns the output dims
+// [512/C rank, 512/C (rank + 1)): 128 heads x 512 fp32 accumulators would
+// fill all 512 TMEM columns of one SM.  The unit's 128-token tiles rotate
+// over the cluster's CTAs: the owner of tile g (g mod C == rank) loads its K,
+// computes S = Q K^T and the softmax, and sends P (bf16) with the tile's
+// reference max and row sums to the other CTAs through distributed shared
+// memory (one bulk copy per CTA).  Every CTA then accumulates P . V over its
+// own dims.  So every score tile is computed once.  The grid is persistent:
+// one cluster per worker, walking its units.
 //
-// Per CTA (384 threads, 12 warps):
+// Per CTA (384 threads, 12 warps), for C = 2:
 //   warp 0      K producer (own tiles): TMA loads of Q dims 0..319 (per
 //               unit) and of the 9 K panels (64 dims x 128 tokens) of the
 //               tile, page by page through kv_indices, into a 3-slot ring;
@@ -32,21 +32,23 @@
 //               32 tokens (16 KB) at a time into a 3-slot ring; rows past the
 //               end of a request are zeroed;
 //   warps 3..10 softmax: two warps per 32 head rows (TMEM lane quadrant),
-//               each owning 64 tokens of a tile (one P panel) and 128 of the
-//               256 output dims.  For an own tile: drain S, row max over the
-//               tile, lazy-rescaled exp2 (the reference max moves only when
-//               a tile's max exceeds it by more than 2^8), P to local and
+//               each owning 64 tokens of a tile (one P panel) and half of
+//               this CTA's output dims.  For an own tile: drain S, row max over
+//               the tile, lazy-rescaled exp2 (the reference max moves only
+//               when a tile's max exceeds it by more than 2^8), P to local and
 //               remote shared memory.  For every tile, in order: take its
 //               reference (own, or received), rescale O in TMEM when the
 //               reference moved, update the row sums, release it to PV.
 //               Then the epilogue O / l, lse;
 //   warp 11     lane 0 issues the PV MMAs (M=128, N=256 dims, K=16 tokens).
 // TMEM columns: O [0, 256) | S [256, 384) | Q dims 320..575 as bf16 pairs
-// [384, 512).
+// [384, 512).  (C = 4: O 128 columns, Q dims 64..575 in TMEM, two P buffers,
+// deeper rings; measured slower on the DeepSeek shape -- each owner then
+// pushes three copies of P -- so C = 2 is the launched configuration.)
 //
-// Reference max of tile g (both CTAs use the same value): the owner takes
-// the lazy update of max(M[g-2], M[g-3]), the two latest references it has
-// already applied, so neither CTA's softmax waits on the other's.  O and the
+// Reference max of tile g (every CTA uses the value the owner sends): the
+// owner takes the lazy update of the two latest references it has already
+// applied, so no CTA's softmax waits on another's.  O and the
 // row sums are kept relative to the reference of the last applied tile.
 //
 // Every wait is bounded (2 s); on expiry the kernel records
@@ -69,58 +71,79 @@ constexpr int kThreads = 384;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kPvWarp = 11;
 constexpr int kPanel = 128 * 128;           // 128 rows x 128 B (one 64-dim panel)
-constexpr int kKSlots = 3;
-constexpr int kVSlots = 3;
 constexpr int kVChunkTok = 32;              // tokens per V chunk: two PV MMAs
 constexpr int kVPanel = kVChunkTok * 128;   // 4 KB: 32 rows x 64 dims
-constexpr int kVSlot = 4 * kVPanel;         // 16 KB: 32 rows x 256 dims
-constexpr int kQSmemPanels = 5;             // Q dims 0..319 in shared memory
 // A tile's row info, per softmax warp: 32 heads x {ref max, lx, lr, -} (16 B);
 // laid out [token half][head] so each warp's block is contiguous.
 constexpr int kInfoRow = 16;
 constexpr int kInfoBytes = 2 * 128 * kInfoRow;
 constexpr int kRecvBytes = 2 * kPanel + kInfoBytes;   // P (both token halves) + info
-
-// shared memory map (offsets from the 1024-byte aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffP = kOffQ + kQSmemPanels * kPanel;   // P [128 x 128] bf16 (2 panels)
-constexpr int kOffK = kOffP + 2 * kPanel;
-constexpr int kOffV = kOffK + kKSlots * kPanel;
-constexpr int kOffInfo = kOffV + kVSlots * kVSlot;     // received row info (the peer's tiles)
-constexpr int kOffInfoOut = kOffInfo + kInfoBytes;     // row info of own tiles, to send
-constexpr int kOffXchg = kOffInfoOut + kInfoBytes;     // 128 x (lx, lr) x 2 halves
-constexpr int kOffMaxX = kOffXchg + 128 * 16;          // [own tile parity][half][128] row maxima
-constexpr int kOffBar = kOffMaxX + 2 * 2 * 128 * 4;
 constexpr int kBarBytes = 512;
-constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;   // + alignment slack
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kOffBar % 8 == 0, "barrier alignment");
+constexpr uint32_t kTmemCols = 512;
+
+// Layout for clusters of C CTAs (C = 2 or 4).  CTA `rank` owns output dims
+// [512 / C * rank, 512 / C * (rank + 1)); its O accumulator takes 512 / C TMEM
+// columns, S 128, and Q's upper dims the rest (as bf16 pairs); Q's lower
+// dims stay in shared memory.  With four CTAs the freed TMEM takes all of Q
+// but one panel, and the freed shared memory buys a second P buffer and
+// deeper copy rings.
+template <int C>
+struct Cfg {
+  static constexpr int kDims = kDCkv / C;                 // output dims per CTA
+  static constexpr uint32_t kColO = 0, kColS = kDims, kColQ = kDims + 128;
+  static constexpr int kQTmemPanels = (kTmemCols - kColQ) / 32;   // 64-dim Q panels in TMEM
+  static constexpr int kQSmemPanels = 9 - kQTmemPanels;           // Q dims below, in smem
+  static constexpr int kPBufs = C == 2 ? 1 : 2;           // P buffers (by tile parity when 2)
+  static constexpr int kKSlots = C == 2 ? 3 : 5;
+  static constexpr int kVPanels = kDims / 64;             // V panels per chunk (this CTA's dims)
+  static constexpr int kVSlot = kVPanels * kVPanel;       // 16 KB (C = 2) or 8 KB (C = 4)
+  static constexpr int kVSlots = C == 2 ? 3 : 6;
+  // shared memory map (offsets from the 1024-byte aligned base)
+  static constexpr int kOffQ = 0;
+  // P buffer b: P [128 x 128] bf16 (2 panels) followed by the tile's row
+  // info, so one copy carries both to another CTA
+  static constexpr int kPStride = kRecvBytes;
+  static constexpr int kOffP = kOffQ + kQSmemPanels * kPanel;
+  static constexpr int kOffK = kOffP + kPBufs * kPStride;
+  static constexpr int kOffV = kOffK + kKSlots * kPanel;
+  static constexpr int kOffXchg = kOffV + kVSlots * kVSlot;             // 128 x (lx, lr) x 2 halves
+  static constexpr int kOffMaxX = kOffXchg + 128 * 16;                  // [own tile parity][half][128] maxima
+  static constexpr int kOffBar = kOffMaxX + 2 * 2 * 128 * 4;
+  static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;         // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kOffBar % 8 == 0, "barrier alignment");
+  static_assert(kPStride % 1024 == 0 && kOffP % 1024 == 0, "P buffers on swizzle-atom boundaries");
+  static_assert(kQTmemPanels * 32 + kColQ == kTmemCols, "TMEM budget");
+};
+
+constexpr int kMaxKSlots = 5, kMaxVSlots = 6;   // ring barriers sized for the deepest rings
+static_assert(Cfg<2>::kKSlots <= kMaxKSlots && Cfg<4>::kKSlots <= kMaxKSlots, "K ring");
+static_assert(Cfg<2>::kVSlots <= kMaxVSlots && Cfg<4>::kVSlots <= kMaxVSlots, "V ring");
 
 enum Bar {
   kQFull = 0, kQTmemFull, kQEmpty,
-  kKFull0, kKEmpty0 = kKFull0 + kKSlots,
-  kVFull0 = kKEmpty0 + kKSlots, kVEmpty0 = kVFull0 + kVSlots, kVTail0 = kVEmpty0 + kVSlots,
-  kSFull = kVTail0 + kVSlots, kSFree,
-  kPFree0,          // 2, by tile parity: both CTAs' PV of the tile done (P buffer reusable)
-  kPRecv = kPFree0 + 2,   // the peer's P and info for a tile it owns have landed
-  kPReady0,         // 2, by tile parity: tile released to PV (O rescaled, P in place)
+  kKFull0, kKEmpty0 = kKFull0 + kMaxKSlots,
+  kVFull0 = kKEmpty0 + kMaxKSlots, kVEmpty0 = kVFull0 + kMaxVSlots, kVTail0 = kVEmpty0 + kMaxVSlots,
+  kSFull = kVTail0 + kMaxVSlots, kSFree,
+  kPFree0,          // 2, by tile parity: every CTA's PV of the tile done (its P buffer reusable)
+  kPRecv0 = kPFree0 + 2,   // 2, by P buffer: a peer's P and info for a tile it owns have landed
+  kPReady0 = kPRecv0 + 2,  // 2, by tile parity: tile released to PV (O rescaled, P in place)
   kPvDone0 = kPReady0 + 2,   // 2, by tile parity: this CTA's PV of the tile completed
   kOFree = kPvDone0 + 2, kFinal, kFinalPv,
   kXchg0, kMaxX0 = kXchg0 + 4,   // 4, per lane quadrant: the two warps' row maxima posted
   kMergeB = kMaxX0 + 4,   // split unit: merge-or-publish decided (flag in shared memory)
+  kPWritten,              // own tile: all 8 softmax warps wrote their P rows and row info
   kNumBars
 };
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
-
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 384;
-constexpr uint32_t kTmemCols = 512;
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P values stay below 2^8
 constexpr int kMergeRegs = 8;               // split request slots whose weights stay in registers
 
-__device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + kOffBar + 8 * i; }
+template <int C>
+__device__ __forceinline__ uint32_t bar_addr(uint32_t base, int i) { return base + Cfg<C>::kOffBar + 8 * i; }
 
 template <int N>
 __device__ __forceinline__ float tree_max(float (&v)[N]) {
@@ -147,29 +170,32 @@ __device__ __forceinline__ float tree_sum(float (&v)[N]) {
   return v[0];
 }
 
-// Q dims 320..575 of head row r into TMEM columns [kColQ, kColQ + 128) of
-// lane r: q_nope dims 320..511 (3 panels of 64) then q_pe (64), each 32
-// columns of packed bf16 pairs.  The warp of column half hc writes panels
-// 2hc and 2hc + 1.
+// Q dims above the shared-memory panels (64 * kQSmemPanels .. 575) of head row
+// r into TMEM columns [kColQ, 512) of lane r: the remaining q_nope panels
+// then q_pe, each 64 dims = 32 columns of packed bf16 pairs.  The warp of
+// column half hc writes the first or the second half of those panels.
+template <int C>
 __device__ __forceinline__ void load_q_tmem(const DecodeArgs& a, int req, int r, int hc,
                                             uint32_t taddr) {
+  using L = Cfg<C>;
+  constexpr int kPer = L::kQTmemPanels / 2;
   const int H = a.num_heads;
   const bool ok = r < H;
   const size_t row = static_cast<size_t>(req) * H + (ok ? r : 0);
   const uint4* qn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_nope) +
-                                                   row * kDCkv + 64 * kQSmemPanels);
+                                                   row * kDCkv + 64 * L::kQSmemPanels);
   const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_pe) +
                                                    row * kDKpe);
 #pragma unroll 1
-  for (int p = 2 * hc; p < 2 * hc + 2; ++p) {
-    const uint4* src = p < 3 ? qn + p * 8 : qp;
+  for (int p = kPer * hc; p < kPer * hc + kPer; ++p) {
+    const uint4* src = p < L::kQTmemPanels - 1 ? qn + p * 8 : qp;
     uint32_t v[32];
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       const uint4 x = ok ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
       v[4 * c] = x.x; v[4 * c + 1] = x.y; v[4 * c + 2] = x.z; v[4 * c + 3] = x.w;
     }
-    tmem_st32(taddr + kColQ + 32 * p, v);
+    tmem_st32(taddr + L::kColQ + 32 * p, v);
   }
   tmem_st_wait();
 }
@@ -212,20 +238,20 @@ __device__ __forceinline__ void store_out_row32(void* out, size_t orow, int d0, 
   }
 }
 
-template <bool kOutF32>
+template <bool kOutF32, int C>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ TcMaps maps) {
+  using L = Cfg<C>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t base = smem_u32(sm);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffBar + kNumBars * 8);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffBar + kNumBars * 8 + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + L::kOffBar + kNumBars * 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + L::kOffBar + kNumBars * 8 + 4);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int worker = blockIdx.x >> 1;
-  const int half = static_cast<int>(cluster_ctarank());   // == blockIdx.x & 1
-  const uint32_t peer = static_cast<uint32_t>(half ^ 1);
+  const int worker = blockIdx.x / C;
+  const int rank = static_cast<int>(cluster_ctarank());   // == blockIdx.x % C
   const PlanDev prm = *a.params;
   const int H = a.num_heads;
   const int P = prm.page_size;
@@ -237,10 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
-      if (i == kQTmemFull || i == kSFree || i == kPReady0 || i == kPReady0 + 1 || i == kOFree)
+      if (i == kQTmemFull || i == kSFree || i == kPReady0 || i == kPReady0 + 1 || i == kOFree ||
+          i == kPWritten)
         cnt = kSoftmaxWarps;
-      if (i == kPFree0 || i == kPFree0 + 1 || (i >= kXchg0 && i < kMergeB)) cnt = 2;   // kXchg*, kMaxX*
-      mbar_init(bar_addr(base, i), cnt);
+      if (i == kPFree0 || i == kPFree0 + 1) cnt = C;              // every CTA's PV commit
+      if (i >= kXchg0 && i < kMergeB) cnt = 2;                    // kXchg*, kMaxX*
+      mbar_init(bar_addr<C>(base, i), cnt);
     }
     fence_barrier_init();
   }
@@ -248,9 +276,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Q rows past num_heads are never written by TMA: make them zero once.
     const int t = threadIdx.x - 96;
     const int per_panel = (128 - H) * 8;
-    for (int i = t; i < kQSmemPanels * per_panel; i += 32 * kSoftmaxWarps) {
+    for (int i = t; i < L::kQSmemPanels * per_panel; i += 32 * kSoftmaxWarps) {
       const int panel = i / per_panel, rem = i % per_panel;
-      *reinterpret_cast<uint4*>(sm + kOffQ + panel * kPanel + (H + rem / 8) * 128 + (rem % 8) * 16) =
+      *reinterpret_cast<uint4*>(sm + L::kOffQ + panel * kPanel + (H + rem / 8) * 128 + (rem % 8) * 16) =
           make_uint4(0, 0, 0, 0);
     }
     fence_proxy_async_smem();
@@ -273,15 +301,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
       const WorkUnit u = a.units[ui];
-      if (uidx > 0 && !(ok = mbar_wait_warp(bar_addr(base, kQEmpty), (uidx - 1) & 1, abort_flag)))
+      if (uidx > 0 && !(ok = mbar_wait_warp(bar_addr<C>(base, kQEmpty), (uidx - 1) & 1, abort_flag)))
         break;
-      if (lane == 0) mbar_arrive_expect_tx(bar_addr(base, kQFull), kQSmemPanels * H * 128);
+      if (lane == 0) mbar_arrive_expect_tx(bar_addr<C>(base, kQFull), L::kQSmemPanels * H * 128);
       __syncwarp();
-      if (lane < kQSmemPanels)
-        tma_load_2d(base + kOffQ + lane * kPanel, &maps.q_nope, 64 * lane, u.req * H,
-                    bar_addr(base, kQFull));
+      if (lane < L::kQSmemPanels)
+        tma_load_2d(base + L::kOffQ + lane * kPanel, &maps.q_nope, 64 * lane, u.req * H,
+                    bar_addr<C>(base, kQFull));
       for (int tok0 = u.tok_begin; tok0 < u.tok_end && ok; tok0 += kT, ++g) {
-        if ((g & 1) != half) continue;
+        if (g % C != rank) continue;
         // lane b < nbox owns page b of this tile (a box of P rows)
         const int nbox = (min(tok0 + kT, u.tok_end) - tok0 + P - 1) / P;
         int row = 0;
@@ -294,15 +322,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           row = page * P;
         }
         for (int j = 0; j < 9; ++j, ++kc) {
-          const int slot = kc % kKSlots;
-          if (!(ok = mbar_wait_warp(bar_addr(base, kKEmpty0 + slot), ((kc / kKSlots) & 1) ^ 1,
+          const int slot = kc % L::kKSlots;
+          if (!(ok = mbar_wait_warp(bar_addr<C>(base, kKEmpty0 + slot), ((kc / L::kKSlots) & 1) ^ 1,
                                     abort_flag)))
             break;
-          const uint32_t full = bar_addr(base, kKFull0 + slot);
+          const uint32_t full = bar_addr<C>(base, kKFull0 + slot);
           if (lane == 0) mbar_arrive_expect_tx(full, nbox * P * 128);
           __syncwarp();
           if (lane < nbox) {
-            const uint32_t dst = base + kOffK + slot * kPanel + lane * P * 128;
+            const uint32_t dst = base + L::kOffK + slot * kPanel + lane * P * 128;
             if (j < 8)
               tma_load_2d(dst, &maps.ckv_k, 64 * j, row, full);
             else
@@ -313,8 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
     if (lane == 0)   // drain: the copies this warp issued land before the CTA exits
-      for (int k = 1; k <= kKSlots && k <= kc; ++k)
-        mbar_wait_drain(bar_addr(base, kKFull0 + (kc - k) % kKSlots), ((kc - k) / kKSlots) & 1);
+      for (int k = 1; k <= L::kKSlots && k <= kc; ++k)
+        mbar_wait_drain(bar_addr<C>(base, kKFull0 + (kc - k) % L::kKSlots), ((kc - k) / L::kKSlots) & 1);
     __syncwarp();
   } else if (warp == 2) {
     // ================= V producer (this CTA's 256 dims of ckv, every tile) =================
@@ -351,41 +379,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = tok0; t < min(tok0 + kT, u.tok_end) && ok; t += kVChunkTok, ++vc) {
         const int slot = vslot;
         const uint32_t ph = vphase;
-        if (++vslot == kVSlots) {
+        if (++vslot == L::kVSlots) {
           vslot = 0;
           vphase ^= 1;
         }
-        if (!(ok = mbar_wait_warp(bar_addr(base, kVEmpty0 + slot), ph ^ 1, abort_flag))) break;
-        // One 3-D copy per page run of the chunk brings this CTA's 4 panels:
-        // pages of >= 32 rows give one 32-row copy (panels 4 KB apart), 16-row
-        // pages two 16-row copies (panels 2 KB apart, second copy 8 KB in).
+        if (!(ok = mbar_wait_warp(bar_addr<C>(base, kVEmpty0 + slot), ph ^ 1, abort_flag))) break;
+        // One 3-D copy per page run of the chunk brings this CTA's kVPanels
+        // panels: pages of >= 32 rows give one 32-row copy (panels 4 KB apart),
+        // 16-row pages two 16-row copies (panels 2 KB apart, the second copy
+        // half a slot in).
         const int rows = min(kVChunkTok, u.tok_end - t);
         const int vbox = P >= kVChunkTok ? kVChunkTok : 16;
         const int ncopy = (rows + vbox - 1) / vbox;
-        const uint32_t full = bar_addr(base, kVFull0 + slot);
-        const uint32_t dst = base + kOffV + slot * kVSlot;
-        if (lane == 0) mbar_arrive_expect_tx(full, ncopy * vbox * 4 * 128);
+        const uint32_t full = bar_addr<C>(base, kVFull0 + slot);
+        const uint32_t dst = base + L::kOffV + slot * L::kVSlot;
+        if (lane == 0) mbar_arrive_expect_tx(full, ncopy * vbox * L::kVPanels * 128);
         __syncwarp();
         // lane c < ncopy issues copy c (lanes past it mirror the last one for the shuffle)
         const int tb = t + vbox * min(lane, ncopy - 1);
         const int page = __shfl_sync(0xffffffffu, pg_cur, (tb - tok0) / P);
         if (lane < ncopy)
-          tma_load_3d(dst + lane * vbox * 4 * 128, &maps.ckv_v, 0, page * P + (tb % P), 4 * half, full);
+          tma_load_3d(dst + lane * vbox * L::kVPanels * 128, &maps.ckv_v, 0, page * P + (tb % P),
+                      L::kVPanels * rank, full);
         if (rows < kVChunkTok) {
           // Last chunk of a request: rows past kv_len may hold anything (even
           // NaN), and P = 0 there does not cancel NaN.  Wait for the copy,
           // zero those rows, then release the chunk through kVTail.
           if (!(ok = mbar_wait_warp(full, ph, abort_flag))) break;
-          for (int q = lane; q < (kVChunkTok - rows) * 32; q += 32) {
-            const int rr = rows + q / 32, pnl = (q % 32) >> 3, c16 = q & 7;
+          constexpr int kRowChunks = L::kVPanels * 8;   // 16-byte pieces of one chunk row
+          for (int q = lane; q < (kVChunkTok - rows) * kRowChunks; q += 32) {
+            const int rr = rows + q / kRowChunks, pnl = (q % kRowChunks) >> 3, c16 = q & 7;
             const int off = vbox == kVChunkTok
                                 ? pnl * kVPanel + rr * 128
-                                : (rr >> 4) * (kVSlot / 2) + pnl * (kVPanel / 2) + (rr & 15) * 128;
-            *reinterpret_cast<uint4*>(sm + kOffV + slot * kVSlot + off + c16 * 16) = make_uint4(0, 0, 0, 0);
+                                : (rr >> 4) * (L::kVSlot / 2) + pnl * (kVPanel / 2) + (rr & 15) * 128;
+            *reinterpret_cast<uint4*>(sm + L::kOffV + slot * L::kVSlot + off + c16 * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_addr(base, kVTail0 + slot));
+          if (lane == 0) mbar_arrive(bar_addr<C>(base, kVTail0 + slot));
         }
       }
       if (!ok) break;
@@ -395,80 +426,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
     if (lane == 0)
-      for (int k = 1; k <= kVSlots && k <= vc; ++k)
-        mbar_wait_drain(bar_addr(base, kVFull0 + (vc - k) % kVSlots), ((vc - k) / kVSlots) & 1);
+      for (int k = 1; k <= L::kVSlots && k <= vc; ++k)
+        mbar_wait_drain(bar_addr<C>(base, kVFull0 + (vc - k) % L::kVSlots), ((vc - k) / L::kVSlots) & 1);
     __syncwarp();
   } else if (warp == 1) {
     // ================= QK issuer (own tiles; whole warp converged, lane 0 issues) =================
     constexpr uint32_t id_qk = idesc_bf16_f32(128, kT, false, false);
     const uint32_t issue = lane == 0;
-    const uint64_t q_desc0 = smem_desc(base + kOffQ, 16, 1024, kSw128);
-    const uint64_t k_desc0 = smem_desc(base + kOffK, 16, 1024, kSw128);
+    const uint64_t q_desc0 = smem_desc(base + L::kOffQ, 16, 1024, kSw128);
+    const uint64_t k_desc0 = smem_desc(base + L::kOffK, 16, 1024, kSw128);
     int g = 0, gl = 0, uidx = 0, kslot = 0;
     uint32_t kphase = 0;
     bool ok = true;
     for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
       const WorkUnit u = a.units[ui];
       const int n = tiles_of(u);
-      if (!(ok = mbar_wait_warp(bar_addr(base, kQFull), uidx & 1, abort_flag) &&
-                 mbar_wait_warp(bar_addr(base, kQTmemFull), uidx & 1, abort_flag)))
+      if (!(ok = mbar_wait_warp(bar_addr<C>(base, kQFull), uidx & 1, abort_flag) &&
+                 mbar_wait_warp(bar_addr<C>(base, kQTmemFull), uidx & 1, abort_flag)))
         break;
       tc_fence_after();
       for (int i = 0; i < n && ok; ++i, ++g) {
-        if ((g & 1) != half) continue;
+        if (g % C != rank) continue;
         // S is single-buffered: the softmax drains it to registers right away.
-        if (!(ok = mbar_wait_warp(bar_addr(base, kSFree), (gl & 1) ^ 1, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(bar_addr<C>(base, kSFree), (gl & 1) ^ 1, abort_flag))) break;
         tc_fence_after();
         for (int j = 0; j < 9; ++j) {
           const int slot = kslot;
           const uint32_t ph = kphase;
-          if (++kslot == kKSlots) {
+          if (++kslot == L::kKSlots) {
             kslot = 0;
             kphase ^= 1;
           }
-          if (!(ok = mbar_wait_warp(bar_addr(base, kKFull0 + slot), ph, abort_flag))) break;
+          if (!(ok = mbar_wait_warp(bar_addr<C>(base, kKFull0 + slot), ph, abort_flag))) break;
           const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((slot * kPanel) >> 4);
-          if (j < kQSmemPanels) {
+          if (j < L::kQSmemPanels) {
             const uint64_t adesc = q_desc0 + static_cast<uint64_t>((j * kPanel) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ss(tmem + kColS, adesc + static_cast<uint64_t>((kk * 32) >> 4),
+              mma_ss(tmem + L::kColS, adesc + static_cast<uint64_t>((kk * 32) >> 4),
                      bdesc + static_cast<uint64_t>((kk * 32) >> 4), id_qk, (j | kk) != 0, issue);
           } else {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + kColS, tmem + kColQ + (j - kQSmemPanels) * 32 + kk * 8,
+              mma_ts(tmem + L::kColS, tmem + L::kColQ + (j - L::kQSmemPanels) * 32 + kk * 8,
                      bdesc + static_cast<uint64_t>((kk * 32) >> 4), id_qk, 1u, issue);
           }
-          mma_commit(bar_addr(base, kKEmpty0 + slot), issue);
+          mma_commit(bar_addr<C>(base, kKEmpty0 + slot), issue);
         }
         if (!ok) break;
-        mma_commit(bar_addr(base, kSFull), issue);
+        mma_commit(bar_addr<C>(base, kSFull), issue);
         ++gl;
       }
       if (!ok) break;
-      mma_commit(bar_addr(base, kQEmpty), issue);   // Q of this unit no longer read
+      mma_commit(bar_addr<C>(base, kQEmpty), issue);   // Q of this unit no longer read
     }
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
     // Drain: all MMAs issued by this warp complete before TMEM is freed.
-    mma_commit(bar_addr(base, kFinal), issue);
-    if (lane == 0) mbar_wait_drain(bar_addr(base, kFinal), 0);
+    mma_commit(bar_addr<C>(base, kFinal), issue);
+    if (lane == 0) mbar_wait_drain(bar_addr<C>(base, kFinal), 0);
     __syncwarp();
   } else if (warp == kPvWarp) {
     // ================= PV issuer (every tile; lane 0 issues) =================
-    constexpr uint32_t id_pv = idesc_bf16_f32(128, 256, false, true);
+    constexpr uint32_t id_pv = idesc_bf16_f32(128, L::kDims, false, true);
     const uint32_t issue = lane == 0;
-    const uint64_t p_desc0 = smem_desc(base + kOffP, 16, 1024, kSw128);
+    const uint64_t p_desc0 = smem_desc(base + L::kOffP, 16, 1024, kSw128);
     // V chunk layout (see the V producer): panels 4 KB apart and the two
     // 16-token slices 2 KB apart, or for 16-row pages 2 KB and 8 KB
     const bool v32 = P >= kVChunkTok;
-    const uint64_t v_desc0 = smem_desc(base + kOffV, v32 ? kVPanel : kVPanel / 2, 1024, kSw128);
-    const uint32_t v_kstep = v32 ? 16 * 128 : kVSlot / 2;
+    const uint64_t v_desc0 = smem_desc(base + L::kOffV, v32 ? kVPanel : kVPanel / 2, 1024, kSw128);
+    const uint32_t v_kstep = v32 ? 16 * 128 : L::kVSlot / 2;
     int g = 0, uidx = 0, vslot = 0;
     uint32_t vphase = 0;
     uint32_t tail_par = 0;   // per V slot: parity of its next tail-chunk release
     bool ok = true;
-    const volatile int* merge_flag = reinterpret_cast<const volatile int*>(sm + kOffBar + kNumBars * 8 + 8);
+    const volatile int* merge_flag = reinterpret_cast<const volatile int*>(sm + L::kOffBar + kNumBars * 8 + 8);
     // After unit v's epilogue released O (kOFree): if v is a split unit that
     // does not merge, its stored share becomes visible GPU-wide and is counted
     // as published (the fence orders the softmax warps' stores, seen through
@@ -476,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto publish = [&](const WorkUnit& v) {
       if (v.n_slots > 0 && *merge_flag == 0 && lane == 0) {
         __threadfence();
-        atomicAdd(a.counters + 4 * v.req + 2 + half, 1);
+        atomicAdd(a.counters + 8 * v.req + 4 + rank, 1);
       }
     };
     for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
@@ -484,55 +515,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = tiles_of(u);
       // the first PV of a unit overwrites O: the previous epilogue must be done
       if (uidx > 0) {
-        if (!(ok = mbar_wait_warp(bar_addr(base, kOFree), (uidx - 1) & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(bar_addr<C>(base, kOFree), (uidx - 1) & 1, abort_flag))) break;
         publish(a.units[ui - 1]);
       }
       for (int i = 0; i < n && ok; ++i, ++g) {
         const int valid = min(kT, u.tok_end - (u.tok_begin + i * kT));
         const int nch = (valid + kVChunkTok - 1) / kVChunkTok;
-        if (!(ok = mbar_wait_warp(bar_addr(base, kPReady0 + (g & 1)), (g >> 1) & 1, abort_flag)))
+        if (!(ok = mbar_wait_warp(bar_addr<C>(base, kPReady0 + (g & 1)), (g >> 1) & 1, abort_flag)))
           break;
         tc_fence_after();
+        const uint64_t p_desc = p_desc0 + static_cast<uint64_t>(((L::kPBufs == 2 ? (g & 1) : 0) * L::kPStride) >> 4);
         for (int c = 0; c < nch; ++c) {
           const int slot = vslot;
           const uint32_t ph = vphase;
-          if (++vslot == kVSlots) {
+          if (++vslot == L::kVSlots) {
             vslot = 0;
             vphase ^= 1;
           }
           if (c == nch - 1 && (valid % kVChunkTok) != 0) {
-            if (!(ok = mbar_wait_warp(bar_addr(base, kVTail0 + slot), (tail_par >> slot) & 1,
+            if (!(ok = mbar_wait_warp(bar_addr<C>(base, kVTail0 + slot), (tail_par >> slot) & 1,
                                       abort_flag)))
               break;
             tail_par ^= 1u << slot;
-          } else if (!(ok = mbar_wait_warp(bar_addr(base, kVFull0 + slot), ph, abort_flag))) {
+          } else if (!(ok = mbar_wait_warp(bar_addr<C>(base, kVFull0 + slot), ph, abort_flag))) {
             break;
           }
 #pragma unroll
           for (int kk = 0; kk < kVChunkTok / 16; ++kk) {
             const int tok = kVChunkTok * c + 16 * kk;   // first token of this MMA's K slice
-            mma_ss(tmem + kColO,
-                   p_desc0 + static_cast<uint64_t>(((tok >> 6) * kPanel + (tok & 63) * 2) >> 4),
-                   v_desc0 + static_cast<uint64_t>((slot * kVSlot + kk * v_kstep) >> 4), id_pv,
+            mma_ss(tmem + L::kColO,
+                   p_desc + static_cast<uint64_t>(((tok >> 6) * kPanel + (tok & 63) * 2) >> 4),
+                   v_desc0 + static_cast<uint64_t>((slot * L::kVSlot + kk * v_kstep) >> 4), id_pv,
                    (i == 0 && c == 0 && kk == 0) ? 0u : 1u, issue);
           }
-          mma_commit(bar_addr(base, kVEmpty0 + slot), issue);
-          // P panel 0 (tokens 0..63) is no longer read after chunk 1: the
-          // next tile's owner may overwrite it in both CTAs
+          mma_commit(bar_addr<C>(base, kVEmpty0 + slot), issue);
         }
         if (!ok) break;
-        mma_commit(bar_addr(base, kPvDone0 + (g & 1)), issue);
-        // P buffer g & 1 is reusable once both CTAs' PV of this tile is done
-        mma_commit_mc(bar_addr(base, kPFree0 + (g & 1)), static_cast<uint16_t>(0x3), issue);
+        mma_commit(bar_addr<C>(base, kPvDone0 + (g & 1)), issue);
+        // the tile's P buffer is reusable once every CTA's PV of the tile is done
+        mma_commit_mc(bar_addr<C>(base, kPFree0 + (g & 1)), static_cast<uint16_t>((1u << C) - 1), issue);
       }
     }
     if (ok && uidx > 0) {   // the last unit's share
-      if ((ok = mbar_wait_warp(bar_addr(base, kOFree), (uidx - 1) & 1, abort_flag)))
+      if ((ok = mbar_wait_warp(bar_addr<C>(base, kOFree), (uidx - 1) & 1, abort_flag)))
         publish(a.units[u1 - 1]);
     }
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
-    mma_commit(bar_addr(base, kFinalPv), issue);
-    if (lane == 0) mbar_wait_drain(bar_addr(base, kFinalPv), 0);
+    mma_commit(bar_addr<C>(base, kFinalPv), issue);
+    if (lane == 0) mbar_wait_drain(bar_addr<C>(base, kFinalPv), 0);
     __syncwarp();
   } else {
     // ================= softmax / epilogue (warps 3..10) =================
@@ -547,10 +577,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t p_off = hc * kPanel + (r >> 3) * 1024 + (r & 7) * 128;
     const int pswz = r & 7;
     const uint32_t info_off = (hc * 128 + r) * kInfoRow;
-    const uint32_t recv_bar_remote = map_to_rank(bar_addr(base, kPRecv), peer);
-    int g = 0, gl = 0, nrecv = 0, uidx = 0, nsplit = 0;
+    constexpr int kCh = L::kDims / 64;              // 32-dim O chunks per warp
+    int g = 0, gl = 0, uidx = 0, nsplit = 0;
+    uint32_t recv_par = 0;                          // bit b: parity of P buffer b's next receive
     bool ok = true;
-    volatile int* merge_flag = reinterpret_cast<volatile int*>(sm + kOffBar + kNumBars * 8 + 8);
+    volatile int* merge_flag = reinterpret_cast<volatile int*>(sm + L::kOffBar + kNumBars * 8 + 8);
     // Requests without tokens: out = 0, lse = -inf (merge entries with no
     // slots, dealt round-robin over the workers).
     if (worker < prm.n_workers && r < H) {
@@ -558,19 +589,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const MergeEntry me = a.merge[e];
         if (me.n_slots != 0) continue;
         const size_t orow = static_cast<size_t>(me.req) * H + r;
-        const int d0 = 256 * half + 128 * hc;
+        const int d0 = L::kDims * rank + (L::kDims / 2) * hc;
         uint4* dst = kOutF32 ? reinterpret_cast<uint4*>(static_cast<float*>(a.out) + orow * kDCkv + d0)
                              : reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow * kDCkv + d0);
 #pragma unroll 4
-        for (int j = 0; j < (kOutF32 ? 32 : 16); ++j) dst[j] = make_uint4(0, 0, 0, 0);
-        if (half == 0 && hc == 0) a.lse[orow] = -INFINITY;
+        for (int j = 0; j < (kOutF32 ? L::kDims / 8 : L::kDims / 16); ++j) dst[j] = make_uint4(0, 0, 0, 0);
+        if (rank == 0 && hc == 0) a.lse[orow] = -INFINITY;
       }
     }
     if (u0 < u1) {
-      load_q_tmem(a, a.units[u0].req, r, hc, lane_addr);
+      load_q_tmem<C>(a, a.units[u0].req, r, hc, lane_addr);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(base, kQTmemFull));
+      if (lane == 0) mbar_arrive(bar_addr<C>(base, kQTmemFull));
     }
     for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
       const WorkUnit u = a.units[ui];
@@ -587,17 +618,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the own tile computed but not yet applied
       float own_m = -INFINITY, own_lx = 0.f, own_lr = 0.f;
       for (int i = 0; i <= n && ok; ++i) {
-        const bool own_now = i < n && ((g0 + i) & 1) == half;
+        const bool own_now = i < n && (g0 + i) % C == rank;
         if (u.n_slots > 0 && warp == 3 && lane == 0) {
-          if (i == i_count) end_count = atomicAdd(a.counters + 4 * u.req + half, 1);
+          if (i == i_count) end_count = atomicAdd(a.counters + 8 * u.req + rank, 1);
           if (i == i_count + 1 && end_count == u.n_slots - 1) {
-            // this unit will merge: bring the other units' shares of this CTA
-            // half (contiguous 32 x H x 32 bytes per slot) into L2 meanwhile
+            // this unit will merge: bring the other units' shares of this
+            // CTA's dims (contiguous kDims / 8 x H x 32 bytes per slot) into L2
+            constexpr int kGroups = L::kDims / 8;
             for (int k = u.slot0; k < u.slot0 + u.n_slots; ++k) {
               if (k == u.out_slot) continue;
-              const char* src = reinterpret_cast<const char*>(a.o_part + part_offset(k, 0, 256 * half, H));
-              for (int off = 0; off < 32 * H * 32; off += 32768)
-                bulk_prefetch_l2(src + off, min(32768, 32 * H * 32 - off));
+              const char* src = reinterpret_cast<const char*>(a.o_part + part_offset(k, 0, L::kDims * rank, H));
+              for (int off = 0; off < kGroups * H * 32; off += 32768)
+                bulk_prefetch_l2(src + off, min(32768, kGroups * H * 32 - off));
             }
           }
         }
@@ -605,15 +637,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (own_now) {
           // ---------- own tile g0 + i: scores -> P (registers) ----------
           const int gg = g0 + i;
-          if (!(ok = mbar_wait_warp(bar_addr(base, kSFull), gl & 1, abort_flag))) break;
+          if (!(ok = mbar_wait_warp(bar_addr<C>(base, kSFull), gl & 1, abort_flag))) break;
           tc_fence_after();
           const int valid = min(kT, u.tok_end - (u.tok_begin + i * kT));
           const int vb = 64 * hc;                      // first token of this warp's half
           float s[64];
           {
             uint32_t v0[32], v1[32];
-            tmem_ld32(lane_addr + kColS + vb, v0);
-            tmem_ld32(lane_addr + kColS + vb + 32, v1);
+            tmem_ld32(lane_addr + L::kColS + vb, v0);
+            tmem_ld32(lane_addr + L::kColS + vb + 32, v1);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -623,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_addr(base, kSFree));
+          if (lane == 0) mbar_arrive(bar_addr<C>(base, kSFree));
           ++gl;
 
           // max (min when c < 0) of s over this warp's valid tokens, then
@@ -644,12 +676,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             hmx = c >= 0.f ? tree_max(t) : tree_min(t);
           }
-          float* mx_slot = reinterpret_cast<float*>(sm + kOffMaxX) + ((gl & 1) * 2 + hc) * 128 + r;
+          float* mx_slot = reinterpret_cast<float*>(sm + L::kOffMaxX) + ((gl & 1) * 2 + hc) * 128 + r;
           *mx_slot = hmx;
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar_addr(base, kMaxX0 + quad));
+          if (lane == 0) mbar_arrive(bar_addr<C>(base, kMaxX0 + quad));
           // phase k of this barrier: both warps of the quadrant posted own tile k
-          if (!(ok = mbar_wait_warp(bar_addr(base, kMaxX0 + quad), (gl - 1) & 1, abort_flag))) break;
+          if (!(ok = mbar_wait_warp(bar_addr<C>(base, kMaxX0 + quad), (gl - 1) & 1, abort_flag))) break;
           const float other = mx_slot[(1 - 2 * hc) * 128];
           const float mx = c * (c >= 0.f ? fmaxf(hmx, other) : fminf(hmx, other));
           // lazy reference: the latest two applied references, moved only when
@@ -688,15 +720,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------- apply tile t = g0 + i - 1 (own or received), release it to PV ----------
         const int t = g0 + i - 1;
         float mt, tlx, tlr;
-        if ((t & 1) == half) {
+        if (t % C == rank) {
           mt = own_m;
           tlx = own_lx;
           tlr = own_lr;
         } else {
-          if (warp == 3 && lane == 0) mbar_arrive_expect_tx(bar_addr(base, kPRecv), kRecvBytes);
-          if (!(ok = mbar_wait_warp(bar_addr(base, kPRecv), nrecv & 1, abort_flag))) break;
-          ++nrecv;
-          const float* info = reinterpret_cast<const float*>(sm + kOffInfo + info_off);
+          const int b = L::kPBufs == 2 ? (t & 1) : 0;   // P buffer (and received info) of tile t
+          if (warp == 3 && lane == 0) mbar_arrive_expect_tx(bar_addr<C>(base, kPRecv0 + b), kRecvBytes);
+          if (!(ok = mbar_wait_warp(bar_addr<C>(base, kPRecv0 + b), (recv_par >> b) & 1, abort_flag)))
+            break;
+          recv_par ^= 1u << b;
+          const float* info =
+              reinterpret_cast<const float*>(sm + L::kOffP + b * L::kPStride + 2 * kPanel + info_off);
           mt = info[0];
           tlx = info[1];
           tlr = info[2];
@@ -705,25 +740,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Stay at most two tiles ahead of PV (PV(t-2) complete): with one
         // kPvDone barrier per tile parity, every wait below is then less
         // than two phases away, so its parity is unambiguous.
-        if (t >= 2 && !(ok = mbar_wait_warp(bar_addr(base, kPvDone0 + (t & 1)), ((t - 2) >> 1) & 1,
+        if (t >= 2 && !(ok = mbar_wait_warp(bar_addr<C>(base, kPvDone0 + (t & 1)), ((t - 2) >> 1) & 1,
                                             abort_flag)))
           break;
         const bool first = t == g0;
         const float alpha = first ? 0.f : exp2f(m_last - mt);
         if (!first && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O holds P . V of earlier tiles relative to m_last: move it to mt
-          if (!(ok = mbar_wait_warp(bar_addr(base, kPvDone0 + ((t - 1) & 1)), ((t - 1) >> 1) & 1,
+          if (!(ok = mbar_wait_warp(bar_addr<C>(base, kPvDone0 + ((t - 1) & 1)), ((t - 1) >> 1) & 1,
                                     abort_flag)))
             break;
           tc_fence_after();
 #pragma unroll 1
-          for (int cc = 4 * hc; cc < 4 * hc + 4; ++cc) {
+          for (int cc = kCh * hc; cc < kCh * hc + kCh; ++cc) {
             uint32_t o[32];
-            tmem_ld32(lane_addr + kColO + 32 * cc, o);
+            tmem_ld32(lane_addr + L::kColO + 32 * cc, o);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
-            tmem_st32(lane_addr + kColO + 32 * cc, o);
+            tmem_st32(lane_addr + L::kColO + 32 * cc, o);
           }
           tmem_st_wait();
         }
@@ -733,39 +768,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         m_last = mt;
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_addr(base, kPReady0 + (t & 1)));
+        if (lane == 0) mbar_arrive(bar_addr<C>(base, kPReady0 + (t & 1)));
         }
         if (own_now) {
           // ---------- own tile g0 + i: P to this CTA and the peer ----------
           // (after tile g0 + i - 1 was released above: its PV, in both CTAs,
           // is what frees the P buffers)
           const int gg = g0 + i;
-          // The P buffer (one, in each CTA) is free once both CTAs' PV of the
-          // previous tile is done.
-          if (gg >= 1 && !(ok = mbar_wait_warp(bar_addr(base, kPFree0 + ((gg - 1) & 1)),
-                                               ((gg - 1) >> 1) & 1, abort_flag)))
+          // The tile's P buffer (in every CTA) is free once every CTA's PV of
+          // the tile that last used it -- kPBufs tiles back -- is done.
+          const int gw = gg - L::kPBufs;
+          if (gw >= 0 && !(ok = mbar_wait_warp(bar_addr<C>(base, kPFree0 + (gw & 1)), (gw >> 1) & 1,
+                                               abort_flag)))
             break;
-          const uint32_t prow = kOffP + p_off;
+          const int b = L::kPBufs == 2 ? (gg & 1) : 0;
+          const uint32_t pbuf = L::kOffP + b * L::kPStride;
+          const uint32_t prow = pbuf + p_off;
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch)
             *reinterpret_cast<uint4*>(sm + prow + ((ch ^ pswz) << 4)) =
                 make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-          *reinterpret_cast<float4*>(sm + kOffInfoOut + info_off) =
+          *reinterpret_cast<float4*>(sm + pbuf + 2 * kPanel + info_off) =
               make_float4(own_m, own_lx, own_lr, 0.f);
-          // This warp's rows are contiguous: P rows 32 quad .. 32 quad + 31 of
-          // panel hc (4 KB) and its 32 info rows (512 B).  One bulk copy each
-          // carries them to the peer (the TMA engine moves distributed shared
-          // memory much faster than per-thread remote stores).
+          // Once all eight warps wrote their rows, one thread sends the whole
+          // buffer (P and row info, 36 KB) to every other CTA of the cluster
+          // with one bulk copy each: the copy engine moves distributed shared
+          // memory far faster than remote stores, and one large copy costs
+          // much less than one per warp.
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) {
-            const uint32_t pblk = kOffP + hc * kPanel + quad * 32 * 128;
-            const uint32_t iblk = (hc * 128 + quad * 32) * kInfoRow;
-            bulk_copy_to_peer(map_to_rank(base + pblk, peer), base + pblk, 32 * 128, recv_bar_remote);
-            bulk_copy_to_peer(map_to_rank(base + kOffInfo + iblk, peer), base + kOffInfoOut + iblk,
-                              32 * kInfoRow, recv_bar_remote);
+          if (lane == 0) mbar_arrive(bar_addr<C>(base, kPWritten));
+          if (warp == 3 && lane == 0) {
+            if (!mbar_wait(bar_addr<C>(base, kPWritten), (gl - 1) & 1, abort_flag)) {
+              report_error(a.err, kErrTimeout);
+            } else {
+#pragma unroll
+              for (int pr = 1; pr < C; ++pr) {
+                const uint32_t peer = static_cast<uint32_t>(rank ^ pr);
+                bulk_copy_to_peer(map_to_rank(base + pbuf, peer), base + pbuf, kRecvBytes,
+                                  map_to_rank(bar_addr<C>(base, kPRecv0 + b), peer));
+              }
+            }
           }
-          fence_proxy_async_smem();
+          __syncwarp();
         }
       }
       if (!ok) break;
@@ -774,30 +819,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Q of the next unit: every own QK of this unit has been drained, and
         // the QK warp has finished the unit (so it consumed this unit's
         // kQTmemFull phase before the next one is signalled)
-        if (!(ok = mbar_wait_warp(bar_addr(base, kQEmpty), uidx & 1, abort_flag))) break;
-        load_q_tmem(a, a.units[ui + 1].req, r, hc, lane_addr);
+        if (!(ok = mbar_wait_warp(bar_addr<C>(base, kQEmpty), uidx & 1, abort_flag))) break;
+        load_q_tmem<C>(a, a.units[ui + 1].req, r, hc, lane_addr);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_addr(base, kQTmemFull));
+        if (lane == 0) mbar_arrive(bar_addr<C>(base, kQTmemFull));
       }
       // ---- epilogue ----
-      if (!(ok = mbar_wait_warp(bar_addr(base, kPvDone0 + ((g - 1) & 1)), ((g - 1) >> 1) & 1,
+      if (!(ok = mbar_wait_warp(bar_addr<C>(base, kPvDone0 + ((g - 1) & 1)), ((g - 1) >> 1) & 1,
                                 abort_flag)))
         break;
       tc_fence_after();
       // Combine the two warps' row sums through shared memory; two phases of
       // kXchg0 + quad per unit.
-      float* xch = reinterpret_cast<float*>(sm + kOffXchg + r * 16);
+      float* xch = reinterpret_cast<float*>(sm + L::kOffXchg + r * 16);
       xch[2 * hc] = lx;
       xch[2 * hc + 1] = lr;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(base, kXchg0 + quad));
-      if (!(ok = mbar_wait_warp(bar_addr(base, kXchg0 + quad), 0, abort_flag))) break;
+      if (lane == 0) mbar_arrive(bar_addr<C>(base, kXchg0 + quad));
+      if (!(ok = mbar_wait_warp(bar_addr<C>(base, kXchg0 + quad), 0, abort_flag))) break;
       const float lx_all = xch[0] + xch[2];
       const float lr_all = xch[1] + xch[3];
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_addr(base, kXchg0 + quad));
-      if (!(ok = mbar_wait_warp(bar_addr(base, kXchg0 + quad), 1, abort_flag))) break;
+      if (lane == 0) mbar_arrive(bar_addr<C>(base, kXchg0 + quad));
+      if (!(ok = mbar_wait_warp(bar_addr<C>(base, kXchg0 + quad), 1, abort_flag))) break;
       // A split request is combined by its unit that counted last (warp 3
       // lane 0 holds that count): the others publish their
       // share (partial O and lse of each CTA half), the last one waits for
@@ -809,18 +854,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 3 && lane == 0) {
           const bool me_last = end_count == u.n_slots - 1;
           if (me_last) {
-            int32_t* cnt = a.counters + 4 * u.req;
-            if (!wait_count_acquire(cnt + 2 + half, u.n_slots - 1, abort_flag)) {
+            int32_t* cnt = a.counters + 8 * u.req;
+            if (!wait_count_acquire(cnt + 4 + rank, u.n_slots - 1, abort_flag)) {
               report_error(a.err, kErrTimeout);
             } else {
-              cnt[half] = 0;       // every unit counted and published: clean for the next launch
-              cnt[2 + half] = 0;
+              cnt[rank] = 0;       // every unit counted and published: clean for the next launch
+              cnt[4 + rank] = 0;
             }
           }
           *merge_flag = me_last;
-          mbar_arrive(bar_addr(base, kMergeB));
+          mbar_arrive(bar_addr<C>(base, kMergeB));
         }
-        if (!(ok = mbar_wait_warp(bar_addr(base, kMergeB), nsplit & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_warp(bar_addr<C>(base, kMergeB), nsplit & 1, abort_flag))) break;
         ++nsplit;
         last = *merge_flag != 0;
       }
@@ -839,7 +884,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int rr = r < H ? r : H - 1;
         const int ns = u.n_slots, own = u.out_slot - u.slot0;
         auto slot_lse = [&](int k) {   // k: index within the request's slots
-          return k == own ? lse_own : __ldcg(a.lse_part + lse_part_offset(u.slot0 + k, half, rr, H));
+          return k == own ? lse_own : __ldcg(a.lse_part + lse_part_offset(u.slot0 + k, rank, rr, H));
         };
         // the first kMergeRegs slot lse values are loaded together (static
         // indices keep them in registers); more slots are re-read
@@ -862,10 +907,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int other = u.slot0 + (1 - own);
           const float w0 = __expf(lk[0] - M) * winv, w1 = __expf(lk[1] - M) * winv;
 #pragma unroll 1
-          for (int cc = 4 * hc; cc < 4 * hc + 4; ++cc) {
-            const int d0 = 256 * half + 32 * cc;
+          for (int cc = kCh * hc; cc < kCh * hc + kCh; ++cc) {
+            const int d0 = L::kDims * rank + 32 * cc;
             uint32_t o[32];
-            tmem_ld32(lane_addr + kColO + 32 * cc, o);   // in flight with the loads below
+            tmem_ld32(lane_addr + L::kColO + 32 * cc, o);   // in flight with the loads below
             float4 q[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j)
@@ -885,8 +930,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
 #pragma unroll 1
-          for (int cc = 4 * hc; cc < 4 * hc + 4; ++cc) {
-            const int d0 = 256 * half + 32 * cc;
+          for (int cc = kCh * hc; cc < kCh * hc + kCh; ++cc) {
+            const int d0 = L::kDims * rank + 32 * cc;
             float acc[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) acc[j] = 0.f;
@@ -896,7 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               float v[32];
               if (k == own) {
                 uint32_t o[32];
-                tmem_ld32(lane_addr + kColO + 32 * cc, o);
+                tmem_ld32(lane_addr + L::kColO + 32 * cc, o);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(o[j]) * inv;
@@ -919,18 +964,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_addr(base, kOFree));
-        if (half == 0 && hc == 0 && r < H) a.lse[orow] = M + __logf(W);
+        if (lane == 0) mbar_arrive(bar_addr<C>(base, kOFree));
+        if (rank == 0 && hc == 0 && r < H) a.lse[orow] = M + __logf(W);
       } else {
 #pragma unroll 1
-        for (int cc = 4 * hc; cc < 4 * hc + 4; ++cc) {
+        for (int cc = kCh * hc; cc < kCh * hc + kCh; ++cc) {
           uint32_t o[32];
-          tmem_ld32(lane_addr + kColO + 32 * cc, o);
+          tmem_ld32(lane_addr + L::kColO + 32 * cc, o);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * inv);
           if (r < H) {
-            const int d0 = 256 * half + 32 * cc;
+            const int d0 = L::kDims * rank + 32 * cc;
             if (split) {
               // lanes hold consecutive heads: each store covers 1 KB of contiguous memory
 #pragma unroll
@@ -944,13 +989,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (split && hc == 0 && r < H) a.lse_part[lse_part_offset(u.out_slot, half, r, H)] = lse_own;
+        if (split && hc == 0 && r < H) a.lse_part[lse_part_offset(u.out_slot, rank, r, H)] = lse_own;
         // O may be overwritten now; for a split unit this also hands the
         // stored share to the PV warp, which publishes it
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_addr(base, kOFree));
-        if (!split && half == 0 && hc == 0 && r < H) a.lse[orow] = lse_own;
+        if (lane == 0) mbar_arrive(bar_addr<C>(base, kOFree));
+        if (!split && rank == 0 && hc == 0 && r < H) a.lse[orow] = lse_own;
       }
     }
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
@@ -965,36 +1010,42 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();   // no CTA leaves while its peer may still address its shared memory
 }
 
+// The launched kernel: clusters of kTcCluster CTAs.
 template <bool kOutF32>
 cudaError_t set_attributes() {
+  using L = Cfg<kTcCluster>;
   static bool attr_set = false;   // set once, before any stream capture
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<kOutF32>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<kOutF32, kTcCluster>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   return cudaSuccess;
 }
 
-template <bool kOutF32>
-cudaError_t launch_impl(const DecodeArgs& a, const TcMaps& maps, cudaStream_t s) {
-  auto* k = decode_tc_kernel<kOutF32>;
-  cudaError_t e = set_attributes<kOutF32>();
-  if (e != cudaSuccess) return e;
+cudaLaunchConfig_t cluster_config(int clusters, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * a.n_workers);
+  cfg.gridDim = dim3(kTcCluster * clusters);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cfg.dynamicSmemBytes = Cfg<kTcCluster>::kSmemBytes;
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.x = kTcCluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k, a, maps);
+  return cfg;
+}
+
+template <bool kOutF32>
+cudaError_t launch_impl(const DecodeArgs& a, const TcMaps& maps, cudaStream_t s) {
+  cudaError_t e = set_attributes<kOutF32>();
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = cluster_config(a.n_workers, attr);
+  cfg.stream = s;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<kOutF32, kTcCluster>, a, maps);
 }
 
 }  // namespace
@@ -1004,19 +1055,10 @@ cudaError_t decode_tc_max_workers(int* workers) {
   cudaError_t e = set_attributes<true>();
   if (e == cudaSuccess) e = set_attributes<false>();
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cudaLaunchConfig_t cfg = cluster_config(1, attr);
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, decode_tc_kernel<false>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, decode_tc_kernel<false, kTcCluster>, &cfg);
   if (e != cudaSuccess) return e;
   *workers = clusters;
   return cudaSuccess;

@@ -22,8 +22,8 @@ struct DecodeArgs {
   float* o_part;               // partial outputs, fp32, layout of part_offset()
   float* lse_part;             // [slots][2][H]: one copy per CTA half (lse_part_offset)
   const MergeEntry* merge;     // split and empty requests
-  int32_t* counters;           // [max_batch][4]: per CTA half, units started and
-                               // shares published; zero between launches
+  int32_t* counters;           // [max_batch][8]: per cluster CTA (up to 4), units
+                               // counted and shares published; zero between launches
   int32_t* err;
   int num_pages;
   int num_heads;
@@ -42,10 +42,11 @@ __host__ __device__ inline size_t part_offset(int slot, int h, int d, int H) {
   return ((static_cast<size_t>(slot) * (kDCkv / 8) + d / 8) * H + h) * 8 + (d & 7);
 }
 
-// Log-sum-exp of partial slot `slot`, head h: the tcgen05 kernel's two CTA
-// halves each keep a copy (half 0's is the one the merge kernel reads).
-__host__ __device__ inline size_t lse_part_offset(int slot, int half, int h, int H) {
-  return (static_cast<size_t>(slot) * 2 + half) * H + h;
+// Log-sum-exp of partial slot `slot`, head h: each CTA of a tcgen05 cluster
+// keeps its own copy (up to four; copy 0 is the one the merge kernel reads).
+constexpr int kLsePartCopies = 4;
+__host__ __device__ inline size_t lse_part_offset(int slot, int copy, int h, int H) {
+  return (static_cast<size_t>(slot) * kLsePartCopies + copy) * H + h;
 }
 
 struct MergeArgs {
@@ -62,7 +63,8 @@ struct MergeArgs {
 // Legacy warp-level tensor path (mma.sync m16n8k16): one CTA per (unit, 16-head group).
 cudaError_t launch_decode_mma(const DecodeArgs& a, bool kv_fp8, bool out_f32, cudaStream_t s);
 
-// tcgen05 / TMEM path: persistent CTA pairs, one per worker.
+// tcgen05 / TMEM path: persistent clusters of kTcCluster CTAs, one per worker.
+constexpr int kTcCluster = 2;
 struct TcMaps {
   CUtensorMap q_nope;   // [B*H, 512] bf16, box 64 x H
   CUtensorMap ckv_k;    // [pages*P, 512] bf16, box 64 x P (one page of a K panel)

@@ -187,9 +187,9 @@ extern "C" mla_status_t mla_decode_noalloc(
   const size_t off_opart = align_up(blob_bytes, 256);
   const size_t off_lpart =
       align_up(off_opart + sizeof(float) * static_cast<size_t>(n_slots) * num_heads * kDCkv, 256);
-  const size_t off_cnt =
-      align_up(off_lpart + sizeof(float) * static_cast<size_t>(n_slots) * 2 * num_heads, 256);
-  const size_t off_err = off_cnt + sizeof(int32_t) * 4 * static_cast<size_t>(batch);
+  const size_t off_cnt = align_up(
+      off_lpart + sizeof(float) * static_cast<size_t>(n_slots) * kLsePartCopies * num_heads, 256);
+  const size_t off_err = off_cnt + sizeof(int32_t) * 8 * static_cast<size_t>(batch);
   const size_t need = off_err + sizeof(int32_t);
   if (need > kScratchBytes) return MLA_ERR_CAPACITY;
 
