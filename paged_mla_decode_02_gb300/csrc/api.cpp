@@ -163,7 +163,8 @@ bool mla::encode_tc_maps(TcMaps* maps, const void* q_nope, const void* ckv_cache
                    page_size, 64) &&
          encode_2d(&maps->kpe_k, kpe_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDKpe,
                    page_size, 64) &&
-         encode_panels_3d(&maps->ckv_v, ckv_cache, kvrows, page_size >= 32 ? 32 : 16, 8 / kTcCluster);
+         encode_panels_3d(&maps->ckv_v, ckv_cache, kvrows, page_size >= kTcVChunkTok ? kTcVChunkTok : 16,
+                          8 / kTcCluster);
 }
 
 extern "C" {
@@ -383,7 +384,8 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
     if (!encode_2d(&maps.q_nope, q_nope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qrows, kDCkv, H, 64) ||
         !encode_2d(&maps.ckv_k, ckv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDCkv, P, 64) ||
         !encode_2d(&maps.kpe_k, kpe_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDKpe, P, 64) ||
-        !encode_panels_3d(&maps.ckv_v, ckv_cache, kvrows, P >= 32 ? 32 : 16, 8 / kTcCluster))
+        !encode_panels_3d(&maps.ckv_v, ckv_cache, kvrows, P >= kTcVChunkTok ? kTcVChunkTok : 16,
+                          8 / kTcCluster))
       return fail(plan, MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     e = launch_decode_tc(a, maps, out_f32, s);
   }

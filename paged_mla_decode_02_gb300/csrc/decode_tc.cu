@@ -71,7 +71,8 @@ constexpr int kThreads = 384;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kPvWarp = 11;
 constexpr int kPanel = 128 * 128;           // 128 rows x 128 B (one 64-dim panel)
-constexpr int kVChunkTok = 32;              // tokens per V chunk: two PV MMAs
+constexpr int kVChunkTok = kTcVChunkTok;    // tokens per V chunk (32: two PV MMAs)
+static_assert(kVChunkTok == 16 || kVChunkTok == 32, "V chunk: one or two 16-token MMA slices");
 constexpr int kVPanel = kVChunkTok * 128;   // 4 KB: 32 rows x 64 dims
 // A tile's row info, per softmax warp: 32 heads x {ref max, lx, lr, -} (16 B);
 // laid out [token half][head] so each warp's block is contiguous.
@@ -389,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // 16-row pages two 16-row copies (panels 2 KB apart, the second copy
         // half a slot in).
         const int rows = min(kVChunkTok, u.tok_end - t);
-        const int vbox = P >= kVChunkTok ? kVChunkTok : 16;
+        const int vbox = P >= kVChunkTok ? kVChunkTok : 16;   // rows of the V map's box
         const int ncopy = (rows + vbox - 1) / vbox;
         const uint32_t full = bar_addr<C>(base, kVFull0 + slot);
         const uint32_t dst = base + L::kOffV + slot * L::kVSlot;

@@ -65,6 +65,9 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, bool kv_fp8, bool out_f32, cu
 
 // tcgen05 / TMEM path: persistent clusters of kTcCluster CTAs, one per worker.
 constexpr int kTcCluster = 2;
+// Tokens per V chunk of the tcgen05 kernel; its V tensor map copies boxes of
+// min(page_size, kTcVChunkTok) rows (host encoding and kernel share this).
+constexpr int kTcVChunkTok = 32;
 struct TcMaps {
   CUtensorMap q_nope;   // [B*H, 512] bf16, box 64 x H
   CUtensorMap ckv_k;    // [pages*P, 512] bf16, box 64 x P (one page of a K panel)
