@@ -44,67 +44,6 @@ constexpr size_t kHostBlobBytes =
     align_up(sizeof(int32_t) * (kMaxWorkers + 1), 16) + sizeof(MergeEntry) * kMaxBatch;
 alignas(16) unsigned char g_host_blob[kHostBlobBytes];
 
-// The planner's partition rule (equal tile shares per worker, units cut at
-// request boundaries, consecutive slots for the units of a split request),
-// written into fixed arrays.  Returns the number of units.
-int partition_fixed(const int32_t* indptr, const int32_t* len, int batch, int n_workers,
-                    WorkUnit* units, int32_t* wptr, MergeEntry* merge, int* n_merge,
-                    int* n_slots) {
-  auto tiles_of_req = [&](int b) { return (len[b] + kTileTc - 1) / kTileTc; };
-  long long total = 0;
-  for (int b = 0; b < batch; ++b) total += tiles_of_req(b);
-  const long long base = total / n_workers, extra = total % n_workers;
-  int nu = 0, req = 0, tile = 0;
-  while (req < batch && tiles_of_req(req) == 0) ++req;
-  for (int w = 0; w < n_workers; ++w) {
-    wptr[w] = nu;
-    long long quota = base + (w < extra ? 1 : 0);
-    while (quota > 0 && req < batch) {
-      const int take = static_cast<int>(std::min<long long>(quota, tiles_of_req(req) - tile));
-      WorkUnit& u = units[nu++];
-      u.req = req;
-      u.tok_begin = tile * kTileTc;
-      u.tok_end = std::min((tile + take) * kTileTc, len[req]);
-      u.out_slot = -1;
-      u.page_base = indptr[req];
-      u.kv_len = len[req];
-      u.slot0 = 0;
-      u.n_slots = 0;
-      quota -= take;
-      tile += take;
-      if (tile == tiles_of_req(req)) {
-        tile = 0;
-        ++req;
-        while (req < batch && tiles_of_req(req) == 0) ++req;
-      }
-    }
-  }
-  wptr[n_workers] = nu;
-  // units of one request are consecutive: a run of two or more is a split request
-  int slot = 0, nm = 0, i = 0;
-  for (int b = 0; b < batch; ++b) {
-    if (tiles_of_req(b) == 0) {
-      merge[nm++] = MergeEntry{b, 0, 0};
-      continue;
-    }
-    int j = i;
-    while (j < nu && units[j].req == b) ++j;
-    if (j - i >= 2) {
-      for (int k = i; k < j; ++k) {
-        units[k].out_slot = slot + (k - i);
-        units[k].slot0 = slot;
-        units[k].n_slots = j - i;
-      }
-      merge[nm++] = MergeEntry{b, slot, j - i};
-      slot += j - i;
-    }
-    i = j;
-  }
-  *n_merge = nm;
-  *n_slots = slot;
-  return nu;
-}
-
 }  // namespace
 }  // namespace mla
 
@@ -164,9 +103,10 @@ extern "C" mla_status_t mla_decode_noalloc(
   // only after the partition: staged separately, then placed
   int32_t wptr_tmp[kMaxWorkers + 1];
   static MergeEntry merge_stage[kMaxBatch];
-  int n_merge = 0, n_slots = 0;
-  const int n_units = partition_fixed(kv_indptr_host, kv_len_host, batch, su.n_workers, units,
-                                      wptr_tmp, merge_stage, &n_merge, &n_slots);
+  int n_merge = 0;
+  const int n_units = partition_units(kv_indptr_host, kv_len_host, batch, su.n_workers, kTileTc,
+                                      units, wptr_tmp);
+  const int n_slots = assign_slots(units, n_units, kv_len_host, batch, kTileTc, merge_stage, &n_merge);
   const size_t off_wptr = align_up(off_units + sizeof(WorkUnit) * n_units, 16);
   const size_t off_merge = align_up(off_wptr + sizeof(int32_t) * (su.n_workers + 1), 16);
   const size_t blob_bytes = off_merge + sizeof(MergeEntry) * n_merge;

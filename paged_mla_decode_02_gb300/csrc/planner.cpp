@@ -7,14 +7,18 @@
 // the same PR's decode_wrapper.plan review (head_dim_ckv = kv_lora_rank,
 // head_dim_kpe = qk_rope_head_dim, page_size, causal=False, sm_scale).
 //
-// Split policy: the batch's tiles are laid end to end, request after request,
-// and cut into n_workers contiguous ranges of equal tile count (the first
-// total % n_workers ranges take one tile more).  A range that crosses a
-// request boundary becomes several work units.  A request covered by a single
-// unit writes its final output directly; a request cut into several units
-// writes one partial (O, lse) per unit and is combined by the merge kernel by
-// log-sum-exp, the combination that cascade attention relies on ("[V1][Core]
-// FlashInfer attention backend for V1", vLLM PR #14061, "Outstanding items").
+// Split policy: requests are laid end to end and dealt to the n_workers
+// workers in order, each worker taking a contiguous run of them.  The plan
+// minimises the largest worker cost under a simple model (quarter tiles): a
+// tile costs kTileCost, every work unit kUnitCost more (the pipeline refills
+// and an epilogue runs), and a unit of a split request kSplitCost more again
+// (its share goes out to memory and is merged).  A request is cut only where
+// a worker fills up, and only into pieces of at least kMinPiece tiles.  A
+// request covered by one unit
+// writes its final output directly; a request cut into several units writes
+// one partial (O, lse) per unit, combined by log-sum-exp, the combination
+// that cascade attention relies on ("[V1][Core] FlashInfer attention backend
+// for V1", vLLM PR #14061, "Outstanding items").
 #include "planner.h"
 
 #include <algorithm>
@@ -72,74 +76,136 @@ mla_status_t validate_batch(const int32_t* kv_indptr, const int32_t* kv_len, int
   return MLA_OK;
 }
 
-void partition_batch(const int32_t* kv_indptr, const int32_t* kv_len, int batch,
-                     int n_workers, int tile_tokens, Partition* out) {
-  out->units.clear();
-  out->merge.clear();
-  out->worker_ptr.assign(n_workers + 1, 0);
-  std::vector<int> tiles(batch);
-  long long total = 0;
-  for (int b = 0; b < batch; ++b) {
-    tiles[b] = (kv_len[b] + tile_tokens - 1) / tile_tokens;
-    total += tiles[b];
-  }
-  out->total_tiles = static_cast<int>(total);
+namespace {
 
-  // Equal shares: the first (total % n_workers) workers take one tile more.
-  const long long base = total / n_workers;
-  const long long extra = total % n_workers;
-  int req = 0, tile = 0;  // cursor over the flattened tile sequence
-  while (req < batch && tiles[req] == 0) ++req;
-  for (int w = 0; w < n_workers; ++w) {
-    out->worker_ptr[w] = static_cast<int32_t>(out->units.size());
-    long long quota = base + (w < extra ? 1 : 0);
-    while (quota > 0 && req < batch) {
-      const int take = static_cast<int>(std::min<long long>(quota, tiles[req] - tile));
-      WorkUnit u;
-      u.req = req;
-      u.tok_begin = tile * tile_tokens;
-      u.tok_end = std::min((tile + take) * tile_tokens, kv_len[req]);
+constexpr int tiles_of(int32_t len, int tile_tokens) { return (len + tile_tokens - 1) / tile_tokens; }
+
+// Greedy fill at makespan `budget` (cost units).  Requests are taken in
+// order; a worker takes whole requests while they fit, and the first one that
+// does not is cut so that the worker is full, when both pieces keep at least
+// kMinPiece tiles (else the next worker starts with it).  Writes the
+// units (req, token range, page base, length) and the worker offsets when
+// `units` is non-null.  Returns the number of units, or -1 when the batch
+// needs more than n_workers workers at this budget.
+int fill_workers(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int n_workers,
+                 int tile_tokens, long long budget, WorkUnit* units, int32_t* worker_ptr) {
+  int w = 0, nu = 0;
+  long long used = 0;   // cost taken by worker w
+  if (worker_ptr) worker_ptr[0] = 0;
+  auto emit = [&](int b, int t0, int t1) {
+    if (units) {
+      WorkUnit& u = units[nu];
+      u.req = b;
+      u.tok_begin = t0 * tile_tokens;
+      u.tok_end = std::min(t1 * tile_tokens, kv_len[b]);
       u.out_slot = -1;
-      u.page_base = kv_indptr[req];
-      u.kv_len = kv_len[req];
+      u.page_base = kv_indptr[b];
+      u.kv_len = kv_len[b];
       u.slot0 = 0;
       u.n_slots = 0;
-      out->units.push_back(u);
-      quota -= take;
-      tile += take;
-      if (tile == tiles[req]) {
-        tile = 0;
-        ++req;
-        while (req < batch && tiles[req] == 0) ++req;
+    }
+    ++nu;
+  };
+  auto next_worker = [&]() {
+    ++w;
+    used = 0;
+    if (worker_ptr && w <= n_workers) worker_ptr[w] = nu;
+  };
+  for (int b = 0; b < batch; ++b) {
+    const int n = tiles_of(kv_len[b], tile_tokens);
+    int t = 0;
+    bool split = false;
+    while (t < n) {
+      if (w >= n_workers) return -1;
+      const int rest = n - t;
+      const long long whole = kUnitCost + static_cast<long long>(kTileCost) * rest + (split ? kSplitCost : 0);
+      if (used + whole <= budget) {
+        emit(b, t, n);
+        used += whole;
+        break;
       }
+      // tiles that fit as a piece of a split request; both pieces keep at
+      // least kMinPiece tiles
+      const long long room = (budget - used - kUnitCost - kSplitCost) / kTileCost;
+      const long long take = std::min<long long>(room, rest - kMinPiece);
+      if (take < kMinPiece) {
+        if (used == 0) return -1;   // not even an empty worker takes a piece
+        next_worker();              // the next worker starts with this request
+        continue;
+      }
+      emit(b, t, t + static_cast<int>(take));
+      t += static_cast<int>(take);
+      split = true;
+      next_worker();
     }
   }
-  out->worker_ptr[n_workers] = static_cast<int32_t>(out->units.size());
+  if (worker_ptr)
+    for (int v = w + 1; v <= n_workers; ++v) worker_ptr[v] = nu;
+  return nu;
+}
 
-  // Slots for split requests, merge entries for split and empty requests.
-  std::vector<int> n_units(batch, 0);
-  for (const WorkUnit& u : out->units) ++n_units[u.req];
-  int slot = 0;
+}  // namespace
+
+int partition_units(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int n_workers,
+                    int tile_tokens, WorkUnit* units, int32_t* worker_ptr) {
+  // Smallest budget the greedy fill meets, by bisection; one worker holding
+  // everything always fits.
+  long long total = 0;
+  for (int b = 0; b < batch; ++b) total += tiles_of(kv_len[b], tile_tokens);
+  long long lo = 0;
+  long long hi = kTileCost * total + static_cast<long long>(kUnitCost + kSplitCost) * (batch + n_workers);
+  while (lo + 1 < hi) {
+    const long long mid = lo + (hi - lo) / 2;
+    if (fill_workers(kv_indptr, kv_len, batch, n_workers, tile_tokens, mid, nullptr, nullptr) >= 0)
+      hi = mid;
+    else
+      lo = mid;
+  }
+  return fill_workers(kv_indptr, kv_len, batch, n_workers, tile_tokens, hi, units, worker_ptr);
+}
+
+int assign_slots(WorkUnit* units, int n_units, const int32_t* kv_len, int batch, int tile_tokens,
+                 MergeEntry* merge, int* n_merge) {
+  // Units of one request are consecutive (the fill walks requests in order):
+  // a run of two or more is a split request, whose k-th unit takes slot
+  // first + k.  Empty requests get a merge entry without slots.
+  int slot = 0, nm = 0, i = 0;
   for (int b = 0; b < batch; ++b) {
-    if (tiles[b] == 0) {
-      out->merge.push_back(MergeEntry{b, 0, 0});
+    if (tiles_of(kv_len[b], tile_tokens) == 0) {
+      merge[nm++] = MergeEntry{b, 0, 0};
       continue;
     }
-    if (n_units[b] < 2) continue;
-    out->merge.push_back(MergeEntry{b, slot, n_units[b]});
-    slot += n_units[b];
-  }
-  // Units of one request are consecutive in the unit list (the walk above is
-  // in tile order), so the k-th unit of request b takes slot first_slot + k.
-  std::vector<int> first(batch, 0), next(batch, 0);
-  for (const MergeEntry& m : out->merge) first[m.req] = next[m.req] = m.first_slot;
-  for (WorkUnit& u : out->units)
-    if (n_units[u.req] >= 2) {
-      u.out_slot = next[u.req]++;
-      u.slot0 = first[u.req];
-      u.n_slots = n_units[u.req];
+    int j = i;
+    while (j < n_units && units[j].req == b) ++j;
+    if (j - i >= 2) {
+      for (int k = i; k < j; ++k) {
+        units[k].out_slot = slot + (k - i);
+        units[k].slot0 = slot;
+        units[k].n_slots = j - i;
+      }
+      merge[nm++] = MergeEntry{b, slot, j - i};
+      slot += j - i;
     }
-  out->n_slots = slot;
+    i = j;
+  }
+  *n_merge = nm;
+  return slot;
+}
+
+void partition_batch(const int32_t* kv_indptr, const int32_t* kv_len, int batch,
+                     int n_workers, int tile_tokens, Partition* out) {
+  out->units.resize(max_units(n_workers, batch));
+  out->worker_ptr.assign(n_workers + 1, 0);
+  out->merge.resize(batch);
+  long long total = 0;
+  for (int b = 0; b < batch; ++b) total += tiles_of(kv_len[b], tile_tokens);
+  out->total_tiles = static_cast<int>(total);
+  const int nu = partition_units(kv_indptr, kv_len, batch, n_workers, tile_tokens,
+                                 out->units.data(), out->worker_ptr.data());
+  out->units.resize(nu);
+  int nm = 0;
+  out->n_slots = assign_slots(out->units.data(), nu, kv_len, batch, tile_tokens, out->merge.data(), &nm);
+  out->merge.resize(nm);
 }
 
 }  // namespace mla

@@ -22,14 +22,37 @@ mla_status_t validate_batch(const int32_t* kv_indptr, const int32_t* kv_len, int
                             int head_dim_ckv, int head_dim_kpe, int page_size,
                             float sm_scale, std::string* why);
 
-// Splits the batch's tile_tokens-token tiles into n_workers contiguous ranges
-// of (nearly) equal tile count; each range is cut at request boundaries into
-// work units.
+// Cost model of the split, in quarter tiles: one tile costs kTileCost, a work
+// unit kUnitCost on top (pipeline fill and epilogue), a unit of a split
+// request kSplitCost more (its share is stored and merged).  Requests are cut
+// only into pieces of at least kMinPiece tiles.
+constexpr int kTileCost = 4;
+constexpr int kUnitCost = 8;
+constexpr int kSplitCost = 4;
+constexpr int kMinPiece = 4;
+
+// Deals the requests' tile_tokens-token tiles to n_workers workers (each a
+// contiguous run of requests, cut into work units at request boundaries) so
+// that the largest worker cost is as small as the greedy fill allows.  Writes
+// units[0 .. return value) (out_slot -1, no slots yet) and worker_ptr[0 ..
+// n_workers]; units needs max_units(n_workers, batch) entries.  Allocates
+// nothing.
+int partition_units(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int n_workers,
+                    int tile_tokens, WorkUnit* units, int32_t* worker_ptr);
+
+// Gives the units of every split request consecutive partial slots and
+// writes one merge entry per split request and per empty request (at most
+// batch entries).  Returns the number of slots.  Allocates nothing.
+int assign_slots(WorkUnit* units, int n_units, const int32_t* kv_len, int batch, int tile_tokens,
+                 MergeEntry* merge, int* n_merge);
+
+// Both steps into growable arrays.
 void partition_batch(const int32_t* kv_indptr, const int32_t* kv_len, int batch,
                      int n_workers, int tile_tokens, Partition* out);
 
 // Upper bounds of the partition sizes, used to size plan buffers at creation:
-// each worker range adds at most one unit beyond the requests it starts.
+// a request is cut only where a worker ends, so each worker adds at most one
+// unit beyond the requests.
 inline int max_units(int n_workers, int max_batch) { return n_workers + max_batch; }
 inline int max_slots(int n_workers, int max_batch) { return n_workers + max_batch; }
 

@@ -267,8 +267,8 @@ def test_full_size_config_sampled(kernel, cfg):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("cfg, lens, heads, P", [
-    ("split_many", [4000, 1, 777], 128, 16),   # a request spread over dozens of units
-    ("deepseek", None, None, None),            # every request split in two
+    ("split_many", [20000, 1, 777], 128, 16),  # one request over ~two dozen units
+    ("ragged", None, None, None),              # many requests split in two or three
 ])
 def test_split_requests_deterministic(kernel, cfg, lens, heads, P):
     # Split requests are combined by whichever unit finishes last; the result
@@ -284,5 +284,11 @@ def test_split_requests_deterministic(kernel, cfg, lens, heads, P):
     reqs = _sample(x, 3) if x.batch > 8 else list(range(x.batch))
     ref_out, ref_lse = O.mla_decode_inputs(x, requests=reqs)
     assert_parity(o0[reqs], l0[reqs], ref_out, ref_lse, f"{cfg} {reqs}")
+    if kernel == "tcgen05":
+        # every request (however many units it was split into, and whichever
+        # unit merged it) against the independent mma.sync kernel, whose
+        # partials are combined by a separate merge kernel
+        om, lm = run_decode(x, d, "mma_sync", torch.float32)
+        assert_parity(o0, l0, om, lm, f"{cfg}: tcgen05 vs mma.sync, all requests")
     del d
     torch.cuda.empty_cache()

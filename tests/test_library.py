@@ -74,14 +74,27 @@ def _check_partition(lens, P, W, T):
             assert a1 == b0
         if len(segs) == 1:
             assert segs[0][2] == -1
-    # balance: tile counts per worker differ by at most one
+    # balance under the planner's cost model (quarter tiles): a tile costs
+    # TILE, a unit UNIT more, a unit of a split request SPLIT more again.  The
+    # largest worker cost stays within a fixed margin of the perfect share of
+    # the work that cannot be avoided (tiles and one unit per request); every
+    # piece of a split request has at least MIN_PIECE tiles.
+    TILE, UNIT, SPLIT, MIN_PIECE = 4, 8, 4, 4
     tiles = np.zeros(W, np.int64)
+    cost = np.zeros(W, np.int64)
     for w in range(W):
         for u in units[wptr[w]:wptr[w + 1]]:
-            tiles[w] += (u[2] - u[1] + T - 1) // T
+            n = (u[2] - u[1] + T - 1) // T
+            tiles[w] += n
+            cost[w] += TILE * n + UNIT + (SPLIT if u[3] >= 0 else 0)
     total = int(((lens + T - 1) // T).sum())
     assert tiles.sum() == total
-    assert tiles.max() - tiles.min() <= 1
+    share = (TILE * total + UNIT * int((lens > 0).sum())) / W
+    assert cost.max() <= share + 2 * (UNIT + SPLIT) + TILE * MIN_PIECE, (cost.max(), share)
+    assert len(units) <= W + len(lens)
+    for b in range(len(lens)):
+        if len(cover[b]) > 1:
+            assert min((t1 - t0 + T - 1) // T for t0, t1, _ in cover[b]) >= MIN_PIECE
     # merge entries: split requests get consecutive slots, empty ones n_slots 0
     used = []
     for req, first, n in merge:
@@ -114,9 +127,13 @@ def test_partition_named_shapes(lib):
     _check_partition([0, 0, 5], 16, 3, 128)
 
 
-def test_partition_long_request_split_over_all_workers(lib):
+def test_partition_long_request_split_over_the_workers(lib):
+    # 1024 tiles on 76 workers: pieces of at most 14 tiles (the smallest
+    # whole-tile share), one per worker, all merged as one request
     units, merge = _check_partition([131072], 64, 76, 128)
-    assert len(units) == 76 and merge.shape[0] == 1 and merge[0, 2] == 76
+    pieces = (units[:, 2] - units[:, 1] + 127) // 128
+    assert pieces.max() == 14 and len(units) == 74
+    assert merge.shape[0] == 1 and merge[0, 2] == len(units)
 
 
 @pytest.mark.parametrize("bad, status", [
