@@ -18,7 +18,9 @@
 // over the cluster's CTAs: the owner of tile g (g mod C == rank) loads its K,
 // computes S = Q K^T and the softmax, and sends P (bf16) with the tile's
 // reference max and row sums to the other CTAs through distributed shared
-// memory (one bulk copy per CTA).  Every CTA then accumulates P . V over its
+// memory (bulk copies: row info and the first 64 tokens of P, then the
+// other 64 on a second barrier, so the receiver's P . V starts on the first
+// half while the second lands).  Every CTA then accumulates P . V over its
 // own dims.  So every score tile is computed once.  The grid is persistent:
 // one cluster per worker, walking its units.
 //
@@ -127,14 +129,15 @@ enum Bar {
   kVFull0 = kKEmpty0 + kMaxKSlots, kVEmpty0 = kVFull0 + kMaxVSlots, kVTail0 = kVEmpty0 + kMaxVSlots,
   kSFull = kVTail0 + kMaxVSlots, kSFree,
   kPFree0,          // 2, by tile parity: every CTA's PV of the tile done (its P buffer reusable)
-  kPRecv0 = kPFree0 + 2,   // 2, by P buffer: a peer's P and info for a tile it owns have landed
+  kPRecv0 = kPFree0 + 2,   // 2, by P buffer: a peer's row info and P token panel 0 have landed
   kPReady0 = kPRecv0 + 2,  // 2, by tile parity: tile released to PV (O rescaled, P in place)
   kPvDone0 = kPReady0 + 2,   // 2, by tile parity: this CTA's PV of the tile completed
   kOFree = kPvDone0 + 2, kFinal, kFinalPv,
   kXchg0, kMaxX0 = kXchg0 + 4,   // 4, per lane quadrant: the two warps' row maxima posted
   kMergeB = kMaxX0 + 4,   // split unit: merge-or-publish decided (flag in shared memory)
   kPWritten,              // own tile: all 8 softmax warps wrote their P rows and row info
-  kNumBars
+  kPRecvB0,               // 2, by P buffer: a peer's P token panel 1 has landed
+  kNumBars = kPRecvB0 + 2
 };
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
 
@@ -187,7 +190,7 @@ __device__ __forceinline__ void load_q_tmem(const DecodeArgs& a, int req, int r,
                                                    row * kDCkv + 64 * L::kQSmemPanels);
   const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_pe) +
                                                    row * kDKpe);
-#pragma unroll 1
+#pragma unroll
   for (int p = kPer * hc; p < kPer * hc + kPer; ++p) {
     const uint4* src = p < L::kQTmemPanels - 1 ? qn + p * 8 : qp;
     uint32_t v[32];
@@ -499,6 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0, uidx = 0, vslot = 0;
     uint32_t vphase = 0;
     uint32_t tail_par = 0;   // per V slot: parity of its next tail-chunk release
+    uint32_t recvb_par = 0;  // per P buffer: parity of its next token-panel-1 receive
     bool ok = true;
     const volatile int* merge_flag = reinterpret_cast<const volatile int*>(sm + L::kOffBar + kNumBars * 8 + 8);
     // After unit v's epilogue released O (kOFree): if v is a split unit that
@@ -526,7 +530,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tc_fence_after();
         const uint64_t p_desc = p_desc0 + static_cast<uint64_t>(((L::kPBufs == 2 ? (g & 1) : 0) * L::kPStride) >> 4);
+        // a received tile's second token panel (tokens 64..127) may still be
+        // in flight: it is waited for before the first MMA that reads it
+        const int bb = L::kPBufs == 2 ? (g & 1) : 0;
+        bool have_b = g % C == rank;
         for (int c = 0; c < nch; ++c) {
+          if (!have_b && c * kVChunkTok >= 64) {
+            if (!(ok = mbar_wait_warp(bar_addr<C>(base, kPRecvB0 + bb), (recvb_par >> bb) & 1, abort_flag))) break;
+            recvb_par ^= 1u << bb;
+            have_b = true;
+          }
           const int slot = vslot;
           const uint32_t ph = vphase;
           if (++vslot == L::kVSlots) {
@@ -552,6 +565,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_commit(bar_addr<C>(base, kVEmpty0 + slot), issue);
         }
         if (!ok) break;
+        if (!have_b) {
+          if (!(ok = mbar_wait_warp(bar_addr<C>(base, kPRecvB0 + bb), (recvb_par >> bb) & 1, abort_flag))) break;
+          recvb_par ^= 1u << bb;
+        }
         mma_commit(bar_addr<C>(base, kPvDone0 + (g & 1)), issue);
         // the tile's P buffer is reusable once every CTA's PV of the tile is done
         mma_commit_mc(bar_addr<C>(base, kPFree0 + (g & 1)), static_cast<uint16_t>((1u << C) - 1), issue);
@@ -727,7 +744,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tlr = own_lr;
         } else {
           const int b = L::kPBufs == 2 ? (t & 1) : 0;   // P buffer (and received info) of tile t
-          if (warp == 3 && lane == 0) mbar_arrive_expect_tx(bar_addr<C>(base, kPRecv0 + b), kRecvBytes);
+          if (warp == 3 && lane == 0) {
+            mbar_arrive_expect_tx(bar_addr<C>(base, kPRecvB0 + b), kPanel);
+            mbar_arrive_expect_tx(bar_addr<C>(base, kPRecv0 + b), kRecvBytes - kPanel);
+          }
           if (!(ok = mbar_wait_warp(bar_addr<C>(base, kPRecv0 + b), (recv_par >> b) & 1, abort_flag)))
             break;
           recv_par ^= 1u << b;
@@ -791,11 +811,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
           *reinterpret_cast<float4*>(sm + pbuf + 2 * kPanel + info_off) =
               make_float4(own_m, own_lx, own_lr, 0.f);
-          // Once all eight warps wrote their rows, one thread sends the whole
-          // buffer (P and row info, 36 KB) to every other CTA of the cluster
-          // with one bulk copy each: the copy engine moves distributed shared
-          // memory far faster than remote stores, and one large copy costs
-          // much less than one per warp.
+          // Once all eight warps wrote their rows, one thread sends the buffer
+          // to every other CTA of the cluster by bulk copies: the row info
+          // with token panel 0, then token panel 1 on a second barrier, so the
+          // peer's PV starts on tokens 0..63 while the rest is in flight.  The
+          // copy engine moves distributed shared memory far faster than
+          // remote stores, and a few large copies cost much less than one per
+          // warp.
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar_addr<C>(base, kPWritten));
@@ -806,8 +828,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int pr = 1; pr < C; ++pr) {
                 const uint32_t peer = static_cast<uint32_t>(rank ^ pr);
-                bulk_copy_to_peer(map_to_rank(base + pbuf, peer), base + pbuf, kRecvBytes,
-                                  map_to_rank(bar_addr<C>(base, kPRecv0 + b), peer));
+                const uint32_t ra = map_to_rank(bar_addr<C>(base, kPRecv0 + b), peer);
+                bulk_copy_to_peer(map_to_rank(base + pbuf + 2 * kPanel, peer), base + pbuf + 2 * kPanel, kInfoBytes, ra);
+                bulk_copy_to_peer(map_to_rank(base + pbuf, peer), base + pbuf, kPanel, ra);
+                bulk_copy_to_peer(map_to_rank(base + pbuf + kPanel, peer), base + pbuf + kPanel, kPanel,
+                                  map_to_rank(bar_addr<C>(base, kPRecvB0 + b), peer));
               }
             }
           }
