@@ -18,9 +18,9 @@
 // over the cluster's CTAs: the owner of tile g (g mod C == rank) loads its K,
 // computes S = Q K^T and the softmax, and sends P (bf16) with the tile's
 // reference max and row sums to the other CTAs through distributed shared
-// memory (bulk copies: row info and the first 64 tokens of P, then the
-// other 64 on a second barrier, so the receiver's P . V starts on the first
-// half while the second lands).  Every CTA then accumulates P . V over its
+// memory (bulk copies on three barriers: the row info, the first 64 tokens
+// of P, the other 64, so the receiver applies the tile and starts P . V on
+// the first half while the rest lands).  Every CTA then accumulates P . V over its
 // own dims.  So every score tile is computed once.  The grid is persistent:
 // one cluster per worker, walking its units.
 //
@@ -129,7 +129,7 @@ enum Bar {
   kVFull0 = kKEmpty0 + kMaxKSlots, kVEmpty0 = kVFull0 + kMaxVSlots, kVTail0 = kVEmpty0 + kMaxVSlots,
   kSFull = kVTail0 + kMaxVSlots, kSFree,
   kPFree0,          // 2, by tile parity: every CTA's PV of the tile done (its P buffer reusable)
-  kPRecv0 = kPFree0 + 2,   // 2, by P buffer: a peer's row info and P token panel 0 have landed
+  kPRecv0 = kPFree0 + 2,   // 2, by P buffer: a peer's row info for a tile it owns has landed
   kPReady0 = kPRecv0 + 2,  // 2, by tile parity: tile released to PV (O rescaled, P in place)
   kPvDone0 = kPReady0 + 2,   // 2, by tile parity: this CTA's PV of the tile completed
   kOFree = kPvDone0 + 2, kFinal, kFinalPv,
@@ -137,7 +137,8 @@ enum Bar {
   kMergeB = kMaxX0 + 4,   // split unit: merge-or-publish decided (flag in shared memory)
   kPWritten,              // own tile: all 8 softmax warps wrote their P rows and row info
   kPRecvB0,               // 2, by P buffer: a peer's P token panel 1 has landed
-  kNumBars = kPRecvB0 + 2
+  kPRecvP0 = kPRecvB0 + 2,  // 2, by P buffer: a peer's P token panel 0 has landed
+  kNumBars = kPRecvP0 + 2
 };
 static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
 
@@ -503,6 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t vphase = 0;
     uint32_t tail_par = 0;   // per V slot: parity of its next tail-chunk release
     uint32_t recvb_par = 0;  // per P buffer: parity of its next token-panel-1 receive
+    uint32_t recvp_par = 0;  // per P buffer: parity of its next token-panel-0 receive
     bool ok = true;
     const volatile int* merge_flag = reinterpret_cast<const volatile int*>(sm + L::kOffBar + kNumBars * 8 + 8);
     // After unit v's epilogue released O (kOFree): if v is a split unit that
@@ -530,10 +532,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tc_fence_after();
         const uint64_t p_desc = p_desc0 + static_cast<uint64_t>(((L::kPBufs == 2 ? (g & 1) : 0) * L::kPStride) >> 4);
-        // a received tile's second token panel (tokens 64..127) may still be
-        // in flight: it is waited for before the first MMA that reads it
+        // A received tile's P arrives in two token panels after its row info
+        // (which the softmax warps waited for): each is waited for before the
+        // first MMA that reads it.
         const int bb = L::kPBufs == 2 ? (g & 1) : 0;
         bool have_b = g % C == rank;
+        if (g % C != rank) {
+          if (!(ok = mbar_wait_warp(bar_addr<C>(base, kPRecvP0 + bb), (recvp_par >> bb) & 1, abort_flag))) break;
+          recvp_par ^= 1u << bb;
+        }
         for (int c = 0; c < nch; ++c) {
           if (!have_b && c * kVChunkTok >= 64) {
             if (!(ok = mbar_wait_warp(bar_addr<C>(base, kPRecvB0 + bb), (recvb_par >> bb) & 1, abort_flag))) break;
@@ -746,7 +753,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int b = L::kPBufs == 2 ? (t & 1) : 0;   // P buffer (and received info) of tile t
           if (warp == 3 && lane == 0) {
             mbar_arrive_expect_tx(bar_addr<C>(base, kPRecvB0 + b), kPanel);
-            mbar_arrive_expect_tx(bar_addr<C>(base, kPRecv0 + b), kRecvBytes - kPanel);
+            mbar_arrive_expect_tx(bar_addr<C>(base, kPRecvP0 + b), kPanel);
+            mbar_arrive_expect_tx(bar_addr<C>(base, kPRecv0 + b), kInfoBytes);
           }
           if (!(ok = mbar_wait_warp(bar_addr<C>(base, kPRecv0 + b), (recv_par >> b) & 1, abort_flag)))
             break;
@@ -756,7 +764,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           mt = info[0];
           tlx = info[1];
           tlr = info[2];
-          fence_proxy_async_smem();   // P written through the peer is read by the MMA next
         }
         // Stay at most two tiles ahead of PV (PV(t-2) complete): with one
         // kPvDone barrier per tile parity, every wait below is then less
@@ -812,9 +819,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<float4*>(sm + pbuf + 2 * kPanel + info_off) =
               make_float4(own_m, own_lx, own_lr, 0.f);
           // Once all eight warps wrote their rows, one thread sends the buffer
-          // to every other CTA of the cluster by bulk copies: the row info
-          // with token panel 0, then token panel 1 on a second barrier, so the
-          // peer's PV starts on tokens 0..63 while the rest is in flight.  The
+          // to every other CTA of the cluster by bulk copies on three
+          // barriers: the row info (all the peer's softmax warps need), token
+          // panel 0, token panel 1 -- so the peer applies the tile and starts
+          // its PV on tokens 0..63 while the rest is in flight.  The
           // copy engine moves distributed shared memory far faster than
           // remote stores, and a few large copies cost much less than one per
           // warp.
@@ -830,7 +838,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t peer = static_cast<uint32_t>(rank ^ pr);
                 const uint32_t ra = map_to_rank(bar_addr<C>(base, kPRecv0 + b), peer);
                 bulk_copy_to_peer(map_to_rank(base + pbuf + 2 * kPanel, peer), base + pbuf + 2 * kPanel, kInfoBytes, ra);
-                bulk_copy_to_peer(map_to_rank(base + pbuf, peer), base + pbuf, kPanel, ra);
+                bulk_copy_to_peer(map_to_rank(base + pbuf, peer), base + pbuf, kPanel,
+                                  map_to_rank(bar_addr<C>(base, kPRecvP0 + b), peer));
                 bulk_copy_to_peer(map_to_rank(base + pbuf + kPanel, peer), base + pbuf + kPanel, kPanel,
                                   map_to_rank(bar_addr<C>(base, kPRecvB0 + b), peer));
               }
