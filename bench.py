@@ -40,22 +40,30 @@ FLOP_PER_TOKEN_HEAD = 2 * 576 + 2 * 512          # QK^T over 576 + PV over 512
 
 
 def workload_config(x) -> dict:
-    return {"workload": f"paged MLA decode {x.name}: batch {x.batch}, heads {x.num_heads}, "
-                        f"kv_len {'mixed' if len(set(x.kv_len.tolist())) > 1 else int(x.kv_len[0])}, "
-                        f"page {x.page_size}, {x.kv_dtype} cache, kv_lora_rank 512, rope 64",
-            "batch": x.batch, "num_heads": x.num_heads, "page_size": x.page_size,
-            "total_kv_tokens": x.total_tokens, "kv_dtype": x.kv_dtype,
-            "sm_scale": x.sm_scale, "l2": "flushed between steps (256 MiB write)"}
+    qtok = f", {x.q_len} query tokens per request (causal in the block)" if x.q_len > 1 else ""
+    cfg = {"workload": f"paged MLA decode {x.name}: batch {x.batch}, heads {x.num_heads}, "
+                       f"kv_len {'mixed' if len(set(x.kv_len.tolist())) > 1 else int(x.kv_len[0])}, "
+                       f"page {x.page_size}, {x.kv_dtype} cache, kv_lora_rank 512, rope 64{qtok}",
+           "batch": x.batch, "num_heads": x.num_heads, "page_size": x.page_size,
+           "total_kv_tokens": x.total_tokens, "kv_dtype": x.kv_dtype,
+           "sm_scale": x.sm_scale, "l2": "flushed between steps (256 MiB write)"}
+    if x.q_len > 1:
+        cfg["q_len"] = x.q_len
+    return cfg
 
 
 def algorithmic(x) -> tuple[float, float]:
-    """(bytes, flops) one batch must move / compute, pad rows not counted."""
+    """(bytes, flops) one batch must move / compute, pad rows not counted.
+    With Q query tokens per request the cache is still needed once; query j
+    of a request attends to kv_len - Q + 1 + j tokens."""
     tok = float(x.total_tokens)
     kv_bytes_per_tok = 576 * (2 if x.kv_dtype == "bf16" else 1)
-    H, B = x.num_heads, x.batch
-    nbytes = (tok * kv_bytes_per_tok + B * H * 576 * 2 + B * H * 512 * 2 + B * H * 4
+    H, B, Q = x.num_heads, x.batch, x.q_len
+    rows = B * Q * H
+    nbytes = (tok * kv_bytes_per_tok + rows * (576 * 2 + 512 * 2 + 4)
               + 4 * len(x.kv_indices) + 8 * B)
-    flops = tok * H * FLOP_PER_TOKEN_HEAD
+    seen = float(Q * x.kv_len.astype(np.int64).sum() - B * Q * (Q - 1) // 2)
+    flops = seen * H * FLOP_PER_TOKEN_HEAD
     return nbytes, flops
 
 
@@ -105,7 +113,11 @@ def oracle_sample(x, budget_s: float):
     order = list(range(x.batch))
     done, t0 = 0, time.perf_counter()
     for b in order:
-        O.mla_decode_inputs(x, requests=[b])
+        if x.q_len > 1:
+            O.mla_decode_multi(x.q_nope, x.q_pe, x.ckv, x.kpe, x.kv_indptr, x.kv_indices,
+                               x.kv_len, x.page_size, x.sm_scale, requests=[b])
+        else:
+            O.mla_decode_inputs(x, requests=[b])
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
@@ -239,15 +251,17 @@ def main() -> None:
 
     q_nope, q_pe, ckv, kpe = bf16(x.q_nope), bf16(x.q_pe), cache(x.ckv), cache(x.kpe)
     idx = torch.from_numpy(x.kv_indices).to(dev)
-    out = torch.empty((x.batch, x.num_heads, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((x.batch, x.num_heads), dtype=torch.float32, device=dev)
+    out = torch.empty(tuple(q_nope.shape[:-1]) + (512,), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(tuple(q_nope.shape[:-1]), dtype=torch.float32, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    dec = mla.MLADecoder(x.batch, x.num_heads, args.kernel)
+    multi = x.q_nope.ndim == 4          # several query tokens per request
+    dec = mla.MLADecoder(x.batch * x.q_len, x.num_heads, args.kernel)
     stream = torch.cuda.Stream(device=dev)
     t_plan = time.perf_counter()
     with torch.cuda.stream(stream):
-        dec.plan(x.kv_indptr, idx, x.kv_len, x.page_size, x.sm_scale)
+        dec.plan(x.kv_indptr, idx, x.kv_len, x.page_size, x.sm_scale,
+                 q_len=x.q_len if multi else 0)
     stream.synchronize()
     plan_us = (time.perf_counter() - t_plan) * 1e6
     info = dec.info()

@@ -117,6 +117,34 @@ mla_status_t mla_decode_plan(mla_plan_t plan, const int32_t* kv_indptr_host,
                              int page_size, float sm_scale, void* stream);
 
 /*
+ * Plan a decode step of q_len query tokens per request (speculative or
+ * multi-token decode: decode with short query lengths, which "[V1][Core]
+ * FlashInfer attention backend for V1" (vLLM PR #14061) finds the prefill
+ * wrapper serves poorly).
+ *   The q_len new tokens of request b are the last q_len of its kv_len cached
+ *   tokens; query j (0-based) sees the tokens at positions
+ *   0 .. kv_len[b] - q_len + j.  This is a causal mask inside the query block
+ *   and none before it.
+ *   Arguments as for mla_decode_plan.  In addition:
+ *   - q_len >= 1;
+ *   - every kv_len[b] >= q_len (else MLA_ERR_INVALID_ARG);
+ *   - batch * q_len <= the plan's max_batch (else MLA_ERR_CAPACITY).
+ *   mla_decode_run then takes
+ *     q_nope [batch, q_len, num_heads, 512],  q_pe [batch, q_len, num_heads, 64],
+ *     out    [batch, q_len, num_heads, 512],  lse  [batch, q_len, num_heads].
+ *   Each query token is planned as its own request over a prefix of its
+ *   request's pages, so a step reads each request's cache q_len times.
+ *   Consecutive queries of a request sit next to each other in the work
+ *   list, so those reads are mostly served by L2.
+ *   q_len = 1 plans exactly what mla_decode_plan plans.
+ */
+mla_status_t mla_decode_plan_multi(mla_plan_t plan, const int32_t* kv_indptr_host,
+                                   const int32_t* kv_indices_dev, const int32_t* kv_len_host,
+                                   int batch, int q_len, int num_heads, int head_dim_ckv,
+                                   int head_dim_kpe, int page_size, float sm_scale,
+                                   void* stream);
+
+/*
  * Run the planned batch on `stream`.  All tensor arguments are DEVICE pointers
  * to contiguous row-major arrays owned by the caller:
  *   q_nope    [batch, num_heads, 512]   q_dtype (MLA_DTYPE_BF16 only)

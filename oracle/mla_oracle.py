@@ -6,7 +6,8 @@ never calls it, and it shares no code with the CUDA path: it decodes the
 stored bf16 / fp8 codes itself, gathers pages itself and evaluates exact
 softmax attention in float64 with numpy.
 
-What it computes (absorbed multi-head latent attention, decode, q_len = 1):
+What it computes (absorbed multi-head latent attention, decode, q_len = 1;
+``mla_decode_multi`` extends it to several query tokens per request):
 for request b with pages ``kv_indices[kv_indptr[b]:kv_indptr[b+1]]`` and
 ``L = kv_len[b]`` tokens, C = the first L gathered ckv rows [L, 512] and
 R = the first L gathered kpe rows [L, 64]; for every head h
@@ -145,6 +146,50 @@ def mla_decode(q_nope, q_pe, ckv, kpe, kv_indptr, kv_indices, kv_len, page_size:
         qn = decode_bf16(q_nope[b])
         qp = decode_bf16(q_pe[b])
         out[i], lse[i] = attend(qn, qp, C, R, sm_scale)
+    return out, lse
+
+
+def mla_decode_multi(q_nope, q_pe, ckv, kpe, kv_indptr, kv_indices, kv_len, page_size: int,
+                     sm_scale: float, kv_dtype: str = "bf16", kv_scale: float = 1.0,
+                     requests=None):
+    """Oracle for decode steps of several query tokens per request.
+
+    q_nope / q_pe are bf16 bit arrays [B,Q,H,512] / [B,Q,H,64]: the Q newest
+    tokens of each request, whose keys are the last Q of its kv_len cached
+    tokens.  Query j (0-based) sits at position L - Q + j and sees the tokens
+    at positions 0 .. L - Q + j: a causal mask inside the query block, none
+    before it.  Returns float64 out [b,Q,H,512] and lse [b,Q,H].
+
+    Sources: decode with short query lengths, which the prefill wrapper serves
+    poorly ("[V1][Core] FlashInfer attention backend for V1", vLLM PR #14061,
+    review discussion of the wrapper's decode performance).  The mask is the
+    reading for speculative or multi-token decode: each new token attends to
+    the cache up to and including itself.
+    """
+    B = len(kv_len)
+    reqs = range(B) if requests is None else list(requests)
+    Q, H = q_nope.shape[1], q_nope.shape[2]
+    out = np.zeros((len(reqs), Q, H, D_CKV))
+    lse = np.zeros((len(reqs), Q, H))
+    for i, b in enumerate(reqs):
+        L = int(kv_len[b])
+        if L < Q:
+            raise ValueError("a request holds fewer cached tokens than query tokens")
+        C = dequantize(gather_request(ckv, kv_indptr, kv_indices, b, L, page_size), kv_dtype, kv_scale)
+        R = dequantize(gather_request(kpe, kv_indptr, kv_indices, b, L, page_size), kv_dtype, kv_scale)
+        pos = np.arange(L)
+        for j in range(Q):
+            qn = decode_bf16(q_nope[b, j])                      # [H,512]
+            qp = decode_bf16(q_pe[b, j])                        # [H,64]
+            s = sm_scale * (qn @ C.T + qp @ R.T)                # [H,L]
+            s = np.where(pos[None, :] <= L - Q + j, s, -np.inf)  # causal inside the block
+            m = s.max(axis=1, keepdims=True)
+            if not np.all(np.isfinite(m)):
+                raise FloatingPointError("non-finite score in the visible tokens")
+            l = np.exp(s - m).sum(axis=1, keepdims=True)
+            lse_j = m + np.log(l)
+            out[i, j] = np.exp(s - lse_j) @ C
+            lse[i, j] = lse_j[:, 0]
     return out, lse
 
 

@@ -12,6 +12,7 @@
 #include <cstring>
 #include <new>
 #include <string>
+#include <vector>
 
 #include "kernels.h"
 #include "mla_decode.h"
@@ -257,24 +258,16 @@ mla_status_t mla_plan_destroy(mla_plan_t plan) {
   return MLA_OK;
 }
 
-mla_status_t mla_decode_plan(mla_plan_t plan, const int32_t* kv_indptr_host,
-                             const int32_t* kv_indices_dev, const int32_t* kv_len_host,
-                             int batch, int num_heads, int head_dim_ckv, int head_dim_kpe,
-                             int page_size, float sm_scale, void* stream) {
-  if (!plan) return MLA_ERR_INVALID_ARG;
-  std::string why;
-  mla_status_t st = validate_batch(kv_indptr_host, kv_len_host, batch, head_dim_ckv,
-                                   head_dim_kpe, page_size, sm_scale, &why);
-  if (st != MLA_OK) return fail(plan, st, why);
-  if (num_heads != plan->num_heads)
-    return fail(plan, MLA_ERR_INVALID_ARG, "num_heads differs from the plan's num_heads");
-  if (batch > plan->max_batch)
-    return fail(plan, MLA_ERR_CAPACITY, "batch exceeds the plan's max_batch");
-  if (kv_indptr_host[batch] > 0 && kv_indices_dev == nullptr)
-    return fail(plan, MLA_ERR_INVALID_ARG, "kv_indices_dev is NULL");
+namespace {
 
+// Partition and upload for n_req requests given by the position of their
+// first page id in kv_indices (page_base) and their token counts (the
+// caller validated both).
+mla_status_t plan_requests(mla_plan_t plan, const int32_t* page_base, const int32_t* len, int n_req,
+                           const int32_t* kv_indices_dev, int num_heads, int page_size,
+                           float sm_scale, void* stream) {
   Partition part;
-  partition_batch(kv_indptr_host, kv_len_host, batch, plan->n_workers, plan->tile_tokens, &part);
+  partition_batch(page_base, len, n_req, plan->n_workers, plan->tile_tokens, &part);
   if (static_cast<int>(part.units.size()) > plan->units_cap || part.n_slots > plan->slots_cap ||
       static_cast<int>(part.merge.size()) > plan->merge_cap)
     return fail(plan, MLA_ERR_CAPACITY, "partition exceeds plan buffers");
@@ -288,7 +281,7 @@ mla_status_t mla_decode_plan(mla_plan_t plan, const int32_t* kv_indptr_host,
   prm.n_units = static_cast<int32_t>(part.units.size());
   prm.n_merge = static_cast<int32_t>(part.merge.size());
   prm.n_workers = plan->n_workers;
-  prm.batch = batch;
+  prm.batch = n_req;
   prm.num_heads = num_heads;
   prm.page_size = page_size;
   prm.sm_scale = sm_scale;
@@ -317,6 +310,67 @@ mla_status_t mla_decode_plan(mla_plan_t plan, const int32_t* kv_indptr_host,
   plan->planned = true;
   plan->last_error.clear();
   return MLA_OK;
+}
+
+// Checks shared by both plan entry points.
+mla_status_t check_plan_args(mla_plan_t plan, const int32_t* kv_indptr_host,
+                             const int32_t* kv_indices_dev, const int32_t* kv_len_host, int batch,
+                             int num_heads, int head_dim_ckv, int head_dim_kpe, int page_size,
+                             float sm_scale) {
+  std::string why;
+  mla_status_t st = validate_batch(kv_indptr_host, kv_len_host, batch, head_dim_ckv,
+                                   head_dim_kpe, page_size, sm_scale, &why);
+  if (st != MLA_OK) return fail(plan, st, why);
+  if (num_heads != plan->num_heads)
+    return fail(plan, MLA_ERR_INVALID_ARG, "num_heads differs from the plan's num_heads");
+  if (kv_indptr_host[batch] > 0 && kv_indices_dev == nullptr)
+    return fail(plan, MLA_ERR_INVALID_ARG, "kv_indices_dev is NULL");
+  return MLA_OK;
+}
+
+}  // namespace
+
+mla_status_t mla_decode_plan(mla_plan_t plan, const int32_t* kv_indptr_host,
+                             const int32_t* kv_indices_dev, const int32_t* kv_len_host,
+                             int batch, int num_heads, int head_dim_ckv, int head_dim_kpe,
+                             int page_size, float sm_scale, void* stream) {
+  if (!plan) return MLA_ERR_INVALID_ARG;
+  mla_status_t st = check_plan_args(plan, kv_indptr_host, kv_indices_dev, kv_len_host, batch,
+                                    num_heads, head_dim_ckv, head_dim_kpe, page_size, sm_scale);
+  if (st != MLA_OK) return st;
+  if (batch > plan->max_batch)
+    return fail(plan, MLA_ERR_CAPACITY, "batch exceeds the plan's max_batch");
+  return plan_requests(plan, kv_indptr_host, kv_len_host, batch, kv_indices_dev, num_heads,
+                       page_size, sm_scale, stream);
+}
+
+mla_status_t mla_decode_plan_multi(mla_plan_t plan, const int32_t* kv_indptr_host,
+                                   const int32_t* kv_indices_dev, const int32_t* kv_len_host,
+                                   int batch, int q_len, int num_heads, int head_dim_ckv,
+                                   int head_dim_kpe, int page_size, float sm_scale,
+                                   void* stream) {
+  if (!plan) return MLA_ERR_INVALID_ARG;
+  mla_status_t st = check_plan_args(plan, kv_indptr_host, kv_indices_dev, kv_len_host, batch,
+                                    num_heads, head_dim_ckv, head_dim_kpe, page_size, sm_scale);
+  if (st != MLA_OK) return st;
+  if (q_len < 1) return fail(plan, MLA_ERR_INVALID_ARG, "q_len must be >= 1");
+  if (static_cast<long long>(batch) * q_len > plan->max_batch)
+    return fail(plan, MLA_ERR_CAPACITY, "batch * q_len exceeds the plan's max_batch");
+  for (int b = 0; b < batch; ++b)
+    if (kv_len_host[b] < q_len)
+      return fail(plan, MLA_ERR_INVALID_ARG,
+                  "every request must hold its q_len query tokens in the cache (kv_len >= q_len)");
+  // Query j of request b sees the first kv_len - q_len + 1 + j tokens: it is
+  // planned as its own request over a prefix of b's pages, at row b * q_len + j
+  // of the [batch * q_len, heads] query and output arrays.
+  std::vector<int32_t> base(static_cast<size_t>(batch) * q_len), len(base.size());
+  for (int b = 0; b < batch; ++b)
+    for (int j = 0; j < q_len; ++j) {
+      base[static_cast<size_t>(b) * q_len + j] = kv_indptr_host[b];
+      len[static_cast<size_t>(b) * q_len + j] = kv_len_host[b] - q_len + 1 + j;
+    }
+  return plan_requests(plan, base.data(), len.data(), batch * q_len, kv_indices_dev, num_heads,
+                       page_size, sm_scale, stream);
 }
 
 mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_pe, int q_dtype,

@@ -37,8 +37,8 @@ FP8_E4M3_NAN_CODE = np.uint8(0x7F)
 @dataclasses.dataclass
 class MLAInputs:
     name: str
-    q_nope: np.ndarray      # uint16 [B,H,512]
-    q_pe: np.ndarray        # uint16 [B,H,64]
+    q_nope: np.ndarray      # uint16 [B,H,512], or [B,Q,H,512] with several query tokens
+    q_pe: np.ndarray        # uint16 [B,H,64], or [B,Q,H,64]
     ckv: np.ndarray         # uint16 or uint8 [pool,P,512]
     kpe: np.ndarray         # uint16 or uint8 [pool,P,64]
     kv_indptr: np.ndarray   # int32 [B+1]
@@ -54,8 +54,12 @@ class MLAInputs:
         return int(self.kv_len.shape[0])
 
     @property
+    def q_len(self) -> int:
+        return 1 if self.q_nope.ndim == 3 else int(self.q_nope.shape[1])
+
+    @property
     def num_heads(self) -> int:
-        return int(self.q_nope.shape[1])
+        return int(self.q_nope.shape[-2])
 
     @property
     def num_pages(self) -> int:
@@ -109,7 +113,7 @@ def make_inputs(name: str, kv_len, num_heads: int, page_size: int, *,
                 pool_pages: int | None = None, key_scale: float = 1.0,
                 kv_dtype: str = "bf16", kv_scale: float = 1.0,
                 sm_scale: float = 1.0 / math.sqrt(192.0),
-                poison: bool = False, slack_pages: int = 0) -> MLAInputs:
+                poison: bool = False, slack_pages: int = 0, q_len: int = 0) -> MLAInputs:
     """Build one paged batch.
 
     ``kv_len`` is either a sequence of ints or a callable ``rng -> int array``
@@ -117,7 +121,8 @@ def make_inputs(name: str, kv_len, num_heads: int, page_size: int, *,
     request order, from a random permutation of the pool.  ``poison`` fills
     every pool page no request uses, and every slot past ``kv_len`` in a
     request's last page, with NaN, so a kernel that reads them and lets them
-    reach an output fails parity.
+    reach an output fails parity.  ``q_len`` > 0 draws that many query tokens
+    per request (q arrays [B,Q,H,.]); 0 keeps the single-token layout [B,H,.].
     """
     if rng is None:
         rng = np.random.Generator(np.random.PCG64(seed))
@@ -137,8 +142,9 @@ def make_inputs(name: str, kv_len, num_heads: int, page_size: int, *,
     kv_indptr = np.zeros(batch + 1, dtype=np.int32)
     kv_indptr[1:] = np.cumsum(npages)
 
-    q_nope = _normal_codes(rng, (batch, num_heads, D_CKV), 1.0, "bf16")
-    q_pe = _normal_codes(rng, (batch, num_heads, D_KPE), 1.0, "bf16")
+    qs = (batch, num_heads) if q_len == 0 else (batch, q_len, num_heads)
+    q_nope = _normal_codes(rng, qs + (D_CKV,), 1.0, "bf16")
+    q_pe = _normal_codes(rng, qs + (D_KPE,), 1.0, "bf16")
     ckv = _normal_codes(rng, (pool, page_size, D_CKV), key_scale, kv_dtype, kv_scale)
     kpe = _normal_codes(rng, (pool, page_size, D_KPE), key_scale, kv_dtype, kv_scale)
 
@@ -178,6 +184,7 @@ def _lognormal_lengths(rng):
 CONFIGS = {
     "tiny": dict(kv_len=[33, 70], num_heads=16, page_size=16, pool_pages=16),
     "deepseek": dict(kv_len=[4096] * 64, num_heads=128, page_size=64),
+    "deepseek_mtp2": dict(kv_len=[4096] * 64, num_heads=128, page_size=64, q_len=2),
     "ragged": dict(kv_len=_ragged_lengths, num_heads=128, page_size=16),
     "long_b1": dict(kv_len=[131072], num_heads=16, page_size=64, key_scale=3.0),
     "long_b4": dict(kv_len=[131072] * 4, num_heads=16, page_size=64, key_scale=3.0),
@@ -188,6 +195,7 @@ CONFIGS = {
 CONFIG_DESCRIPTIONS = {
     "tiny": "B2 H16 P16 L{33,70} pool16 bf16",
     "deepseek": "B64 H128 P64 L4096 bf16",
+    "deepseek_mtp2": "B64 H128 P64 L4096 bf16, 2 query tokens per request",
     "ragged": "B128 H128 P16 L~U[1,8192] bf16",
     "long_b1": "B1 H16 P64 L131072 bf16 keys x3",
     "long_b4": "B4 H16 P64 L131072 bf16 keys x3",

@@ -32,7 +32,7 @@ KERNELS = {"default": KERNEL_DEFAULT, "tcgen05": KERNEL_TCGEN05, "mma_sync": KER
 EXPORTED = ("mla_plan_create", "mla_decode_plan", "mla_decode_run", "mla_decode_run_host",
             "mla_plan_check_status", "mla_plan_info", "mla_plan_destroy", "mla_status_string",
             "mla_plan_last_error", "mla_plan_partition_host", "mla_plan_set_profile_events",
-            "mla_decode_noalloc")
+            "mla_decode_noalloc", "mla_decode_plan_multi")
 
 
 class MLAError(RuntimeError):
@@ -79,6 +79,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_decode_plan.restype = c_int
     lib.mla_decode_plan.argtypes = [_VP, _I32P, _VP, _I32P, c_int, c_int, c_int, c_int, c_int,
                                     c_float, _VP]
+    lib.mla_decode_plan_multi.restype = c_int
+    lib.mla_decode_plan_multi.argtypes = [_VP, _I32P, _VP, _I32P, c_int, c_int, c_int, c_int,
+                                          c_int, c_int, c_float, _VP]
     lib.mla_decode_run.restype = c_int
     lib.mla_decode_run.argtypes = [_VP, _VP, _VP, c_int, _VP, _VP, c_int, c_float, c_int, _VP,
                                    c_int, _VP, _VP]
@@ -181,6 +184,25 @@ def mla_decode_plan(plan, kv_indptr, kv_indices, kv_len, num_heads: int, head_di
                              int(head_dim_ckv), int(head_dim_kpe), int(page_size),
                              float(sm_scale), _stream_handle(stream))
     _check(st, plan, "mla_decode_plan")
+
+
+def mla_decode_plan_multi(plan, kv_indptr, kv_indices, kv_len, q_len: int, num_heads: int,
+                          head_dim_ckv: int, head_dim_kpe: int, page_size: int, sm_scale: float,
+                          stream=None) -> None:
+    """Plan a step of q_len query tokens per request (causal inside the query
+    block; see mla_decode.h).  Arrays as for ``mla_decode_plan``."""
+    lib = load_library()
+    indptr = _i32_host(kv_indptr)
+    lens = _i32_host(kv_len)
+    batch = lens.shape[0]
+    if indptr.shape[0] != batch + 1:
+        raise ValueError("kv_indptr must have batch + 1 entries")
+    idx_ptr = _ptr(kv_indices) if kv_indices is not None and kv_indices.numel() > 0 else None
+    st = lib.mla_decode_plan_multi(plan, indptr.ctypes.data_as(_I32P), idx_ptr,
+                                   lens.ctypes.data_as(_I32P), batch, int(q_len), int(num_heads),
+                                   int(head_dim_ckv), int(head_dim_kpe), int(page_size),
+                                   float(sm_scale), _stream_handle(stream))
+    _check(st, plan, "mla_decode_plan_multi")
 
 
 def mla_decode_run(plan, q_nope, q_pe, ckv_cache, kpe_cache, out, lse, kv_scale: float = 1.0,
@@ -301,19 +323,27 @@ class MLADecoder:
         self._kv_indices = None
 
     def plan(self, kv_indptr, kv_indices, kv_len, page_size: int, sm_scale: float,
-             head_dim_ckv: int = 512, head_dim_kpe: int = 64, stream=None) -> None:
-        mla_decode_plan(self.handle, kv_indptr, kv_indices, kv_len, self.num_heads,
-                        head_dim_ckv, head_dim_kpe, page_size, sm_scale, stream)
+             head_dim_ckv: int = 512, head_dim_kpe: int = 64, stream=None, q_len: int = 0) -> None:
+        """q_len 0: one query token per request (q and out [B, H, .]);
+        q_len >= 1: that many, causal inside the block (q and out [B, Q, H, .])."""
+        if q_len:
+            mla_decode_plan_multi(self.handle, kv_indptr, kv_indices, kv_len, q_len,
+                                  self.num_heads, head_dim_ckv, head_dim_kpe, page_size,
+                                  sm_scale, stream)
+        else:
+            mla_decode_plan(self.handle, kv_indptr, kv_indices, kv_len, self.num_heads,
+                            head_dim_ckv, head_dim_kpe, page_size, sm_scale, stream)
+        self.q_len = int(q_len)
         self._kv_indices = kv_indices     # keep the borrowed page table alive
 
     def run(self, q_nope, q_pe, ckv_cache, kpe_cache, out=None, lse=None,
             kv_scale: float = 1.0, out_dtype=None, stream=None):
         import torch
-        B, H = q_nope.shape[0], q_nope.shape[1]
+        lead = tuple(q_nope.shape[:-1])          # (B, H) or (B, Q, H)
         if out is None:
-            out = torch.empty((B, H, 512), dtype=out_dtype or torch.bfloat16, device=q_nope.device)
+            out = torch.empty(lead + (512,), dtype=out_dtype or torch.bfloat16, device=q_nope.device)
         if lse is None:
-            lse = torch.empty((B, H), dtype=torch.float32, device=q_nope.device)
+            lse = torch.empty(lead, dtype=torch.float32, device=q_nope.device)
         mla_decode_run(self.handle, q_nope, q_pe, ckv_cache, kpe_cache, out, lse, kv_scale, stream)
         return out, lse
 

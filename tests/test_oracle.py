@@ -319,3 +319,61 @@ def test_pins_catch_page_indexing_mistake():
     out, _ = O.mla_decode(x.q_nope, x.q_pe, x.ckv, x.kpe, x.kv_indptr, shifted, x.kv_len,
                           x.page_size, x.sm_scale)
     assert np.abs(out - bo).max() > 1e-3
+
+
+# ---------------------------------------------------------------------------
+# several query tokens per request (causal inside the query block)
+# ---------------------------------------------------------------------------
+
+def _multi(lens, heads, P, Q, seed=31):
+    return I.make_inputs("mq", lens, heads, P, seed=seed, q_len=Q, slack_pages=2, poison=True)
+
+
+def _multi_oracle(x):
+    return O.mla_decode_multi(x.q_nope, x.q_pe, x.ckv, x.kpe, x.kv_indptr, x.kv_indices,
+                              x.kv_len, x.page_size, x.sm_scale)
+
+
+def test_multi_token_single_query_is_decode():
+    x = _multi([37, 5, 64], 4, 16, 1)
+    out, lse = _multi_oracle(x)
+    o1, l1 = O.mla_decode(x.q_nope[:, 0], x.q_pe[:, 0], x.ckv, x.kpe, x.kv_indptr,
+                          x.kv_indices, x.kv_len, x.page_size, x.sm_scale)
+    assert np.array_equal(out[:, 0], o1) and np.array_equal(lse[:, 0], l1)
+
+
+@pytest.mark.parametrize("Q", [2, 3, 5])
+def test_multi_token_query_j_is_decode_of_the_prefix(Q):
+    """Query j of a block of Q sees exactly the first L - Q + 1 + j tokens: it
+    equals single-token decode of the request cut to that length (through the
+    page table, so cut inside a page too), and differs from the lengths one
+    shorter or longer (an off-by-one or a missing mask is caught)."""
+    x = _multi([37, 5, 64], 4, 16, Q)
+    out, lse = _multi_oracle(x)
+    for j in range(Q):
+        cut = x.kv_len - Q + 1 + j
+        oj, lj = O.mla_decode(x.q_nope[:, j], x.q_pe[:, j], x.ckv, x.kpe, x.kv_indptr,
+                              x.kv_indices, cut, x.page_size, x.sm_scale)
+        assert np.abs(out[:, j] - oj).max() < 1e-12 and np.abs(lse[:, j] - lj).max() < 1e-12
+        for d in (-1, 1):
+            alt = np.clip(cut + d, 1, x.kv_len)
+            oa, _ = O.mla_decode(x.q_nope[:, j], x.q_pe[:, j], x.ckv, x.kpe, x.kv_indptr,
+                                 x.kv_indices, alt, x.page_size, x.sm_scale)
+            moved = alt != cut
+            if moved.any():
+                assert np.abs(out[moved, j] - oa[moved]).max(axis=(1, 2)).min() > 1e-6
+
+
+def test_multi_token_bruteforce():
+    x = _multi([6, 4], 2, 2, 3, seed=12)
+    out, lse = _multi_oracle(x)
+    for j in range(3):
+        bo, bl = _bruteforce(x.q_nope[:, j], x.q_pe[:, j], x.ckv, x.kpe, x.kv_indptr,
+                             x.kv_indices, x.kv_len - 3 + 1 + j, x.page_size, x.sm_scale)
+        assert np.abs(out[:, j] - bo).max() < 1e-12 and np.abs(lse[:, j] - bl).max() < 1e-12
+
+
+def test_multi_token_needs_the_query_tokens_in_the_cache():
+    x = _multi([2, 9], 2, 16, 3)
+    with pytest.raises(ValueError):
+        _multi_oracle(x)
