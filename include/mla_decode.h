@@ -223,6 +223,33 @@ mla_status_t mla_decode_noalloc(const int32_t* kv_indptr_host, const int32_t* kv
                                 float* lse, int check_status, void* stream);
 
 /*
+ * Combine two attention states of the same query rows over disjoint sets of
+ * tokens.  This is the log-sum-exp combination cascade (multi-level)
+ * attention relies on ("[V1][Core] FlashInfer attention backend for V1",
+ * vLLM PR #14061, "Outstanding items").  Decode a shared prefix and each
+ * request's own suffix as two batches, then merge: the result is the decode
+ * over the concatenated pages.
+ * For every row r (a request and head):
+ *   M = max(lse_a[r], lse_b[r]),  w_x = exp(lse_x[r] - M),
+ *   out[r] = (w_a o_a[r] + w_b o_b[r]) / (w_a + w_b),
+ *   lse_out[r] = M + ln(w_a + w_b).
+ *   A state with lse = -inf carries no weight, whatever its o holds.  Both
+ *   -inf give out = 0, lse = -inf.
+ *   o_a, o_b  DEVICE fp32 [rows, 512], 16-byte aligned;
+ *   lse_a, lse_b  DEVICE fp32 [rows] (natural log);
+ *   out       DEVICE [rows, 512] of out_dtype (MLA_DTYPE_BF16 or FP32), 16-byte
+ *             aligned; it may be o_a or o_b (fp32);
+ *   lse_out   DEVICE fp32 [rows]; it may be lse_a or lse_b.
+ * No allocation and no synchronisation; the work is queued on `stream`.
+ * Returns MLA_ERR_INVALID_ARG for rows < 0, a NULL pointer or a misaligned
+ * tensor, MLA_ERR_UNSUPPORTED for another out_dtype, MLA_ERR_CUDA when the
+ * launch fails.
+ */
+mla_status_t mla_merge_states(const float* o_a, const float* lse_a, const float* o_b,
+                              const float* lse_b, void* out, int out_dtype, float* lse_out,
+                              int rows, void* stream);
+
+/*
  * Synchronise the device, then read and clear the plan's device error word.
  * Returns MLA_OK, MLA_ERR_DEVICE_TIMEOUT or MLA_ERR_DEVICE_BOUNDS (the first
  * error a kernel recorded since the last check), or MLA_ERR_CUDA.

@@ -15,6 +15,7 @@
 #include <vector>
 
 #include "kernels.h"
+#include "merge.h"
 #include "mla_decode.h"
 #include "planner.h"
 
@@ -507,6 +508,25 @@ mla_status_t mla_decode_run_host(mla_plan_t plan, const void* q_nope_host, const
       (e = cudaMemcpyAsync(lse_host, dr + align16(ob), lb, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
     return cuda_fail(plan, e, "device to host copy");
   if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(plan, e, "cudaStreamSynchronize");
+  return MLA_OK;
+}
+
+mla_status_t mla_merge_states(const float* o_a, const float* lse_a, const float* o_b,
+                              const float* lse_b, void* out, int out_dtype, float* lse_out,
+                              int rows, void* stream) {
+  if (rows < 0) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != MLA_DTYPE_BF16 && out_dtype != MLA_DTYPE_FP32) return MLA_ERR_UNSUPPORTED;
+  if (rows == 0) return MLA_OK;
+  if (!o_a || !lse_a || !o_b || !lse_b || !out || !lse_out) return MLA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(o_a) | reinterpret_cast<uintptr_t>(o_b) |
+       reinterpret_cast<uintptr_t>(out)) & 15)
+    return MLA_ERR_INVALID_ARG;
+  cudaError_t e = launch_merge_states(o_a, lse_a, o_b, lse_b, out, out_dtype == MLA_DTYPE_FP32,
+                                      lse_out, rows, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
   return MLA_OK;
 }
 

@@ -10,6 +10,7 @@
 #include <cuda_bf16.h>
 
 #include "kernels.h"
+#include "merge.h"
 
 namespace mla {
 namespace {
@@ -109,7 +110,77 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
   }
 }
 
+// Two attention states of the same rows over disjoint token sets (a shared
+// prefix and a request's own suffix, say) combined into one: one warp per
+// row, 16 consecutive dims per lane (four 16-byte loads from each state), the
+// whole row read before it is written, so the output may alias an input.
+constexpr int kStatesWarps = 8;
+template <bool kOutF32>
+__global__ void __launch_bounds__(32 * kStatesWarps)
+    merge_states_kernel(const float* __restrict__ o_a, const float* __restrict__ lse_a,
+                        const float* __restrict__ o_b, const float* __restrict__ lse_b, void* out,
+                        float* lse_out, int rows) {
+  const int row = blockIdx.x * kStatesWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const size_t base = static_cast<size_t>(row) * kDCkv + 16 * lane;
+  const float la = lse_a[row], lb = lse_b[row];
+  const float M = fmaxf(la, lb);
+  float wa = 0.f, wb = 0.f, lse = -INFINITY;
+  if (M != -INFINITY) {
+    wa = __expf(la - M);
+    wb = __expf(lb - M);
+    const float inv = 1.f / (wa + wb);
+    lse = M + __logf(wa + wb);
+    wa *= inv;
+    wb *= inv;
+  }
+  float4 a4[4], b4[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    a4[k] = __ldg(reinterpret_cast<const float4*>(o_a + base) + k);
+    b4[k] = __ldg(reinterpret_cast<const float4*>(o_b + base) + k);
+  }
+  float v[16];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {   // a state without weight adds nothing, even where it holds NaN
+    v[4 * k] = (wa != 0.f ? wa * a4[k].x : 0.f) + (wb != 0.f ? wb * b4[k].x : 0.f);
+    v[4 * k + 1] = (wa != 0.f ? wa * a4[k].y : 0.f) + (wb != 0.f ? wb * b4[k].y : 0.f);
+    v[4 * k + 2] = (wa != 0.f ? wa * a4[k].z : 0.f) + (wb != 0.f ? wb * b4[k].z : 0.f);
+    v[4 * k + 3] = (wa != 0.f ? wa * a4[k].w : 0.f) + (wb != 0.f ? wb * b4[k].w : 0.f);
+  }
+  __syncwarp();
+  if (kOutF32) {
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + base);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+  } else {
+    uint32_t w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+      w[k] = *reinterpret_cast<const uint32_t*>(&b2);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + base);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  }
+  if (lane == 0) lse_out[row] = lse;
+}
+
 }  // namespace
+
+cudaError_t launch_merge_states(const float* o_a, const float* lse_a, const float* o_b,
+                                const float* lse_b, void* out, bool out_f32, float* lse_out,
+                                int rows, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int grid = (rows + kStatesWarps - 1) / kStatesWarps;
+  if (out_f32)
+    merge_states_kernel<true><<<grid, 32 * kStatesWarps, 0, s>>>(o_a, lse_a, o_b, lse_b, out, lse_out, rows);
+  else
+    merge_states_kernel<false><<<grid, 32 * kStatesWarps, 0, s>>>(o_a, lse_a, o_b, lse_b, out, lse_out, rows);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge(const MergeArgs& a, bool out_f32, cudaStream_t s) {
   if (a.merge_cap <= 0) return cudaSuccess;

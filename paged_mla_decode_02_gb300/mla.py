@@ -32,7 +32,7 @@ KERNELS = {"default": KERNEL_DEFAULT, "tcgen05": KERNEL_TCGEN05, "mma_sync": KER
 EXPORTED = ("mla_plan_create", "mla_decode_plan", "mla_decode_run", "mla_decode_run_host",
             "mla_plan_check_status", "mla_plan_info", "mla_plan_destroy", "mla_status_string",
             "mla_plan_last_error", "mla_plan_partition_host", "mla_plan_set_profile_events",
-            "mla_decode_noalloc", "mla_decode_plan_multi")
+            "mla_decode_noalloc", "mla_decode_plan_multi", "mla_merge_states")
 
 
 class MLAError(RuntimeError):
@@ -79,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_decode_plan.restype = c_int
     lib.mla_decode_plan.argtypes = [_VP, _I32P, _VP, _I32P, c_int, c_int, c_int, c_int, c_int,
                                     c_float, _VP]
+    lib.mla_merge_states.restype = c_int
+    lib.mla_merge_states.argtypes = [_VP, _VP, _VP, _VP, _VP, c_int, _VP, c_int, _VP]
     lib.mla_decode_plan_multi.restype = c_int
     lib.mla_decode_plan_multi.argtypes = [_VP, _I32P, _VP, _I32P, c_int, c_int, c_int, c_int,
                                           c_int, c_int, c_float, _VP]
@@ -203,6 +205,27 @@ def mla_decode_plan_multi(plan, kv_indptr, kv_indices, kv_len, q_len: int, num_h
                                    int(head_dim_ckv), int(head_dim_kpe), int(page_size),
                                    float(sm_scale), _stream_handle(stream))
     _check(st, plan, "mla_decode_plan_multi")
+
+
+def mla_merge_states(o_a, lse_a, o_b, lse_b, out, lse_out, stream=None) -> None:
+    """Combine two attention states of the same rows over disjoint token sets
+    by log-sum-exp (see mla_decode.h).  o_a / o_b fp32 [..., 512], lse_a /
+    lse_b fp32 [...] on the device; out (bf16 or fp32) and lse_out may alias
+    the inputs."""
+    import torch
+    lib = load_library()
+    rows = int(lse_a.numel())
+    for name, t in (("o_a", o_a), ("o_b", o_b), ("out", out)):
+        if not t.is_contiguous() or t.numel() != rows * 512:
+            raise ValueError(f"{name} must be a contiguous [rows, 512] tensor")
+    for name, t in (("o_a", o_a), ("o_b", o_b), ("lse_a", lse_a), ("lse_b", lse_b), ("lse_out", lse_out)):
+        if t.dtype != torch.float32:
+            raise ValueError(f"{name} must be float32")
+    if lse_b.numel() != rows or lse_out.numel() != rows:
+        raise ValueError("lse tensors must have one entry per row")
+    st = lib.mla_merge_states(_ptr(o_a), _ptr(lse_a), _ptr(o_b), _ptr(lse_b), _ptr(out),
+                              _dtype_code(out, "out"), _ptr(lse_out), rows, _stream_handle(stream))
+    _check(st, None, "mla_merge_states")
 
 
 def mla_decode_run(plan, q_nope, q_pe, ckv_cache, kpe_cache, out, lse, kv_scale: float = 1.0,
