@@ -208,6 +208,275 @@ def run_reference(args, x) -> None:
     print(json.dumps(line), flush=True)
 
 
+CASCADE_PREFIX, CASCADE_SUFFIX, CASCADE_BATCH = 2048, 2048, 64
+
+
+def cascade_inputs():
+    """64 requests of 128 heads over 64-token pages: a 2048-token prefix that
+    every request shares, then 2048 tokens of each request's own.  Request 0
+    of the generated batch holds the prefix pages; requests 1.. hold the
+    suffixes and the queries."""
+    from paged_mla_decode_02_gb300 import inputs as I
+    return I.make_inputs("deepseek_cascade", [CASCADE_PREFIX] + [CASCADE_SUFFIX] * CASCADE_BATCH,
+                         128, 64, seed=0)
+
+
+def run_cascade(args) -> None:
+    """Two-level decode step: the shared prefix (once per request) and the own
+    suffixes as two planned batches, combined by mla_merge_states."""
+    import torch
+    from paged_mla_decode_02_gb300 import build as B
+    from paged_mla_decode_02_gb300 import mla
+    x = cascade_inputs()
+    Bq, H, P = CASCADE_BATCH, x.num_heads, x.page_size
+    torch.cuda.set_device(0)
+    B.build()
+    dev = torch.device("cuda", 0)
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    qn, qp = bf16(x.q_nope[1:]), bf16(x.q_pe[1:])
+    ckv, kpe = bf16(x.ckv), bf16(x.kpe)
+    pre_pages = x.kv_indices[x.kv_indptr[0]:x.kv_indptr[1]]
+    npre = len(pre_pages)
+    pre_idx = torch.from_numpy(np.tile(pre_pages, Bq).astype(np.int32)).to(dev)
+    suf_idx = torch.from_numpy(x.kv_indices[x.kv_indptr[1]:].astype(np.int32)).to(dev)
+    stream = torch.cuda.Stream(device=dev)
+    d_pre = mla.MLADecoder(Bq, H)
+    d_suf = mla.MLADecoder(Bq, H)
+    o0 = torch.empty((Bq, H, 512), dtype=torch.float32, device=dev)
+    o1 = torch.empty_like(o0)
+    l0 = torch.empty((Bq, H), dtype=torch.float32, device=dev)
+    l1 = torch.empty_like(l0)
+    out = torch.empty((Bq, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty_like(l0)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    with torch.cuda.stream(stream):
+        d_pre.plan(np.arange(Bq + 1, dtype=np.int32) * npre, pre_idx,
+                   np.full(Bq, CASCADE_PREFIX, np.int32), P, x.sm_scale)
+        d_suf.plan(x.kv_indptr[1:] - x.kv_indptr[1], suf_idx, x.kv_len[1:], P, x.sm_scale)
+
+    def step(q_nope, q_pe):
+        d_pre.run(q_nope, q_pe, ckv, kpe, o0, l0, stream=stream)
+        d_suf.run(q_nope, q_pe, ckv, kpe, o1, l1, stream=stream)
+        mla.mla_merge_states(o0, l0, o1, l1, out, lse, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step(qn, qp)
+    stream.synchronize()
+    d_pre.check_status()
+    d_suf.check_status()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(0)
+    with torch.cuda.stream(stream):
+        for e0, e1 in ev:
+            flush.zero_()
+            e0.record(stream)
+            step(qn, qp)
+            e1.record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    d_pre.check_status()
+    d_suf.check_status()
+    us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1000.0
+
+    # end to end: queries from pinned host memory in, output and lse back
+    qn_h, qp_h = qn.cpu().pin_memory(), qp.cpu().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    qn_d, qp_d = torch.empty_like(qn), torch.empty_like(qp)
+    e2e = []
+    for i in range(args.steps + 2):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            qn_d.copy_(qn_h, non_blocking=True)
+            qp_d.copy_(qp_h, non_blocking=True)
+            step(qn_d, qp_d)
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+        stream.synchronize()
+        if i >= 2:
+            e2e.append((time.perf_counter() - t0) * 1e6)
+
+    tok = float(CASCADE_PREFIX + Bq * CASCADE_SUFFIX)            # distinct cached tokens
+    rows = Bq * H
+    nbytes = (tok * 1152 + rows * (576 * 2 + 512 * 2 + 4)
+              + 4 * (npre + len(suf_idx)) + 8 * Bq)
+    flops = float(Bq) * (CASCADE_PREFIX + CASCADE_SUFFIX) * H * FLOP_PER_TOKEN_HEAD
+    hbm, bf, _, peak_src = peaks()
+    t_hbm, t_tc = nbytes / (hbm * 1e9) * 1e6, flops / (bf * 1e12) * 1e6
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    achieved = nbytes / (us * 1e-6) / 1e9 if bound == "hbm" else flops / (us * 1e-6) / 1e12
+    peak = hbm if bound == "hbm" else bf
+    line = {"metric": METRIC, "value": us, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": us / 1000.0, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"two-level (cascade) MLA decode: {Bq} requests, 128 heads, "
+                                   f"a {CASCADE_PREFIX}-token prefix shared by all plus "
+                                   f"{CASCADE_SUFFIX} own tokens each, page 64, bf16 cache; "
+                                   f"prefix decode + suffix decode + state merge per step",
+                       "batch": Bq, "num_heads": H, "page_size": P,
+                       "l2": "flushed between steps (256 MiB write)"},
+            "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
+                         "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": achieved / peak,
+                         "traffic": None, "peak_source": peak_src,
+                         "kernel": "whole step (two decode launches + merge)",
+                         "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                         "roofline_time_us": max(t_hbm, t_tc)},
+            "clocks": clk,
+            "e2e": {"value": statistics.mean(e2e), "unit": UNIT,
+                    "h2d_bytes_per_step": int((qn.numel() + qp.numel()) * 2),
+                    "d2h_bytes_per_step": int(out.numel() * 2 + lse.numel() * 4)},
+            "gpu_launches": 3 * args.steps}
+    if not args.no_cpu_baseline:
+        # the oracle on the concatenated pages of as many requests as fit the budget
+        from oracle import mla_oracle as O
+        t0, done = time.perf_counter(), 0
+        for b in range(Bq):
+            own = x.kv_indices[x.kv_indptr[b + 1]:x.kv_indptr[b + 2]]
+            pages = np.concatenate([pre_pages, own]).astype(np.int32)
+            O.mla_decode(x.q_nope[b + 1:b + 2], x.q_pe[b + 1:b + 2], x.ckv, x.kpe,
+                         np.array([0, len(pages)], np.int32), pages,
+                         np.array([CASCADE_PREFIX + CASCADE_SUFFIX], np.int32), P, x.sm_scale)
+            done += 1
+            if time.perf_counter() - t0 > args.cpu_budget:
+                break
+        secs = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": secs / done * Bq * 1e6, "unit": UNIT,
+                                "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{done} of {Bq} requests over their concatenated "
+                                          f"pages ({secs:.1f}s float64 numpy), scaled to the batch"}
+    print(json.dumps(line), flush=True)
+    d_pre.close()
+    d_suf.close()
+
+
+def run_absorbed(args) -> None:
+    """The absorbed decode layer: a head's no-rope query taken into the latent
+    space (mla_absorb_q), the latent decode, and its output taken back to the
+    head's value width (mla_project_out), on the deepseek decode shape with
+    qk_nope_head_dim = v_head_dim = 128 (random weights)."""
+    import torch
+    from paged_mla_decode_02_gb300 import build as B
+    from paged_mla_decode_02_gb300 import inputs as I
+    from paged_mla_decode_02_gb300 import mla
+    x = I.make_config("deepseek")
+    Bq, H, P, dn, dv = x.batch, x.num_heads, x.page_size, 128, 128
+    torch.cuda.set_device(0)
+    B.build()
+    dev = torch.device("cuda", 0)
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    g = torch.Generator(device="cpu").manual_seed(0)
+    q_raw = torch.randn((Bq, H, dn), generator=g).to(torch.bfloat16).to(dev)
+    w_uk = (torch.randn((H, 512, dn), generator=g) / math.sqrt(dn)).to(torch.bfloat16).to(dev)
+    w_uv = (torch.randn((H, 512, dv), generator=g) / math.sqrt(512)).to(torch.bfloat16).to(dev)
+    q_pe, ckv, kpe = bf16(x.q_pe), bf16(x.ckv), bf16(x.kpe)
+    idx = torch.from_numpy(x.kv_indices).to(dev)
+    q_nope = torch.empty((Bq, H, 512), dtype=torch.bfloat16, device=dev)
+    out = torch.empty((Bq, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Bq, H), dtype=torch.float32, device=dev)
+    o = torch.empty((Bq, H, dv), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    dec = mla.MLADecoder(Bq, H)
+    with torch.cuda.stream(stream):
+        dec.plan(x.kv_indptr, idx, x.kv_len, P, x.sm_scale)
+
+    def step(qr):
+        mla.mla_absorb_q(qr, w_uk, q_nope, stream=stream)
+        dec.run(q_nope, q_pe, ckv, kpe, out, lse, stream=stream)
+        mla.mla_project_out(out, w_uv, o, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            step(q_raw)
+    stream.synchronize()
+    dec.check_status()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    pa = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    clocks = ClockSampler(0)
+    with torch.cuda.stream(stream):
+        for (e0, e1), (p0, p1) in zip(ev, pa):
+            flush.zero_()
+            e0.record(stream)
+            mla.mla_absorb_q(q_raw, w_uk, q_nope, stream=stream)
+            p0.record(stream)
+            dec.run(q_nope, q_pe, ckv, kpe, out, lse, stream=stream)
+            p1.record(stream)
+            mla.mla_project_out(out, w_uv, o, stream=stream)
+            e1.record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    dec.check_status()
+    us = statistics.mean(a.elapsed_time(b) for a, b in ev) * 1000.0
+    dec_us = statistics.mean(a.elapsed_time(b) for a, b in pa) * 1000.0
+
+    qr_h = q_raw.cpu().pin_memory()
+    qr_d = torch.empty_like(q_raw)
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    e2e = []
+    for i in range(args.steps + 2):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            qr_d.copy_(qr_h, non_blocking=True)
+            step(qr_d)
+            o_h.copy_(o, non_blocking=True)
+            lse_h.copy_(lse, non_blocking=True)
+        stream.synchronize()
+        if i >= 2:
+            e2e.append((time.perf_counter() - t0) * 1e6)
+
+    dec_bytes, dec_flops = algorithmic(x)
+    rows = Bq * H
+    # the chain's own inputs and outputs: q_raw in, o out, the two weights;
+    # the latent q_nope / out between the launches are not counted
+    nbytes = (dec_bytes - rows * (512 * 2 + 512 * 2) + rows * (dn * 2 + dv * 2)
+              + H * 512 * (dn + dv) * 2)
+    flops = dec_flops + 2.0 * rows * 512 * (dn + dv)
+    hbm, bf, _, peak_src = peaks()
+    t_hbm, t_tc = nbytes / (hbm * 1e9) * 1e6, flops / (bf * 1e12) * 1e6
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    achieved = nbytes / (us * 1e-6) / 1e9 if bound == "hbm" else flops / (us * 1e-6) / 1e12
+    peak = hbm if bound == "hbm" else bf
+    line = {"metric": METRIC, "value": us, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": us / 1000.0, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"absorbed MLA decode layer on the deepseek shape: {Bq} requests "
+                                   f"x 4096 tokens, 128 heads, page 64; q_raw (dn {dn}) -> W_UK "
+                                   f"absorb -> latent decode -> W_UV projection (dv {dv})",
+                       "batch": Bq, "num_heads": H, "page_size": P,
+                       "l2": "flushed between steps (256 MiB write)"},
+            "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
+                         "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": achieved / peak,
+                         "traffic": None, "peak_source": peak_src,
+                         "kernel": "whole step (absorb + decode + project launches)",
+                         "decode_us": dec_us, "projections_us": us - dec_us,
+                         "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
+                         "roofline_time_us": max(t_hbm, t_tc)},
+            "clocks": clk,
+            "e2e": {"value": statistics.mean(e2e), "unit": UNIT,
+                    "h2d_bytes_per_step": int(qr_h.numel() * 2),
+                    "d2h_bytes_per_step": int(o_h.numel() * 2 + lse_h.numel() * 4)},
+            "gpu_launches": 3 * args.steps}
+    print(json.dumps(line), flush=True)
+    dec.close()
+
+
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -223,6 +492,20 @@ def main() -> None:
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
+    if args.config == "deepseek_absorbed":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the oracle arm is timed on the single-level configs"}))
+            return
+        run_absorbed(args)
+        return
+    if args.config == "deepseek_cascade":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable":
+                              "the oracle arm is timed on the single-level configs"}))
+            return
+        run_cascade(args)
+        return
     from paged_mla_decode_02_gb300 import inputs as I
     x = I.make_config(args.config)
     if args.impl == "reference":

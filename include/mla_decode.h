@@ -250,6 +250,33 @@ mla_status_t mla_merge_states(const float* o_a, const float* lse_a, const float*
                               int rows, void* stream);
 
 /*
+ * The per-head projections on either side of the latent decode (absorbed MLA:
+ * the decode runs in the kv_lora_rank-wide latent space of the compressed
+ * cache, head_dim_ckv = kv_lora_rank -- "[WIP] support flashinfer_mla",
+ * vLLM-metax PR #113, review of the decode_wrapper.plan parameters).
+ *
+ * mla_absorb_q: q_nope[b,h,:] = W_UK[h] . q_raw[b,h,:]
+ *   q_raw  DEVICE bf16 [batch, num_heads, head_dim_nope]  (a head's no-rope query)
+ *   w_uk   DEVICE bf16 [num_heads, 512, head_dim_nope]    (key up-projection)
+ *   q_nope DEVICE bf16 [batch, num_heads, 512]            (the decode's q_nope)
+ * mla_project_out: o[b,h,:] = out[b,h,:] . W_UV[h]
+ *   out    DEVICE bf16 [batch, num_heads, 512]            (the decode's out)
+ *   w_uv   DEVICE bf16 [num_heads, 512, head_dim_v]       (value up-projection)
+ *   o      DEVICE bf16 [batch, num_heads, head_dim_v]
+ * head_dim_nope, head_dim_v: 64 or 128 (else MLA_ERR_UNSUPPORTED).  All
+ * pointers 16-byte aligned (else MLA_ERR_INVALID_ARG).  The products
+ * accumulate in fp32 on the tensor cores and are rounded to bf16 once.  No
+ * allocation.  The work is queued on `stream`.  check_status != 0 waits for
+ * it and returns MLA_ERR_DEVICE_TIMEOUT if a device wait gave up (the error
+ * is then cleared); otherwise the call returns at once.  Calls on different
+ * streams may overlap.
+ */
+mla_status_t mla_absorb_q(const void* q_raw, const void* w_uk, void* q_nope, int batch,
+                          int num_heads, int head_dim_nope, int check_status, void* stream);
+mla_status_t mla_project_out(const void* out, const void* w_uv, void* o, int batch,
+                             int num_heads, int head_dim_v, int check_status, void* stream);
+
+/*
  * Synchronise the device, then read and clear the plan's device error word.
  * Returns MLA_OK, MLA_ERR_DEVICE_TIMEOUT or MLA_ERR_DEVICE_BOUNDS (the first
  * error a kernel recorded since the last check), or MLA_ERR_CUDA.

@@ -221,6 +221,30 @@ def lse_merge(outs, lses):
     return out, lse
 
 
+def absorb_q(q_nope_raw, W_UK):
+    """The decode's q_nope from a head's own query: per head h,
+    q_nope[b,h] = W_UK[h] @ q_raw[b,h], mapping the head's dn-wide no-rope
+    query into the 512-wide latent space of the compressed cache (so the
+    scores need no up-projection of the keys).
+
+    q_nope_raw bf16 bits [B,H,dn]; W_UK bf16 bits [H,512,dn].  Returns float64
+    [B,H,512].  Sources: the decode runs on the compressed cache of width
+    kv_lora_rank with the query's rope part kept apart (head_dim_ckv =
+    kv_lora_rank, head_dim_kpe = qk_rope_head_dim: "[WIP] support
+    flashinfer_mla", review of the decode_wrapper.plan parameters), which
+    needs the query taken into that space first.
+    """
+    return np.einsum("hnd,bhd->bhn", decode_bf16(W_UK), decode_bf16(q_nope_raw))
+
+
+def project_out(out, W_UV):
+    """A head's value output from the decode's latent output: per head h,
+    o[b,h] = out[b,h] @ W_UV[h] (512 -> dv).  out float64 [B,H,512] (or bf16
+    bits); W_UV bf16 bits [H,512,dv].  Returns float64 [B,H,dv]."""
+    o = decode_bf16(out) if np.asarray(out).dtype == np.uint16 else np.asarray(out, np.float64)
+    return np.einsum("bhn,hnv->bhv", o, decode_bf16(W_UV))
+
+
 def unabsorbed_attention(q_nope_orig, q_pe, C, R, W_UK, W_UV, sm_scale: float):
     """MLA attention in its explicit (un-absorbed) form, for pinning ``attend``.
 

@@ -16,6 +16,7 @@
 
 #include "kernels.h"
 #include "merge.h"
+#include "tmap.h"
 #include "mla_decode.h"
 #include "planner.h"
 
@@ -98,12 +99,11 @@ void release(mla_plan_t p) {
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (the library
 // does not link libcuda directly, so it loads on machines without a driver).
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn get_encode_fn() { return tensor_map_encoder(); }
 
-EncodeTiledFn get_encode_fn() {
+}  // namespace
+
+EncodeTiledFn mla::tensor_map_encoder() {
   static EncodeTiledFn fn = nullptr;
   if (!fn) {
     void* ptr = nullptr;
@@ -115,6 +115,8 @@ EncodeTiledFn get_encode_fn() {
   }
   return fn;
 }
+
+namespace {
 
 // 2-D row-major map [rows, cols] of elements of elem_bytes, box [box_rows, box_cols]
 // (box_cols * elem_bytes = 128 bytes), 128-byte swizzle.

@@ -32,7 +32,8 @@ KERNELS = {"default": KERNEL_DEFAULT, "tcgen05": KERNEL_TCGEN05, "mma_sync": KER
 EXPORTED = ("mla_plan_create", "mla_decode_plan", "mla_decode_run", "mla_decode_run_host",
             "mla_plan_check_status", "mla_plan_info", "mla_plan_destroy", "mla_status_string",
             "mla_plan_last_error", "mla_plan_partition_host", "mla_plan_set_profile_events",
-            "mla_decode_noalloc", "mla_decode_plan_multi", "mla_merge_states")
+            "mla_decode_noalloc", "mla_decode_plan_multi", "mla_merge_states",
+            "mla_absorb_q", "mla_project_out")
 
 
 class MLAError(RuntimeError):
@@ -79,6 +80,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_decode_plan.restype = c_int
     lib.mla_decode_plan.argtypes = [_VP, _I32P, _VP, _I32P, c_int, c_int, c_int, c_int, c_int,
                                     c_float, _VP]
+    lib.mla_absorb_q.restype = c_int
+    lib.mla_absorb_q.argtypes = [_VP, _VP, _VP, c_int, c_int, c_int, c_int, _VP]
+    lib.mla_project_out.restype = c_int
+    lib.mla_project_out.argtypes = [_VP, _VP, _VP, c_int, c_int, c_int, c_int, _VP]
     lib.mla_merge_states.restype = c_int
     lib.mla_merge_states.argtypes = [_VP, _VP, _VP, _VP, _VP, c_int, _VP, c_int, _VP]
     lib.mla_decode_plan_multi.restype = c_int
@@ -205,6 +210,47 @@ def mla_decode_plan_multi(plan, kv_indptr, kv_indices, kv_len, q_len: int, num_h
                                    int(head_dim_ckv), int(head_dim_kpe), int(page_size),
                                    float(sm_scale), _stream_handle(stream))
     _check(st, plan, "mla_decode_plan_multi")
+
+
+def _bf16_contig(name, t):
+    import torch
+    if t.dtype != torch.bfloat16 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous bfloat16 tensor")
+
+
+def mla_absorb_q(q_raw, w_uk, q_nope=None, check_status: bool = False, stream=None):
+    """q_nope[b,h] = W_UK[h] . q_raw[b,h]: q_raw bf16 [B,H,dn], w_uk bf16
+    [H,512,dn]; returns (or fills) q_nope bf16 [B,H,512]."""
+    import torch
+    B, H, dn = q_raw.shape
+    if q_nope is None:
+        q_nope = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q_raw.device)
+    for name, t in (("q_raw", q_raw), ("w_uk", w_uk), ("q_nope", q_nope)):
+        _bf16_contig(name, t)
+    if tuple(w_uk.shape) != (H, 512, dn) or tuple(q_nope.shape) != (B, H, 512):
+        raise ValueError("w_uk must be [H, 512, dn] and q_nope [B, H, 512]")
+    st = load_library().mla_absorb_q(_ptr(q_raw), _ptr(w_uk), _ptr(q_nope), B, H, dn,
+                                     int(bool(check_status)), _stream_handle(stream))
+    _check(st, None, "mla_absorb_q")
+    return q_nope
+
+
+def mla_project_out(out, w_uv, o=None, check_status: bool = False, stream=None):
+    """o[b,h] = out[b,h] . W_UV[h]: out bf16 [B,H,512], w_uv bf16 [H,512,dv];
+    returns (or fills) o bf16 [B,H,dv]."""
+    import torch
+    B, H, _ = out.shape
+    dv = w_uv.shape[2]
+    if o is None:
+        o = torch.empty((B, H, dv), dtype=torch.bfloat16, device=out.device)
+    for name, t in (("out", out), ("w_uv", w_uv), ("o", o)):
+        _bf16_contig(name, t)
+    if tuple(out.shape) != (B, H, 512) or tuple(w_uv.shape) != (H, 512, dv) or tuple(o.shape) != (B, H, dv):
+        raise ValueError("out must be [B, H, 512], w_uv [H, 512, dv] and o [B, H, dv]")
+    st = load_library().mla_project_out(_ptr(out), _ptr(w_uv), _ptr(o), B, H, dv,
+                                        int(bool(check_status)), _stream_handle(stream))
+    _check(st, None, "mla_project_out")
+    return o
 
 
 def mla_merge_states(o_a, lse_a, o_b, lse_b, out, lse_out, stream=None) -> None:

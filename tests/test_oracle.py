@@ -377,3 +377,47 @@ def test_multi_token_needs_the_query_tokens_in_the_cache():
     x = _multi([2, 9], 2, 16, 3)
     with pytest.raises(ValueError):
         _multi_oracle(x)
+
+
+# ---------------------------------------------------------------------------
+# the projections around the latent decode
+# ---------------------------------------------------------------------------
+
+def _bf16_bits(a):
+    return torch.from_numpy(np.asarray(a, np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_absorb_decode_project_equals_unabsorbed_attention():
+    """absorb_q -> decode -> project_out is the explicit MLA attention with
+    up-projected keys and values (on the same bf16 values)."""
+    rng = _rng(21)
+    B, H, dn, dv, P = 2, 3, 128, 128, 16
+    x = I.make_inputs("ab", [40, 23], H, P, seed=22)
+    q_raw = _bf16_bits(rng.standard_normal((B, H, dn)))
+    W_UK = _bf16_bits(rng.standard_normal((H, 512, dn)) / math.sqrt(dn))
+    W_UV = _bf16_bits(rng.standard_normal((H, 512, dv)) / math.sqrt(512))
+    q_abs = O.absorb_q(q_raw, W_UK)
+    # the decode takes bf16 queries: feed it the exact absorbed values through
+    # an fp64 attend (the decode's own rounding is tested elsewhere)
+    got = np.zeros((B, H, dv))
+    for b in range(B):
+        C = O.decode_bf16(O.gather_request(x.ckv, x.kv_indptr, x.kv_indices, b, int(x.kv_len[b]), P))
+        R = O.decode_bf16(O.gather_request(x.kpe, x.kv_indptr, x.kv_indices, b, int(x.kv_len[b]), P))
+        out, _ = O.attend(q_abs[b], O.decode_bf16(x.q_pe[b]), C, R, x.sm_scale)
+        got[b] = O.project_out(out[None], W_UV)[0]
+        ref = O.unabsorbed_attention(O.decode_bf16(q_raw[b]), O.decode_bf16(x.q_pe[b]), C, R,
+                                     O.decode_bf16(W_UK), O.decode_bf16(W_UV), x.sm_scale)
+        assert np.abs(got[b] - ref).max() < 1e-9
+
+
+def test_projections_catch_transposed_weights():
+    """Using a head's weight transposed (or another head's) changes the result."""
+    rng = _rng(23)
+    q_raw = _bf16_bits(rng.standard_normal((2, 2, 128)))
+    W = _bf16_bits(rng.standard_normal((2, 512, 128)))
+    good = O.absorb_q(q_raw, W)
+    swapped = O.absorb_q(q_raw, W[::-1].copy())
+    assert np.abs(good - swapped).max() > 1e-3
+    out = rng.standard_normal((2, 2, 512))
+    Wv = _bf16_bits(rng.standard_normal((2, 512, 128)))
+    assert np.abs(O.project_out(out, Wv) - O.project_out(out, Wv[::-1].copy())).max() > 1e-3
