@@ -11,7 +11,8 @@
 // Both are, per head, a GEMM with the batch as M:
 //   absorb:  [B x 512] = [B x dn] . W_UK[h]^T   (W_UK[h] rows are K-major)
 //   project: [B x dv]  = [B x 512] . W_UV[h]    (W_UV[h] rows are N-major)
-// One CTA per (head, 128 rows of the batch): TMA brings the head's weights and
+// Absorb runs one CTA per (head, 128 latent dims, 128 rows of the batch),
+// project one per (head, 128 rows): TMA brings the head's weights and
 // query / output rows into shared memory (128-byte swizzled panels), one
 // thread issues tcgen05 MMAs (M 128, K 16) into TMEM, four warps read the
 // fp32 accumulators back (one TMEM lane quadrant each), round to bf16 and
@@ -59,16 +60,21 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const uint32_
   for (int k = 0; k < 4; ++k) d[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
 }
 
-// q_nope[b, h, :] = W_UK[h] . q_raw[b, h, :] for the 128 rows of blockIdx.y.
-// Shared memory: A = DN / 64 panels of [128 rows x 64] (the query rows),
-// B = DN / 64 panels of [512 rows x 64] (W_UK[h], rows = latent dims).
+// Latent dims per absorb CTA: a quarter of the 512, so four CTAs share a
+// head and each holds 64 KB of shared memory (three fit on an SM).
+constexpr int kAbsorbN = 128;
+
+// q_nope[b, h, n0 .. n0 + 127] = W_UK[h][n0 ..] . q_raw[b, h, :] for the 128
+// rows of blockIdx.z, n0 = 128 blockIdx.y.  Shared memory: A = DN / 64 panels
+// of [128 rows x 64] (the query rows), B = DN / 64 panels of [128 rows x 64]
+// (W_UK[h] rows n0 .. n0 + 127).
 template <int DN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads)
     absorb_q_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_w,
                     __nv_bfloat16* __restrict__ q_nope, int batch, int heads) {
   constexpr int kP = DN / 64;
   constexpr int kA = kP * kPanel;
-  constexpr int kB = kP * 4 * kPanel;
+  constexpr int kB = kP * kPanel;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -76,7 +82,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   Tail* tail = reinterpret_cast<Tail*>(sm + kA + kB);
   const uint32_t bar_full = smem_u32(&tail->bar[0]), bar_mma = smem_u32(&tail->bar[1]);
   volatile int* abort_flag = &tail->abort;
-  const int h = blockIdx.x, m0 = blockIdx.y * kRows;
+  const int h = blockIdx.x, n0 = blockIdx.y * kAbsorbN, m0 = blockIdx.z * kRows;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     tail->abort = 0;
@@ -84,7 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_mma, 1);
     fence_barrier_init();
   }
-  if (warp == 0) tmem_alloc(smem_u32(&tail->tmem), 512);
+  if (warp == 0) tmem_alloc(smem_u32(&tail->tmem), kAbsorbN);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -96,39 +102,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(bar_full, kA + kB);
       for (int p = 0; p < kP; ++p) {
         tma_load_3d(base + p * kPanel, &map_q, 64 * p, h, m0, bar_full);
-        for (int r = 0; r < 2; ++r)   // W_UK[h] rows 256 r .. 256 r + 255
-          tma_load_2d(base + kA + p * 4 * kPanel + r * 2 * kPanel, &map_w, 64 * p, 512 * h + 256 * r,
-                      bar_full);
+        tma_load_2d(base + kA + p * kPanel, &map_w, 64 * p, 512 * h + n0, bar_full);
       }
     }
     __syncwarp();
     if (mbar_wait_warp(bar_full, 0, abort_flag)) {
       tc_fence_after();
-      constexpr uint32_t idesc = idesc_bf16_f32(kRows, 256, false, false);
+      constexpr uint32_t idesc = idesc_bf16_f32(kRows, kAbsorbN, false, false);
       const uint64_t a0 = smem_desc(base, 16, 1024, kSw128);
       const uint64_t b0 = smem_desc(base + kA, 16, 1024, kSw128);
-#pragma unroll 1
-      for (int nh = 0; nh < 2; ++nh)       // latent dims 256 nh .. 256 nh + 255
-        for (int p = 0; p < kP; ++p)
+      for (int p = 0; p < kP; ++p)
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem + 256 * nh, a0 + static_cast<uint64_t>((p * kPanel + kk * 32) >> 4),
-                   b0 + static_cast<uint64_t>((p * 4 * kPanel + nh * 2 * kPanel + kk * 32) >> 4),
-                   idesc, (p | kk) != 0, lane == 0);
+        for (int kk = 0; kk < 4; ++kk)
+          mma_ss(tmem, a0 + static_cast<uint64_t>((p * kPanel + kk * 32) >> 4),
+                 b0 + static_cast<uint64_t>((p * kPanel + kk * 32) >> 4), idesc, (p | kk) != 0,
+                 lane == 0);
       mma_commit(bar_mma, lane == 0);
       issued = true;
     } else if (lane == 0) {
       report_error(&g_proj_err, kErrTimeout);
     }
   }
-  // epilogue: row b = m0 + 32 warp + lane, 16 chunks of 32 latent dims
+  // epilogue: row b = m0 + 32 warp + lane, 4 chunks of 32 latent dims
   const bool ok = mbar_wait_warp(bar_mma, 0, abort_flag);
   tc_fence_after();
   if (ok) {
     const int b = m0 + 32 * warp + lane;
-    __nv_bfloat16* row = q_nope + (static_cast<size_t>(b) * heads + h) * kDCkv;
+    __nv_bfloat16* row = q_nope + (static_cast<size_t>(b) * heads + h) * kDCkv + n0;
 #pragma unroll 1
-    for (int c = 0; c < kDCkv / 32; ++c) {
+    for (int c = 0; c < kAbsorbN / 32; ++c) {
       uint32_t v[32];
       tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * c, v);
       tmem_ld_wait();
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, kAbsorbN);
   }
 }
 
@@ -260,13 +262,13 @@ bool encode_rows(CUtensorMap* m, const void* base, int batch, int heads, int wid
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 2-D map of the weights [heads * 512, width] bf16, box 256 rows x 64 elements.
-bool encode_weights(CUtensorMap* m, const void* base, int heads, int width) {
+// 2-D map of the weights [heads * 512, width] bf16, box box_rows x 64 elements.
+bool encode_weights(CUtensorMap* m, const void* base, int heads, int width, uint32_t box_rows) {
   EncodeTiledFn fn = tensor_map_encoder();
   if (!fn) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(width), static_cast<cuuint64_t>(heads) * 512};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(width) * 2};
-  cuuint32_t box[2] = {64, 256};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -317,15 +319,15 @@ extern "C" mla_status_t mla_absorb_q(const void* q_nope_raw, const void* w_uk, v
   if (!aligned16(q_nope_raw) || !aligned16(w_uk) || !aligned16(q_nope)) return MLA_ERR_INVALID_ARG;
   CUtensorMap mq, mw;
   if (!encode_rows(&mq, q_nope_raw, batch, num_heads, head_dim_nope) ||
-      !encode_weights(&mw, w_uk, num_heads, head_dim_nope))
+      !encode_weights(&mw, w_uk, num_heads, head_dim_nope, kAbsorbN))
     return MLA_ERR_CUDA;
-  const dim3 grid(num_heads, (batch + kRows - 1) / kRows);
+  const dim3 grid(num_heads, kDCkv / kAbsorbN, (batch + kRows - 1) / kRows);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto* dst = static_cast<__nv_bfloat16*>(q_nope);
   const cudaError_t e =
       head_dim_nope == 128
-          ? launch(absorb_q_kernel<128>, 2 * kPanel + 8 * kPanel + 1024 + 64, grid, s, mq, mw, dst, batch, num_heads)
-          : launch(absorb_q_kernel<64>, kPanel + 4 * kPanel + 1024 + 64, grid, s, mq, mw, dst, batch, num_heads);
+          ? launch(absorb_q_kernel<128>, 4 * kPanel + 1024 + 64, grid, s, mq, mw, dst, batch, num_heads)
+          : launch(absorb_q_kernel<64>, 2 * kPanel + 1024 + 64, grid, s, mq, mw, dst, batch, num_heads);
   return finish(e, check_status, s);
 }
 
@@ -337,7 +339,8 @@ extern "C" mla_status_t mla_project_out(const void* out, const void* w_uv, void*
   if (!out || !w_uv || !o) return MLA_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(w_uv) || !aligned16(o)) return MLA_ERR_INVALID_ARG;
   CUtensorMap mo, mw;
-  if (!encode_rows(&mo, out, batch, num_heads, kDCkv) || !encode_weights(&mw, w_uv, num_heads, head_dim_v))
+  if (!encode_rows(&mo, out, batch, num_heads, kDCkv) ||
+      !encode_weights(&mw, w_uv, num_heads, head_dim_v, 256))
     return MLA_ERR_CUDA;
   const dim3 grid(num_heads, (batch + kRows - 1) / kRows);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
