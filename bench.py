@@ -1,13 +1,18 @@
 """Benchmark of the paged MLA decode path on one GB300 (or N replicas).
 
-One step = one ``mla_decode_run`` (split-KV decode kernel + LSE merge kernel)
-over one batch of the workload, inputs resident in HBM.  Default workload:
-DeepSeek-V3-shaped decode, batch 64, 128 heads, kv_len 4096 per request,
-page size 64, bf16 cache, pages randomly permuted over the pool.
+One step = one ``mla_decode_run`` (the tcgen05 decode kernel, split
+requests merged inside it) over one batch of the workload, inputs resident
+in HBM.  Default workload: DeepSeek-V3-shaped decode, batch 64, 128 heads,
+kv_len 4096 per request, page size 64, bf16 cache, pages randomly permuted
+over the pool.  Other modes (``--config``): deepseek_mtp2 (two query tokens
+per request), deepseek_absorbed (W_UK absorb + decode + W_UV projection),
+deepseek_cascade (shared prefix + own suffix + state merge).
 
 Prints one JSON line.  ``value`` is microseconds per batch (device time of
-the timed steps, CUDA events on the launching stream, L2 flushed between
-steps by writing a buffer larger than L2).  ``roofline`` reports the decode
+the timed steps, CUDA events on the launching stream).  The inputs are larger
+than L2, and L2 is flushed between steps: a buffer larger than it is written,
+then another read, so the next step finds neither its inputs nor dirty lines
+in L2.  ``roofline`` reports the decode
 kernel alone (timed with events recorded by the library around it) against
 the measured HBM bandwidth; ``e2e`` is the same step through the host-buffer
 entry point with the q / out / lse copies inside the timed region;
@@ -46,7 +51,7 @@ def workload_config(x) -> dict:
                        f"page {x.page_size}, {x.kv_dtype} cache, kv_lora_rank 512, rope 64{qtok}",
            "batch": x.batch, "num_heads": x.num_heads, "page_size": x.page_size,
            "total_kv_tokens": x.total_tokens, "kv_dtype": x.kv_dtype,
-           "sm_scale": x.sm_scale, "l2": "flushed between steps (256 MiB write)"}
+           "sm_scale": x.sm_scale, "l2": L2_NOTE}
     if x.q_len > 1:
         cfg["q_len"] = x.q_len
     return cfg
@@ -79,6 +84,26 @@ def peaks() -> tuple[float, float, float, str]:
         except Exception:
             pass
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+L2_NOTE = ("inputs larger than L2, and L2 flushed between steps: 256 MiB written, then "
+           "256 MiB read, so no kernel input and no dirty line is left in it")
+
+
+class L2Flush:
+    """Between timed steps: write a 256 MiB buffer (evicting every kernel
+    input from the 129 MB L2), then read another, so the write-backs of the
+    dirty lines happen here and not inside the next timed step."""
+
+    def __init__(self, dev):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        self.r = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+
+    def zero_(self):
+        import torch
+        self.w.zero_()
+        self.r.sum(dtype=torch.int32)
 
 
 PROFILE = os.path.join(ROOT, "profiles", "decode_tc_deepseek.md")
@@ -251,7 +276,7 @@ def run_cascade(args) -> None:
     l1 = torch.empty_like(l0)
     out = torch.empty((Bq, H, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty_like(l0)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     with torch.cuda.stream(stream):
         d_pre.plan(np.arange(Bq + 1, dtype=np.int32) * npre, pre_idx,
                    np.full(Bq, CASCADE_PREFIX, np.int32), P, x.sm_scale)
@@ -327,7 +352,7 @@ def run_cascade(args) -> None:
                                    f"{CASCADE_SUFFIX} own tokens each, page 64, bf16 cache; "
                                    f"prefix decode + suffix decode + state merge per step",
                        "batch": Bq, "num_heads": H, "page_size": P,
-                       "l2": "flushed between steps (256 MiB write)"},
+                       "l2": L2_NOTE},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
                          "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": achieved / peak,
                          "traffic": None, "peak_source": peak_src,
@@ -390,7 +415,7 @@ def run_absorbed(args) -> None:
     out = torch.empty((Bq, H, 512), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((Bq, H), dtype=torch.float32, device=dev)
     o = torch.empty((Bq, H, dv), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.Stream(device=dev)
     dec = mla.MLADecoder(Bq, H)
     with torch.cuda.stream(stream):
@@ -470,7 +495,7 @@ def run_absorbed(args) -> None:
                                    f"x 4096 tokens, 128 heads, page 64; q_raw (dn {dn}) -> W_UK "
                                    f"absorb -> latent decode -> W_UV projection (dv {dv})",
                        "batch": Bq, "num_heads": H, "page_size": P,
-                       "l2": "flushed between steps (256 MiB write)"},
+                       "l2": L2_NOTE},
             "roofline": {"bound": bound, "achieved": achieved, "peak": peak,
                          "unit": "GB/s" if bound == "hbm" else "TFLOP/s", "frac": achieved / peak,
                          "traffic": None, "peak_source": peak_src,
@@ -546,7 +571,7 @@ def main() -> None:
     idx = torch.from_numpy(x.kv_indices).to(dev)
     out = torch.empty(tuple(q_nope.shape[:-1]) + (512,), dtype=torch.bfloat16, device=dev)
     lse = torch.empty(tuple(q_nope.shape[:-1]), dtype=torch.float32, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev)
 
     multi = x.q_nope.ndim == 4          # several query tokens per request
     dec = mla.MLADecoder(x.batch * x.q_len, x.num_heads, args.kernel)
