@@ -151,7 +151,12 @@ mla_status_t mla_decode_plan_multi(mla_plan_t plan, const int32_t* kv_indptr_hos
  *   q_pe      [batch, num_heads, 64]    q_dtype
  *   ckv_cache [num_pages, page_size, 512]  kv_dtype (BF16 or FP8_E4M3), 16-byte aligned
  *   kpe_cache [num_pages, page_size, 64]   kv_dtype, 16-byte aligned
- *   kv_scale  per-tensor dequantisation scale of the cache (use 1.0 for bf16)
+ *   kv_scale  per-tensor dequantisation scale of an FP8_E4M3 cache (value =
+ *             code * kv_scale), finite and > 0; ignored for a BF16 cache
+ * An FP8_E4M3 cache runs on the tcgen05 kernel with page_size 32 or 64 (each
+ * copied tile is expanded to bf16 in shared memory; every e4m3 value is exact
+ * in bf16), and on the mma.sync kernel with any page size; with the tcgen05
+ * kernel and 16-token pages the call returns MLA_ERR_UNSUPPORTED.
  *   out       [batch, num_heads, 512]   out_dtype (BF16 or FP32)
  *   lse       [batch, num_heads]        fp32, natural log
  * Launches the decode kernel; with the tcgen05 kernel that is the only launch

@@ -119,9 +119,11 @@ EncodeTiledFn mla::tensor_map_encoder() {
 namespace {
 
 // 2-D row-major map [rows, cols] of elements of elem_bytes, box [box_rows, box_cols]
-// (box_cols * elem_bytes = 128 bytes), 128-byte swizzle.
+// (box_cols * elem_bytes = 128 bytes with the 128-byte swizzle, else any
+// multiple of 16 bytes).
 bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes,
-               uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols) {
+               uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
@@ -129,7 +131,7 @@ bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int ele
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -139,16 +141,21 @@ bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int ele
 // (64, box_rows, box_panels) lands in shared memory panel by panel, each
 // panel box_rows x 128 bytes with the 128-byte swizzle -- the layout the MMA
 // reads -- in one copy instead of one per panel.
+// An e4m3 cache (one byte per element) is mapped the same way with 64-byte
+// panel rows and no swizzle: the kernel expands the bytes to the swizzled
+// bf16 layout itself.
 bool encode_panels_3d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows,
-                      uint32_t box_panels) {
+                      uint32_t box_panels, bool fp8 = false) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
+  const uint64_t eb = fp8 ? 1 : 2;
   cuuint64_t dims[3] = {64, rows, kDCkv / 64};
-  cuuint64_t strides[2] = {kDCkv * 2, 128};
+  cuuint64_t strides[2] = {kDCkv * eb, 64 * eb};
   cuuint32_t box[3] = {64, box_rows, box_panels};
   cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -158,17 +165,18 @@ bool encode_panels_3d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t 
 // The tcgen05 kernel's tensor maps for one batch (also used by the entry point
 // that works from static scratch memory).
 bool mla::encode_tc_maps(TcMaps* maps, const void* q_nope, const void* ckv_cache, const void* kpe_cache,
-                    int batch, int num_heads, int page_size, int num_pages) {
+                    int batch, int num_heads, int page_size, int num_pages, bool kv_fp8) {
   const uint64_t qrows = static_cast<uint64_t>(batch) * num_heads;
   const uint64_t kvrows = static_cast<uint64_t>(num_pages) * page_size;
+  const CUtensorMapDataType kt = kv_fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle ks = kv_fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+  const int eb = kv_fp8 ? 1 : 2;
   return encode_2d(&maps->q_nope, q_nope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qrows, kDCkv,
                    num_heads, 64) &&
-         encode_2d(&maps->ckv_k, ckv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDCkv,
-                   page_size, 64) &&
-         encode_2d(&maps->kpe_k, kpe_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDKpe,
-                   page_size, 64) &&
+         encode_2d(&maps->ckv_k, ckv_cache, kt, eb, kvrows, kDCkv, page_size, 64, ks) &&
+         encode_2d(&maps->kpe_k, kpe_cache, kt, eb, kvrows, kDKpe, page_size, 64, ks) &&
          encode_panels_3d(&maps->ckv_v, ckv_cache, kvrows, page_size >= kTcVChunkTok ? kTcVChunkTok : 16,
-                          8 / kTcCluster);
+                          8 / kTcCluster, kv_fp8);
 }
 
 extern "C" {
@@ -420,7 +428,7 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
   a.err = plan->d_err;
   a.num_pages = num_pages;
   a.num_heads = plan->num_heads;
-  a.kv_scale = kv_scale;
+  a.kv_scale = fp8 ? kv_scale : 1.f;   // the dequantisation scale of fp8 codes only
   a.units_cap = plan->units_cap;
   a.n_workers = plan->n_workers;
 
@@ -430,21 +438,14 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
   if (plan->kernel == MLA_KERNEL_MMA_SYNC) {
     e = launch_decode_mma(a, fp8, out_f32, s);
   } else {
-    if (fp8)
+    if (fp8 && plan->params.page_size < kTcVChunkTok)
       return fail(plan, MLA_ERR_UNSUPPORTED,
-                  "the tcgen05 kernel takes bf16 caches; use MLA_KERNEL_MMA_SYNC for fp8");
+                  "the tcgen05 kernel takes fp8 caches with page_size >= 32; use MLA_KERNEL_MMA_SYNC");
     TcMaps maps;
-    const int H = plan->num_heads;
-    const int P = plan->params.page_size;
-    const uint64_t qrows = static_cast<uint64_t>(plan->params.batch) * H;
-    const uint64_t kvrows = static_cast<uint64_t>(num_pages) * P;
-    if (!encode_2d(&maps.q_nope, q_nope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qrows, kDCkv, H, 64) ||
-        !encode_2d(&maps.ckv_k, ckv_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDCkv, P, 64) ||
-        !encode_2d(&maps.kpe_k, kpe_cache, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kvrows, kDKpe, P, 64) ||
-        !encode_panels_3d(&maps.ckv_v, ckv_cache, kvrows, P >= kTcVChunkTok ? kTcVChunkTok : 16,
-                          8 / kTcCluster))
+    if (!encode_tc_maps(&maps, q_nope, ckv_cache, kpe_cache, plan->params.batch, plan->num_heads,
+                        plan->params.page_size, num_pages, fp8))
       return fail(plan, MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    e = launch_decode_tc(a, maps, out_f32, s);
+    e = launch_decode_tc(a, maps, out_f32, fp8, s);
   }
   if (e != cudaSuccess) return cuda_fail(plan, e, "decode kernel launch");
   if (plan->prof_stop && (e = cudaEventRecord(plan->prof_stop, s)) != cudaSuccess)

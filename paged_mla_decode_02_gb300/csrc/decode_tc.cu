@@ -81,7 +81,7 @@ constexpr int kVPanel = kVChunkTok * 128;   // 4 KB: 32 rows x 64 dims
 constexpr int kInfoRow = 16;
 constexpr int kInfoBytes = 2 * 128 * kInfoRow;
 constexpr int kRecvBytes = 2 * kPanel + kInfoBytes;   // P (both token halves) + info
-constexpr int kBarBytes = 512;
+constexpr int kBarBytes = 640;
 constexpr uint32_t kTmemCols = 512;
 
 // Layout for clusters of C CTAs (C = 2 or 4).  CTA `rank` owns output dims
@@ -138,9 +138,10 @@ enum Bar {
   kPWritten,              // own tile: all 8 softmax warps wrote their P rows and row info
   kPRecvB0,               // 2, by P buffer: a peer's P token panel 1 has landed
   kPRecvP0 = kPRecvB0 + 2,  // 2, by P buffer: a peer's P token panel 0 has landed
-  kNumBars = kPRecvP0 + 2
+  kKReady0 = kPRecvP0 + 2,  // kMaxKSlots, by K slot (fp8 cache): panel expanded to bf16
+  kNumBars = kKReady0 + kMaxKSlots
 };
-static_assert(kNumBars * 8 + 16 <= kBarBytes, "barrier area");
+static_assert(kNumBars * 8 + 16 + 4 * kMaxVSlots <= kBarBytes, "barrier area");
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -243,7 +244,56 @@ __device__ __forceinline__ void store_out_row32(void* out, size_t orow, int d0, 
   }
 }
 
-template <bool kOutF32, int C>
+// fp8 (e4m3) caches: a copy lands as rows of 64 codes (64 bytes) in the upper
+// half of a shared-memory slot, and the producing warp expands it in place to
+// the bf16 rows of the 128-byte-swizzled panel the MMA reads (16-byte chunk c
+// of row r at chunk c ^ (r & 7)).  Each step reads its 32 rows before any lane
+// writes: a bf16 row r covers the bytes of fp8 rows 2r - 128 and 2r - 127 of
+// a 128-row panel (of the same or earlier steps), and for a V chunk bf16
+// panel p covers fp8 panels 2p - 4 and 2p - 3 (of the same or earlier panels).
+__device__ __forceinline__ void expand_row_fp8(unsigned char* dst_row, int r, const uint4 (&q)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint4 lo, hi;
+    e4m3x16_to_bf16x16(q[k], lo, hi);
+    *reinterpret_cast<uint4*>(dst_row + (((2 * k) ^ (r & 7)) << 4)) = lo;
+    *reinterpret_cast<uint4*>(dst_row + (((2 * k + 1) ^ (r & 7)) << 4)) = hi;
+  }
+}
+
+// A K panel slot: 128 rows (tokens) of 64 dims.  Warp-wide.
+__device__ __forceinline__ void expand_k_panel(unsigned char* slot, int lane) {
+#pragma unroll 1
+  for (int it = 0; it < 4; ++it) {
+    const int r = 32 * it + lane;
+    const uint4* src = reinterpret_cast<const uint4*>(slot + kPanel / 2 + 64 * r);
+    uint4 q[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) q[k] = src[k];
+    __syncwarp();
+    expand_row_fp8(slot + 128 * r, r, q);
+    __syncwarp();
+  }
+}
+
+// A V chunk slot: kPanels panels of kVChunkTok rows; rows >= rows_valid
+// (past the request's last token) become zeros.  Warp-wide.
+template <int kPanels>
+__device__ __forceinline__ void expand_v_chunk(unsigned char* slot, int lane, int rows_valid) {
+  static_assert(kVChunkTok == 32, "one row per lane");
+#pragma unroll 1
+  for (int p = 0; p < kPanels; ++p) {
+    const uint4* src = reinterpret_cast<const uint4*>(slot + kPanels * kVPanel / 2 + p * (kVPanel / 2) + 64 * lane);
+    uint4 q[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) q[k] = lane < rows_valid ? src[k] : make_uint4(0, 0, 0, 0);
+    __syncwarp();
+    expand_row_fp8(slot + p * kVPanel + 128 * lane, lane, q);
+    __syncwarp();
+  }
+}
+
+template <bool kOutF32, int C, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ TcMaps maps) {
   using L = Cfg<C>;
@@ -304,10 +354,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= K producer (own tiles) =================
     int kc = 0, g = 0, uidx = 0;
     bool ok = true;
+    // fp8 cache: panel k is expanded to bf16 once panel k + kKSlots - 1 has
+    // been issued (its slot's copy is then in flight), and every issued panel
+    // before this warp waits on anything the QK warp signals
+    int kx = 0;   // next panel to expand
+    auto expand_upto = [&](int end) {
+      for (; kx < end && ok; ++kx) {
+        const int slot = kx % L::kKSlots;
+        if (!(ok = mbar_wait_warp(bar_addr<C>(base, kKFull0 + slot), (kx / L::kKSlots) & 1, abort_flag)))
+          break;
+        expand_k_panel(sm + L::kOffK + slot * kPanel, lane);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_addr<C>(base, kKReady0 + slot));
+      }
+    };
     for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
       const WorkUnit u = a.units[ui];
-      if (uidx > 0 && !(ok = mbar_wait_warp(bar_addr<C>(base, kQEmpty), (uidx - 1) & 1, abort_flag)))
+      if (kFp8) expand_upto(kc);
+      if (uidx > 0 && ok && !(ok = mbar_wait_warp(bar_addr<C>(base, kQEmpty), (uidx - 1) & 1, abort_flag)))
         break;
+      if (!ok) break;
       if (lane == 0) mbar_arrive_expect_tx(bar_addr<C>(base, kQFull), L::kQSmemPanels * H * 128);
       __syncwarp();
       if (lane < L::kQSmemPanels)
@@ -332,18 +399,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     abort_flag)))
             break;
           const uint32_t full = bar_addr<C>(base, kKFull0 + slot);
-          if (lane == 0) mbar_arrive_expect_tx(full, nbox * P * 128);
+          constexpr int kRowBytes = kFp8 ? 64 : 128;   // one row of a panel as copied
+          if (lane == 0) mbar_arrive_expect_tx(full, nbox * P * kRowBytes);
           __syncwarp();
           if (lane < nbox) {
-            const uint32_t dst = base + L::kOffK + slot * kPanel + lane * P * 128;
+            const uint32_t dst = base + L::kOffK + slot * kPanel + (kFp8 ? kPanel / 2 : 0) + lane * P * kRowBytes;
             if (j < 8)
               tma_load_2d(dst, &maps.ckv_k, 64 * j, row, full);
             else
               tma_load_2d(dst, &maps.kpe_k, 0, row, full);
           }
+          if (kFp8) expand_upto(kc + 2 - L::kKSlots);
         }
       }
     }
+    if (kFp8) expand_upto(kc);
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
     if (lane == 0)   // drain: the copies this warp issued land before the CTA exits
       for (int k = 1; k <= L::kKSlots && k <= kc; ++k)
@@ -370,6 +440,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     int vc = 0, vslot = 0;
     uint32_t vphase = 0;   // parity of the current pass over the ring
     bool ok = true;
+    // fp8 cache: chunk k is expanded to bf16 (rows past the request's end
+    // zeroed) once chunk k + kVSlots - 1 has been issued; its valid row count
+    // waits in shared memory, one entry per slot
+    volatile int* vrows = reinterpret_cast<volatile int*>(sm + L::kOffBar + kNumBars * 8 + 16);
+    int vx = 0;   // next chunk to expand
+    auto expand_upto = [&](int end) {
+      for (; vx < end && ok; ++vx) {
+        const int slot = vx % L::kVSlots;
+        if (!(ok = mbar_wait_warp(bar_addr<C>(base, kVFull0 + slot), (vx / L::kVSlots) & 1, abort_flag)))
+          break;
+        expand_v_chunk<L::kVPanels>(sm + L::kOffV + slot * L::kVSlot, lane, vrows[slot]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_addr<C>(base, kVTail0 + slot));
+      }
+    };
     int pg_cur = u0 < u1 ? tile_pages(u0, 0) : 0;
     for (int ui = u0, i = 0; ui < u1 && ok;) {
       const WorkUnit u = a.units[ui];
@@ -397,16 +483,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vbox = P >= kVChunkTok ? kVChunkTok : 16;   // rows of the V map's box
         const int ncopy = (rows + vbox - 1) / vbox;
         const uint32_t full = bar_addr<C>(base, kVFull0 + slot);
-        const uint32_t dst = base + L::kOffV + slot * L::kVSlot;
-        if (lane == 0) mbar_arrive_expect_tx(full, ncopy * vbox * L::kVPanels * 128);
+        constexpr int kRowBytes = kFp8 ? 64 : 128;   // one row of a panel as copied
+        const uint32_t dst = base + L::kOffV + slot * L::kVSlot + (kFp8 ? L::kVSlot / 2 : 0);
+        if (lane == 0) {
+          if (kFp8) vrows[slot] = rows;
+          mbar_arrive_expect_tx(full, ncopy * vbox * L::kVPanels * kRowBytes);
+        }
         __syncwarp();
         // lane c < ncopy issues copy c (lanes past it mirror the last one for the shuffle)
         const int tb = t + vbox * min(lane, ncopy - 1);
         const int page = __shfl_sync(0xffffffffu, pg_cur, (tb - tok0) / P);
         if (lane < ncopy)
-          tma_load_3d(dst + lane * vbox * L::kVPanels * 128, &maps.ckv_v, 0, page * P + (tb % P),
+          tma_load_3d(dst + lane * vbox * L::kVPanels * kRowBytes, &maps.ckv_v, 0, page * P + (tb % P),
                       L::kVPanels * rank, full);
-        if (rows < kVChunkTok) {
+        if (kFp8) {
+          expand_upto(vc + 2 - L::kVSlots);
+        } else if (rows < kVChunkTok) {
           // Last chunk of a request: rows past kv_len may hold anything (even
           // NaN), and P = 0 there does not cancel NaN.  Wait for the copy,
           // zero those rows, then release the chunk through kVTail.
@@ -429,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ui = ui2;
       i = i2;
     }
+    if (kFp8) expand_upto(vc);
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
     if (lane == 0)
       for (int k = 1; k <= L::kVSlots && k <= vc; ++k)
@@ -462,7 +555,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             kslot = 0;
             kphase ^= 1;
           }
-          if (!(ok = mbar_wait_warp(bar_addr<C>(base, kKFull0 + slot), ph, abort_flag))) break;
+          // bf16: the copy has landed; fp8: the K producer expanded it
+          if (!(ok = mbar_wait_warp(bar_addr<C>(base, (kFp8 ? kKReady0 : kKFull0) + slot), ph, abort_flag)))
+            break;
           const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((slot * kPanel) >> 4);
           if (j < L::kQSmemPanels) {
             const uint64_t adesc = q_desc0 + static_cast<uint64_t>((j * kPanel) >> 4);
@@ -553,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             vslot = 0;
             vphase ^= 1;
           }
-          if (c == nch - 1 && (valid % kVChunkTok) != 0) {
+          if (kFp8 || (c == nch - 1 && (valid % kVChunkTok) != 0)) {
             if (!(ok = mbar_wait_warp(bar_addr<C>(base, kVTail0 + slot), (tail_par >> slot) & 1,
                                       abort_flag)))
               break;
@@ -596,7 +691,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int hc = (warp - 3) >> 2;                 // token half / P panel / O column half
     const int r = quad * 32 + lane;                 // head row == TMEM lane
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const float c = prm.sm_scale * kLog2e;
+    // scores on the stored cache values: kv_scale folds the fp8 dequantisation
+    // in (1 for a bf16 cache); the epilogue multiplies O by it too
+    const float c = prm.sm_scale * a.kv_scale * kLog2e;
     const float pad = c >= 0.f ? -INFINITY : INFINITY;   // neutral for the max of s * c
     // P of tile g lives in buffer g & 1 in both CTAs; this row's chunk area:
     const uint32_t p_off = hc * kPanel + (r >> 3) * 1024 + (r & 7) * 128;
@@ -1046,12 +1143,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // The launched kernel: clusters of kTcCluster CTAs.
-template <bool kOutF32>
+template <bool kOutF32, bool kFp8>
 cudaError_t set_attributes() {
   using L = Cfg<kTcCluster>;
   static bool attr_set = false;   // set once, before any stream capture
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<kOutF32, kTcCluster>,
+    cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<kOutF32, kTcCluster, kFp8>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
@@ -1073,34 +1170,38 @@ cudaLaunchConfig_t cluster_config(int clusters, cudaLaunchAttribute* attr) {
   return cfg;
 }
 
-template <bool kOutF32>
+template <bool kOutF32, bool kFp8>
 cudaError_t launch_impl(const DecodeArgs& a, const TcMaps& maps, cudaStream_t s) {
-  cudaError_t e = set_attributes<kOutF32>();
+  cudaError_t e = set_attributes<kOutF32, kFp8>();
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(a.n_workers, attr);
   cfg.stream = s;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<kOutF32, kTcCluster>, a, maps);
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<kOutF32, kTcCluster, kFp8>, a, maps);
 }
 
 }  // namespace
 
 cudaError_t decode_tc_max_workers(int* workers) {
   *workers = 0;
-  cudaError_t e = set_attributes<true>();
-  if (e == cudaSuccess) e = set_attributes<false>();
+  cudaError_t e = set_attributes<true, false>();
+  if (e == cudaSuccess) e = set_attributes<false, false>();
+  if (e == cudaSuccess) e = set_attributes<true, true>();
+  if (e == cudaSuccess) e = set_attributes<false, true>();
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = cluster_config(1, attr);
   int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, decode_tc_kernel<false, kTcCluster>, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&clusters, decode_tc_kernel<false, kTcCluster, false>, &cfg);
   if (e != cudaSuccess) return e;
   *workers = clusters;
   return cudaSuccess;
 }
 
-cudaError_t launch_decode_tc(const DecodeArgs& a, const TcMaps& maps, bool out_f32, cudaStream_t s) {
-  return out_f32 ? launch_impl<true>(a, maps, s) : launch_impl<false>(a, maps, s);
+cudaError_t launch_decode_tc(const DecodeArgs& a, const TcMaps& maps, bool out_f32, bool kv_fp8,
+                             cudaStream_t s) {
+  if (kv_fp8) return out_f32 ? launch_impl<true, true>(a, maps, s) : launch_impl<false, true>(a, maps, s);
+  return out_f32 ? launch_impl<true, false>(a, maps, s) : launch_impl<false, false>(a, maps, s);
 }
 
 }  // namespace mla

@@ -70,16 +70,18 @@ constexpr int kTcCluster = 2;
 constexpr int kTcVChunkTok = 32;
 struct TcMaps {
   CUtensorMap q_nope;   // [B*H, 512] bf16, box 64 x H
-  CUtensorMap ckv_k;    // [pages*P, 512] bf16, box 64 x P (one page of a K panel)
-  CUtensorMap kpe_k;    // [pages*P, 64] bf16, box 64 x P
+  CUtensorMap ckv_k;    // [pages*P, 512] bf16 (fp8), box 64 x P (one page of a K panel)
+  CUtensorMap kpe_k;    // [pages*P, 64] bf16 (fp8), box 64 x P
   CUtensorMap ckv_v;    // (64, pages*P, 8 panels) view of ckv, box 64 x min(P, 32) x 4 panels
 };
-cudaError_t launch_decode_tc(const DecodeArgs& a, const TcMaps& maps, bool out_f32,
+// kv_fp8: e4m3 cache (maps of bytes without swizzle, page_size >= 32); the
+// kernel expands each copy to bf16 in shared memory and scales by kv_scale.
+cudaError_t launch_decode_tc(const DecodeArgs& a, const TcMaps& maps, bool out_f32, bool kv_fp8,
                              cudaStream_t s);
 // Host: the tensor maps launch_decode_tc takes, for one batch (false when the
 // driver's encoder is unavailable or rejects an argument).
 bool encode_tc_maps(TcMaps* maps, const void* q_nope, const void* ckv_cache, const void* kpe_cache,
-                    int batch, int num_heads, int page_size, int num_pages);
+                    int batch, int num_heads, int page_size, int num_pages, bool kv_fp8 = false);
 // Clusters of two CTAs of the tcgen05 kernel that can be resident at once
 // (the persistent grid uses at most that many workers).
 cudaError_t decode_tc_max_workers(int* workers);

@@ -162,10 +162,10 @@ extern "C" mla_status_t mla_decode_noalloc(
   a.err = reinterpret_cast<int32_t*>(sc + off_err);
   a.num_pages = num_pages;
   a.num_heads = num_heads;
-  a.kv_scale = kv_scale;
+  a.kv_scale = 1.f;   // a bf16 cache: no dequantisation scale
   a.units_cap = n_units;
   a.n_workers = su.n_workers;
-  if ((e = launch_decode_tc(a, maps, out_dtype == MLA_DTYPE_FP32, s)) != cudaSuccess) {
+  if ((e = launch_decode_tc(a, maps, out_dtype == MLA_DTYPE_FP32, false, s)) != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;
   }

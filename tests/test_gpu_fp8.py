@@ -1,0 +1,64 @@
+"""fp8 (e4m3) caches on both kernels against the oracle on the dequantised
+values: the tcgen05 kernel expands each copied tile to bf16 in shared memory
+(every e4m3 value is exact in bf16) and folds kv_scale into the scores and
+the output; the mma.sync kernel converts while staging."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_helpers import assert_parity, run_decode, to_device
+from oracle import mla_oracle as O
+from paged_mla_decode_02_gb300 import inputs as I
+from paged_mla_decode_02_gb300 import mla
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = ["tcgen05", "mma_sync"]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("lens, heads, P, scale", [
+    ([1, 31, 32, 33, 200], 16, 32, 1.0),     # ragged tails inside a V chunk and a page
+    ([129, 4000, 64], 128, 64, 0.5),         # split request, a power-of-two scale
+    ([700, 2, 1500], 64, 64, 0.37),          # a scale that is not a power of two
+])
+def test_fp8_cache_matches_oracle(kernel, lens, heads, P, scale):
+    x = I.make_inputs("f8", lens, heads, P, seed=19, kv_dtype="fp8_e4m3", kv_scale=scale,
+                      poison=True, slack_pages=2)
+    d = to_device(x)
+    out, lse = run_decode(x, d, kernel, torch.float32)
+    ref_out, ref_lse = O.mla_decode_inputs(x)
+    assert_parity(out, lse, ref_out, ref_lse, f"fp8 {kernel} {lens} P={P} scale={scale}")
+
+
+def test_fp8_tcgen05_matches_bf16_cache_of_the_same_values():
+    """An fp8 cache and the bf16 cache holding the same (exact) values give the
+    same result up to summation order on the tcgen05 kernel."""
+    x = I.make_inputs("f8b", [300, 1000, 77], 128, 64, seed=23, kv_dtype="fp8_e4m3")
+    d = to_device(x)
+    o8, l8 = run_decode(x, d, "tcgen05", torch.float32)
+    d16 = dict(d, ckv=d["ckv"].to(torch.bfloat16), kpe=d["kpe"].to(torch.bfloat16))
+    x16 = I.MLAInputs(**{**x.__dict__, "kv_dtype": "bf16"})
+    o16, l16 = run_decode(x16, d16, "tcgen05", torch.float32)
+    assert np.abs(o8 - o16).max() < 1e-4 and np.abs(l8 - l16).max() < 1e-4
+
+
+def test_fp8_tcgen05_rejects_16_token_pages():
+    x = I.make_inputs("f8p16", [40, 9], 16, 16, seed=2, kv_dtype="fp8_e4m3")
+    d = to_device(x)
+    with pytest.raises(mla.MLAError) as ei:
+        run_decode(x, d, "tcgen05", torch.float32)
+    assert ei.value.status == mla.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_kv_scale_is_ignored_for_bf16_caches(kernel):
+    """kv_scale dequantises fp8 codes; a bf16 cache holds its values as they are."""
+    x = I.make_inputs("s16", [90, 500], 32, 32, seed=29)
+    d = to_device(x)
+    o1, l1 = run_decode(x, d, kernel, torch.float32)
+    x2 = I.MLAInputs(**{**x.__dict__, "kv_scale": 3.0})
+    o2, l2 = run_decode(x2, d, kernel, torch.float32)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)

@@ -252,8 +252,6 @@ def _sample(x, k, seed=0):
 @pytest.mark.parametrize("cfg", ["deepseek", "ragged", "long_b1", "long_b4", "fp8"])
 def test_full_size_config_sampled(kernel, cfg):
     x = _config(cfg)
-    if cfg == "fp8" and kernel == "tcgen05":
-        pytest.skip("fp8 caches run on the mma.sync kernel")
     d = to_device(x)
     out, lse = run_decode(x, d, kernel, torch.float32)
     reqs = _sample(x, 3 if x.batch > 8 else x.batch)
