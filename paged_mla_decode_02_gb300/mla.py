@@ -274,14 +274,36 @@ def mla_merge_states(o_a, lse_a, o_b, lse_b, out, lse_out, stream=None) -> None:
     _check(st, None, "mla_merge_states")
 
 
+def _check_layouts(q_nope, q_pe, ckv_cache, kpe_cache, out, lse, page_size=None) -> None:
+    """The shapes mla_decode.h documents, checked before the library reads
+    through the raw pointers: the cache [pages, page_size, 512] and [pages,
+    page_size, 64] of one dtype, q [..., 512] / [..., 64], out [..., 512] and
+    lse [...] over the same leading dims."""
+    if ckv_cache.dim() != 3 or ckv_cache.shape[2] != 512:
+        raise ValueError(f"ckv_cache must be [num_pages, page_size, 512], got {tuple(ckv_cache.shape)}")
+    if tuple(kpe_cache.shape) != (ckv_cache.shape[0], ckv_cache.shape[1], 64):
+        raise ValueError(f"kpe_cache must be [num_pages, page_size, 64] like ckv_cache, "
+                         f"got {tuple(kpe_cache.shape)}")
+    if kpe_cache.dtype != ckv_cache.dtype:
+        raise ValueError("ckv_cache and kpe_cache must have the same dtype")
+    if page_size is not None and ckv_cache.shape[1] != page_size:
+        raise ValueError(f"the cache holds pages of {ckv_cache.shape[1]} tokens, the plan {page_size}")
+    lead = tuple(q_nope.shape[:-1])
+    if q_nope.shape[-1] != 512 or tuple(q_pe.shape) != lead + (64,):
+        raise ValueError("q_nope must be [..., 512] and q_pe [..., 64] over the same leading dims")
+    if tuple(out.shape) != lead + (512,) or tuple(lse.shape) != lead:
+        raise ValueError("out must be [..., 512] and lse [...] over q_nope's leading dims")
+
+
 def mla_decode_run(plan, q_nope, q_pe, ckv_cache, kpe_cache, out, lse, kv_scale: float = 1.0,
-                   stream=None) -> None:
+                   stream=None, page_size=None) -> None:
     """Run the planned batch on device tensors (see mla_decode.h for layouts)."""
     lib = load_library()
     for name, t in (("q_nope", q_nope), ("q_pe", q_pe), ("ckv_cache", ckv_cache),
                     ("kpe_cache", kpe_cache), ("out", out), ("lse", lse)):
         if not t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    _check_layouts(q_nope, q_pe, ckv_cache, kpe_cache, out, lse, page_size)
     num_pages = int(ckv_cache.shape[0])
     st = lib.mla_decode_run(plan, _ptr(q_nope), _ptr(q_pe), _dtype_code(q_nope, "q_nope"),
                             _ptr(ckv_cache), _ptr(kpe_cache), _dtype_code(ckv_cache, "ckv_cache"),
@@ -308,6 +330,7 @@ def mla_decode_noalloc(kv_indptr, kv_indices, kv_len, page_size: int, sm_scale: 
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
     if _dtype_code(q_nope, "q_nope") != DTYPE_BF16 or _dtype_code(ckv_cache, "ckv_cache") != DTYPE_BF16:
         raise ValueError("mla_decode_noalloc takes bf16 queries and caches")
+    _check_layouts(q_nope, q_pe, ckv_cache, kpe_cache, out, lse, int(page_size))
     idx_ptr = _ptr(kv_indices) if kv_indices is not None and kv_indices.numel() > 0 else None
     st = lib.mla_decode_noalloc(indptr.ctypes.data_as(_I32P), idx_ptr, lens.ctypes.data_as(_I32P),
                                 batch, int(q_nope.shape[1]), int(page_size), float(sm_scale),
@@ -326,6 +349,9 @@ def mla_decode_run_host(plan, q_nope_host, q_pe_host, ckv_cache, kpe_cache, out_
                     ("lse", lse_host)):
         if t.is_cuda or not t.is_contiguous():
             raise ValueError(f"{name} must be a contiguous host tensor")
+    if not ckv_cache.is_cuda or not kpe_cache.is_cuda:
+        raise ValueError("the cache must be on the device")
+    _check_layouts(q_nope_host, q_pe_host, ckv_cache, kpe_cache, out_host, lse_host)
     st = lib.mla_decode_run_host(plan, _ptr(q_nope_host), _ptr(q_pe_host),
                                  _dtype_code(q_nope_host, "q_nope"), _ptr(ckv_cache),
                                  _ptr(kpe_cache), _dtype_code(ckv_cache, "ckv_cache"),
@@ -390,6 +416,7 @@ class MLADecoder:
         self.num_heads = int(num_heads)
         self.handle = mla_plan_create(max_batch, num_heads, kernel)
         self._kv_indices = None
+        self.page_size = None
 
     def plan(self, kv_indptr, kv_indices, kv_len, page_size: int, sm_scale: float,
              head_dim_ckv: int = 512, head_dim_kpe: int = 64, stream=None, q_len: int = 0) -> None:
@@ -403,6 +430,7 @@ class MLADecoder:
             mla_decode_plan(self.handle, kv_indptr, kv_indices, kv_len, self.num_heads,
                             head_dim_ckv, head_dim_kpe, page_size, sm_scale, stream)
         self.q_len = int(q_len)
+        self.page_size = int(page_size)
         self._kv_indices = kv_indices     # keep the borrowed page table alive
 
     def run(self, q_nope, q_pe, ckv_cache, kpe_cache, out=None, lse=None,
@@ -413,7 +441,8 @@ class MLADecoder:
             out = torch.empty(lead + (512,), dtype=out_dtype or torch.bfloat16, device=q_nope.device)
         if lse is None:
             lse = torch.empty(lead, dtype=torch.float32, device=q_nope.device)
-        mla_decode_run(self.handle, q_nope, q_pe, ckv_cache, kpe_cache, out, lse, kv_scale, stream)
+        mla_decode_run(self.handle, q_nope, q_pe, ckv_cache, kpe_cache, out, lse, kv_scale, stream,
+                       page_size=self.page_size)
         return out, lse
 
     def info(self) -> dict:

@@ -62,3 +62,19 @@ def test_kv_scale_is_ignored_for_bf16_caches(kernel):
     x2 = I.MLAInputs(**{**x.__dict__, "kv_scale": 3.0})
     o2, l2 = run_decode(x2, d, kernel, torch.float32)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_cache_of_the_wrong_width_is_rejected_before_any_launch():
+    """fp8 codes reinterpreted as bf16 (rows half as wide as the layout says)
+    would make the kernel read past the buffer: the binding refuses them."""
+    x = I.make_inputs("f8w", [100, 30], 16, 32, seed=3, kv_dtype="fp8_e4m3")
+    d = to_device(x)
+    as_bf16 = d["ckv"].view(torch.uint8).view(torch.bfloat16)       # [pages, P, 256]
+    kpe16 = d["kpe"].view(torch.uint8).view(torch.bfloat16)         # [pages, P, 32]
+    dec = mla.MLADecoder(x.batch, x.num_heads, "tcgen05")
+    try:
+        dec.plan(x.kv_indptr, d["kv_indices"], x.kv_len, x.page_size, x.sm_scale)
+        with pytest.raises(ValueError):
+            dec.run(d["q_nope"], d["q_pe"], as_bf16, kpe16)
+    finally:
+        dec.close()
