@@ -354,12 +354,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= K producer (own tiles) =================
     int kc = 0, g = 0, uidx = 0;
     bool ok = true;
-    // fp8 cache: panel k is expanded to bf16 once panel k + kKSlots - 1 has
-    // been issued (its slot's copy is then in flight), and every issued panel
-    // before this warp waits on anything the QK warp signals
+    // fp8 cache: the even panels of a tile (j = 0, 2, .., 8) are expanded to
+    // bf16 here, panel k once panel k + kKSlots - 1 has been issued, and every
+    // issued one before this warp waits on anything the QK warp signals; the
+    // QK warp expands the odd panels itself
     int kx = 0;   // next panel to expand
     auto expand_upto = [&](int end) {
       for (; kx < end && ok; ++kx) {
+        if ((kx % 9) & 1) continue;
         const int slot = kx % L::kKSlots;
         if (!(ok = mbar_wait_warp(bar_addr<C>(base, kKFull0 + slot), (kx / L::kKSlots) & 1, abort_flag)))
           break;
@@ -440,17 +442,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     int vc = 0, vslot = 0;
     uint32_t vphase = 0;   // parity of the current pass over the ring
     bool ok = true;
-    // fp8 cache: chunk k is expanded to bf16 (rows past the request's end
-    // zeroed) once chunk k + kVSlots - 1 has been issued; its valid row count
-    // waits in shared memory, one entry per slot
+    // fp8 cache: the even chunks of a tile are expanded to bf16 here (rows
+    // past the request's end zeroed), chunk k once chunk k + kVSlots - 1 has
+    // been issued; the PV warp expands the odd ones.  A chunk's valid row
+    // count (and bit 16: odd in its tile) waits in shared memory, one entry
+    // per slot.
     volatile int* vrows = reinterpret_cast<volatile int*>(sm + L::kOffBar + kNumBars * 8 + 16);
     int vx = 0;   // next chunk to expand
     auto expand_upto = [&](int end) {
       for (; vx < end && ok; ++vx) {
         const int slot = vx % L::kVSlots;
+        const int info = vrows[slot];
+        if (info >> 16) continue;
         if (!(ok = mbar_wait_warp(bar_addr<C>(base, kVFull0 + slot), (vx / L::kVSlots) & 1, abort_flag)))
           break;
-        expand_v_chunk<L::kVPanels>(sm + L::kOffV + slot * L::kVSlot, lane, vrows[slot]);
+        expand_v_chunk<L::kVPanels>(sm + L::kOffV + slot * L::kVSlot, lane, info);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_addr<C>(base, kVTail0 + slot));
@@ -486,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kRowBytes = kFp8 ? 64 : 128;   // one row of a panel as copied
         const uint32_t dst = base + L::kOffV + slot * L::kVSlot + (kFp8 ? L::kVSlot / 2 : 0);
         if (lane == 0) {
-          if (kFp8) vrows[slot] = rows;
+          if (kFp8) vrows[slot] = rows | ((((t - tok0) / kVChunkTok) & 1) << 16);
           mbar_arrive_expect_tx(full, ncopy * vbox * L::kVPanels * kRowBytes);
         }
         __syncwarp();
@@ -535,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t k_desc0 = smem_desc(base + L::kOffK, 16, 1024, kSw128);
     int g = 0, gl = 0, uidx = 0, kslot = 0;
     uint32_t kphase = 0;
+    uint32_t ready_par = 0;   // fp8: per K slot, parity of its next kKReady phase
     bool ok = true;
     for (int ui = u0; ui < u1 && ok; ++ui, ++uidx) {
       const WorkUnit u = a.units[ui];
@@ -555,9 +562,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             kslot = 0;
             kphase ^= 1;
           }
-          // bf16: the copy has landed; fp8: the K producer expanded it
-          if (!(ok = mbar_wait_warp(bar_addr<C>(base, (kFp8 ? kKReady0 : kKFull0) + slot), ph, abort_flag)))
+          if (kFp8 && (j & 1)) {
+            // fp8, odd panel: expanded here once its copy has landed
+            if (!(ok = mbar_wait_warp(bar_addr<C>(base, kKFull0 + slot), ph, abort_flag))) break;
+            expand_k_panel(sm + L::kOffK + slot * kPanel, lane);
+            fence_proxy_async_smem();
+            __syncwarp();
+          } else if (kFp8) {
+            // fp8, even panel: the K producer expanded it (kKReady counts even panels only)
+            if (!(ok = mbar_wait_warp(bar_addr<C>(base, kKReady0 + slot), (ready_par >> slot) & 1, abort_flag)))
+              break;
+            ready_par ^= 1u << slot;
+          } else if (!(ok = mbar_wait_warp(bar_addr<C>(base, kKFull0 + slot), ph, abort_flag))) {
             break;
+          }
           const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((slot * kPanel) >> 4);
           if (j < L::kQSmemPanels) {
             const uint64_t adesc = q_desc0 + static_cast<uint64_t>((j * kPanel) >> 4);
@@ -648,7 +666,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             vslot = 0;
             vphase ^= 1;
           }
-          if (kFp8 || (c == nch - 1 && (valid % kVChunkTok) != 0)) {
+          if (kFp8 && (c & 1)) {
+            // fp8, odd chunk of the tile: expanded here once its copy has landed
+            if (!(ok = mbar_wait_warp(bar_addr<C>(base, kVFull0 + slot), ph, abort_flag))) break;
+            expand_v_chunk<L::kVPanels>(sm + L::kOffV + slot * L::kVSlot, lane,
+                                        min(kVChunkTok, valid - kVChunkTok * c));
+            fence_proxy_async_smem();
+            __syncwarp();
+          } else if (kFp8 || (c == nch - 1 && (valid % kVChunkTok) != 0)) {
             if (!(ok = mbar_wait_warp(bar_addr<C>(base, kVTail0 + slot), (tail_par >> slot) & 1,
                                       abort_flag)))
               break;

@@ -78,3 +78,24 @@ def test_cache_of_the_wrong_width_is_rejected_before_any_launch():
             dec.run(d["q_nope"], d["q_pe"], as_bf16, kpe16)
     finally:
         dec.close()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_every_finite_fp8_code_converts_exactly(kernel):
+    """Requests of one token: the output is that token's ckv row itself
+    (softmax of one score is 1), so it must equal the stored values exactly.
+    The row holds every finite e4m3 code, subnormals included; the scores
+    (lse) come from the same converted values."""
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)   # 254 codes
+    row = np.concatenate([finite, finite[::-1], np.zeros(4, np.uint8)])               # 512
+    rng = np.random.Generator(np.random.PCG64(5))
+    x = I.make_inputs("codes", [1, 1, 1, 1], 16, 32, seed=31, kv_dtype="fp8_e4m3")
+    for b in range(x.batch):
+        page = x.kv_indices[x.kv_indptr[b]]
+        x.ckv[page, 0, :] = np.roll(row, 37 * b)
+        x.kpe[page, 0, :] = rng.choice(finite, size=64)
+    d = to_device(x)
+    out, lse = run_decode(x, d, kernel, torch.float32)
+    ref_out, ref_lse = O.mla_decode_inputs(x)
+    assert np.array_equal(out, ref_out), "a converted code differs from its e4m3 value"
+    assert np.abs(lse - ref_lse).max() < 1e-3
