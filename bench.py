@@ -208,6 +208,19 @@ def dist_env():
     return world, rank, local
 
 
+def job_us_per_batch(total_ms: float, steps: int, world: int, device=None) -> float:
+    """Whole-job microseconds per batch for N replicas: each rank ran one
+    batch per step, so the job did steps x world batches in the time of the
+    slowest rank (max over ranks of its total)."""
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms * 1000.0 / steps / world
+
+
 def run_reference(args, x) -> None:
     """Oracle-only arm: each step is a bounded sample of the batch on host cores."""
     world, rank, _ = dist_env()
@@ -629,12 +642,7 @@ def main() -> None:
 
     step_ms = [a.elapsed_time(b) for a, b in zip(s0, s1)]
     kern_ms = [a.elapsed_time(b) for a, b in zip(k0, k1)]
-    dev_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([dev_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dev_ms = float(t.item())
-    us_per_batch = dev_ms * 1000.0 / args.steps / world
+    us_per_batch = job_us_per_batch(sum(step_ms), args.steps, world, dev)
 
     # end to end through the host-buffer entry point (q in, out / lse back)
     qn_h = q_nope.cpu().pin_memory()
@@ -650,7 +658,7 @@ def main() -> None:
         t0 = time.perf_counter()
         mla.mla_decode_run_host(dec.handle, qn_h, qp_h, ckv, kpe, out_h, lse_h, x.kv_scale, stream)
         e2e.append((time.perf_counter() - t0) * 1e6)
-    e2e_us = statistics.mean(e2e)
+    e2e_us = job_us_per_batch(sum(e2e) / 1000.0, args.steps, world, dev)
 
     nbytes, flops = algorithmic(x)
     hbm, bf, bfs, peak_src = peaks()
