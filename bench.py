@@ -103,7 +103,7 @@ class L2Flush:
     def zero_(self):
         import torch
         self.w.zero_()
-        self.r.view(torch.int32).sum()   # the read pass: int32 words, no widened copy
+        self.r.view(torch.float32).sum()   # the read pass, reduced as fp32 words: no widened copy
 
 
 PROFILE = os.path.join(ROOT, "profiles", "decode_tc_deepseek.md")

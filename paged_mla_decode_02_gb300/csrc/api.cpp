@@ -119,8 +119,8 @@ EncodeTiledFn mla::tensor_map_encoder() {
 namespace {
 
 // 2-D row-major map [rows, cols] of elements of elem_bytes, box [box_rows, box_cols]
-// (box_cols * elem_bytes = 128 bytes with the 128-byte swizzle, else any
-// multiple of 16 bytes).
+// (box_cols * elem_bytes = 128 bytes with the 128-byte swizzle, 64 with the
+// 64-byte one).
 bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem_bytes,
                uint64_t rows, uint64_t cols, uint32_t box_rows, uint32_t box_cols,
                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
@@ -142,7 +142,9 @@ bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int ele
 // panel box_rows x 128 bytes with the 128-byte swizzle -- the layout the MMA
 // reads -- in one copy instead of one per panel.
 // An e4m3 cache (one byte per element) is mapped the same way with 64-byte
-// panel rows and no swizzle: the kernel expands the bytes to the swizzled
+// panel rows and the 64-byte swizzle (16-byte chunk c of row r lands at
+// chunk c ^ ((r >> 1) & 3), so the kernel's row-per-lane reads are free of
+// bank conflicts); the kernel expands the bytes to the 128-byte-swizzled
 // bf16 layout itself.
 bool encode_panels_3d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows,
                       uint32_t box_panels, bool fp8 = false) {
@@ -155,7 +157,7 @@ bool encode_panels_3d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t 
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                  fp8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -169,7 +171,7 @@ bool mla::encode_tc_maps(TcMaps* maps, const void* q_nope, const void* ckv_cache
   const uint64_t qrows = static_cast<uint64_t>(batch) * num_heads;
   const uint64_t kvrows = static_cast<uint64_t>(num_pages) * page_size;
   const CUtensorMapDataType kt = kv_fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const CUtensorMapSwizzle ks = kv_fp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapSwizzle ks = kv_fp8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
   const int eb = kv_fp8 ? 1 : 2;
   return encode_2d(&maps->q_nope, q_nope, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, qrows, kDCkv,
                    num_heads, 64) &&

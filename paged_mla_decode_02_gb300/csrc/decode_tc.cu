@@ -245,9 +245,12 @@ __device__ __forceinline__ void store_out_row32(void* out, size_t orow, int d0, 
 }
 
 // fp8 (e4m3) caches: a copy lands as rows of 64 codes (64 bytes) in the upper
-// half of a shared-memory slot, and the producing warp expands it in place to
-// the bf16 rows of the 128-byte-swizzled panel the MMA reads (16-byte chunk c
-// of row r at chunk c ^ (r & 7)).  Each step reads its 32 rows before any lane
+// half of a shared-memory slot, 64-byte swizzled (16-byte chunk c of row r at
+// chunk c ^ ((r >> 1) & 3), every destination 512-byte aligned), and a warp
+// expands it in place to the bf16 rows of the 128-byte-swizzled panel the
+// MMA reads (chunk c of row r at chunk c ^ (r & 7)).  One lane per row: the
+// 64-byte swizzle puts the 8 rows of each 8-lane phase on distinct banks
+// for the reads, and the 128-byte one for the writes.  Each step reads its 32 rows before any lane
 // writes: a bf16 row r covers the bytes of fp8 rows 2r - 128 and 2r - 127 of
 // a 128-row panel (of the same or earlier steps), and for a V chunk bf16
 // panel p covers fp8 panels 2p - 4 and 2p - 3 (of the same or earlier panels).
@@ -269,7 +272,7 @@ __device__ __forceinline__ void expand_k_panel(unsigned char* slot, int lane) {
     const uint4* src = reinterpret_cast<const uint4*>(slot + kPanel / 2 + 64 * r);
     uint4 q[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) q[k] = src[k];
+    for (int k = 0; k < 4; ++k) q[k] = src[k ^ ((r >> 1) & 3)];
     __syncwarp();
     expand_row_fp8(slot + 128 * r, r, q);
     __syncwarp();
@@ -286,7 +289,7 @@ __device__ __forceinline__ void expand_v_chunk(unsigned char* slot, int lane, in
     const uint4* src = reinterpret_cast<const uint4*>(slot + kPanels * kVPanel / 2 + p * (kVPanel / 2) + 64 * lane);
     uint4 q[4];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) q[k] = lane < rows_valid ? src[k] : make_uint4(0, 0, 0, 0);
+    for (int k = 0; k < 4; ++k) q[k] = lane < rows_valid ? src[k ^ ((lane >> 1) & 3)] : make_uint4(0, 0, 0, 0);
     __syncwarp();
     expand_row_fp8(slot + p * kVPanel + 128 * lane, lane, q);
     __syncwarp();
