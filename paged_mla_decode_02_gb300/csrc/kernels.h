@@ -74,7 +74,7 @@ struct TcMaps {
   CUtensorMap kpe_k;    // [pages*P, 64] bf16 (fp8), box 64 x P
   CUtensorMap ckv_v;    // (64, pages*P, 8 panels) view of ckv, box 64 x min(P, 32) x 4 panels
 };
-// kv_fp8: e4m3 cache (maps of bytes without swizzle, page_size >= 32); the
+// kv_fp8: e4m3 cache (byte maps, 64-byte swizzle, page_size >= 32); the
 // kernel expands each copy to bf16 in shared memory and scales by kv_scale.
 cudaError_t launch_decode_tc(const DecodeArgs& a, const TcMaps& maps, bool out_f32, bool kv_fp8,
                              cudaStream_t s);
