@@ -358,9 +358,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kc = 0, g = 0, uidx = 0;
     bool ok = true;
     // fp8 cache: the even panels of a tile (j = 0, 2, .., 8) are expanded to
-    // bf16 here, panel k once panel k + kKSlots - 1 has been issued, and every
-    // issued one before this warp waits on anything the QK warp signals; the
-    // QK warp expands the odd panels itself
+    // bf16 here, panel k once panel k + 1 has been issued (one behind: a
+    // longer lag would chain the expansion of panel k behind the MMAs of
+    // panel k - 1 through the ring), and every issued one before this warp
+    // waits on anything the QK warp signals; the QK warp expands the odd
+    // panels itself
     int kx = 0;   // next panel to expand
     auto expand_upto = [&](int end) {
       for (; kx < end && ok; ++kx) {
@@ -414,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
               tma_load_2d(dst, &maps.kpe_k, 0, row, full);
           }
-          if (kFp8) expand_upto(kc + 2 - L::kKSlots);
+          if (kFp8) expand_upto(kc);
         }
       }
     }
@@ -446,8 +448,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t vphase = 0;   // parity of the current pass over the ring
     bool ok = true;
     // fp8 cache: the even chunks of a tile are expanded to bf16 here (rows
-    // past the request's end zeroed), chunk k once chunk k + kVSlots - 1 has
-    // been issued; the PV warp expands the odd ones.  A chunk's valid row
+    // past the request's end zeroed), chunk k once chunk k + 1 has been
+    // issued (one behind, as for K); the PV warp expands the odd ones.  A chunk's valid row
     // count (and bit 16: odd in its tile) waits in shared memory, one entry
     // per slot.
     volatile int* vrows = reinterpret_cast<volatile int*>(sm + L::kOffBar + kNumBars * 8 + 16);
@@ -506,7 +508,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(dst + lane * vbox * L::kVPanels * kRowBytes, &maps.ckv_v, 0, page * P + (tb % P),
                       L::kVPanels * rank, full);
         if (kFp8) {
-          expand_upto(vc + 2 - L::kVSlots);
+          expand_upto(vc);
         } else if (rows < kVChunkTok) {
           // Last chunk of a request: rows past kv_len may hold anything (even
           // NaN), and P = 0 there does not cancel NaN.  Wait for the copy,
