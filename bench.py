@@ -72,6 +72,11 @@ def algorithmic(x) -> tuple[float, float]:
     return nbytes, flops
 
 
+def pct(ms: list[float]) -> list[float]:
+    """p10, p50, p90 of a list of millisecond times, in microseconds."""
+    return [float(np.percentile(ms, q) * 1000) for q in (10, 50, 90)]
+
+
 def peaks() -> tuple[float, float, float, str]:
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -106,7 +111,7 @@ class L2Flush:
         self.r.view(torch.float32).sum()   # the read pass, reduced as fp32 words: no widened copy
 
 
-PROFILE = os.path.join(ROOT, "profiles", "decode_tc_deepseek.md")
+PROFILE = os.path.join(ROOT, "profiles", "decode_tc_deepseek.json")
 KERNEL_SOURCES = ["decode_tc.cu", "tc_utils.cuh", "device_utils.cuh", "kernels.h", "mla_internal.h"]
 
 
@@ -122,11 +127,7 @@ def profiled_traffic(workload: str) -> float | None:
         h.update(f.encode())
         with open(os.path.join(ROOT, "paged_mla_decode_02_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    vals = {}
-    for line in open(PROFILE):
-        if ":" in line and line.split(":", 1)[0] in ("source_sha256", "dram_bytes_per_launch"):
-            k, v = line.split(":", 1)
-            vals[k] = v.strip()
+    vals = json.load(open(PROFILE))
     if vals.get("source_sha256") != h.hexdigest() or "dram_bytes_per_launch" not in vals:
         return None
     return float(vals["dram_bytes_per_launch"])
@@ -528,7 +529,7 @@ def run_absorbed(args) -> None:
 def main() -> None:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="deepseek")
@@ -605,31 +606,51 @@ def main() -> None:
             step()
     stream.synchronize()
     dec.check_status()
-    k0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    k1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    s0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    s1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    K = args.steps
+    ev = lambda n: [torch.cuda.Event(enable_timing=True) for _ in range(n)]   # noqa: E731
+    k0, k1, s0, s1, h0 = ev(K), ev(K), ev(K), ev(K), ev(K + 1)
     # torch creates an event lazily at its first record: create all of them
     # here, before the library is handed their handles
     with torch.cuda.stream(stream):
-        for e in k0 + k1 + s0 + s1:
+        for e in k0 + k1 + s0 + s1 + h0:
             e.record(stream)
         for _ in range(args.warmup):
             flush.zero_()
             step()
     stream.synchronize()
 
+    # (1) the decode kernel alone: K eager runs, events the library records
+    # immediately around its kernel launch (roofline.kernel_us)
+    with torch.cuda.stream(stream):
+        for i in range(K):
+            flush.zero_()
+            mla.mla_plan_set_profile_events(dec.handle, k0[i], k1[i])
+            step()
+    stream.synchronize()
+    mla.mla_plan_set_profile_events(dec.handle, None, None)
+    dec.check_status()
+    kern_ms = [a.elapsed_time(b) for a, b in zip(k0, k1)]
+
+    # (2) the timed steps: the run replayed from a CUDA graph, L2 flushed
+    # before each replay (outside the events)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            graph.replay()
+    stream.synchronize()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     wall0 = time.perf_counter()
     with torch.cuda.stream(stream):
-        for i in range(args.steps):
+        for i in range(K):
             flush.zero_()
-            mla.mla_plan_set_profile_events(dec.handle, k0[i], k1[i])
             s0[i].record(stream)
-            step()
+            graph.replay()
             s1[i].record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
@@ -637,12 +658,20 @@ def main() -> None:
         dist.barrier()
     wall = time.perf_counter() - wall0
     clk = clocks.stop()
-    mla.mla_plan_set_profile_events(dec.handle, None, None)
     dec.check_status()
-
     step_ms = [a.elapsed_time(b) for a, b in zip(s0, s1)]
-    kern_ms = [a.elapsed_time(b) for a, b in zip(k0, k1)]
-    us_per_batch = job_us_per_batch(sum(step_ms), args.steps, world, dev)
+    us_per_batch = job_us_per_batch(sum(step_ms), K, world, dev)
+
+    # (3) hot: K replays back to back, nothing flushed (the inputs exceed L2,
+    # so most of them still come from DRAM)
+    with torch.cuda.stream(stream):
+        h0[0].record(stream)
+        for i in range(K):
+            graph.replay()
+            h0[i + 1].record(stream)
+    stream.synchronize()
+    dec.check_status()
+    hot_ms = [h0[i].elapsed_time(h0[i + 1]) for i in range(K)]
 
     # end to end through the host-buffer entry point (q in, out / lse back)
     qn_h = q_nope.cpu().pin_memory()
@@ -704,7 +733,14 @@ def main() -> None:
             "gpu_launches": (1 if info["kernel"] == mla.KERNEL_TCGEN05 else 2) * args.steps,
             "wall_s_timed": wall, "plan_us": plan_us,
             "kernel": info["kernel"], "plan": info,
-            "step_us_p10_p50_p90": [float(np.percentile(step_ms, q) * 1000) for q in (10, 50, 90)]}
+            "timing": {"method": "each timed step replays the run from a CUDA graph; CUDA events "
+                                 "on the launching stream around each replay; L2 flushed before "
+                                 "each cold replay, outside the events",
+                       "cold_us_mean": us_per_batch,
+                       "cold_us_p10_p50_p90": pct(step_ms),
+                       "hot_us_mean": statistics.mean(hot_ms) * 1000.0,
+                       "hot_us_p10_p50_p90": pct(hot_ms),
+                       "kernel_us_p10_p50_p90": pct(kern_ms)}}
     if not args.no_cpu_baseline and world == 1:
         us, n, secs = oracle_sample(x, args.cpu_budget)
         line["cpu_baseline"] = {"value": us, "unit": UNIT, "cores": os.cpu_count(),

@@ -201,21 +201,32 @@ mla_status_t mla_decode_run_host(mla_plan_t plan, const void* q_nope_host,
  *   48 MiB scratch array inside the library; the work-unit list is built in
  *   static host memory.  Nothing is allocated (no cudaMalloc, no pinned host
  *   memory, no heap allocation on success).
+ *   The array is a __device__ variable of the library image: its 48 MiB are
+ *   taken on every device where the library's module is loaded, whether or
+ *   not this call is ever used (plan / run callers pay it too), until the
+ *   process exits.
  *   Limits: batch <= 4096 (else MLA_ERR_CAPACITY, before any device work); the
  *   batch's partials and work units must fit the scratch (else
  *   MLA_ERR_CAPACITY; with 128 heads they take about 38 MiB at most on a
- *   152-SM GPU).  bf16 q and caches only; head dims 512 / 64.
+ *   152-SM GPU).  bf16 q and caches only (the call has no dtype argument: an
+ *   fp8 cache passed here is read as bf16 and gives wrong results);
+ *   kv_scale must be 1 (another value is MLA_ERR_UNSUPPORTED); head dims
+ *   512 / 64.
  *   Arguments as for mla_decode_plan / mla_decode_run (kv_indptr_host and
  *   kv_len_host on the host, everything else on the device; kv_indices_dev is
  *   only read by this call's kernel).
  *   The first call on a device does the setup (looks up the scratch address,
  *   queries the SM count and kernel residency); make it before any work that
  *   must not see those calls.
- *   Each call zeroes, on `stream`, the counters and the status word the
- *   kernel expects at zero, uploads its work units and launches one kernel;
- *   it returns without waiting unless check_status is nonzero, in which case
- *   it synchronises `stream` and returns MLA_ERR_DEVICE_BOUNDS /
- *   MLA_ERR_DEVICE_TIMEOUT if the kernel recorded one.
+ *   Each call zeroes, on `stream`, the split counters the kernel expects at
+ *   zero, uploads its work units and launches one kernel; it returns without
+ *   waiting unless check_status is nonzero.  The device status word is
+ *   sticky: it keeps the first error (a page id out of range, an expired
+ *   device wait) that any call recorded, until a call with check_status != 0
+ *   synchronises `stream`, reads it, clears it and returns it
+ *   (MLA_ERR_DEVICE_BOUNDS / MLA_ERR_DEVICE_TIMEOUT).  So a caller that
+ *   checks only every few steps still learns of an error in a step it did
+ *   not check; that step's out / lse are not to be trusted.
  *   The scratch and the host staging are shared by all calls in the process:
  *   calls that overlap (other streams, other host threads) race and corrupt
  *   each other.  Issue them one after another on one stream.

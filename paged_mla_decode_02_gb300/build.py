@@ -42,8 +42,8 @@ def _headers() -> list[str]:
     return hs
 
 
-def _compile(nvcc: str, src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(nvcc: str, src: str, extra: list[str], build_dir: str = BUILD) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     cmd = [nvcc, *ARCH, *COMMON, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -72,6 +72,31 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     if verbose:
         print(f"built {LIB}")
     return LIB
+
+
+def build_variant(name: str, defines: list[str]) -> str:
+    """Build ``lib/libmla_decode_<name>.so`` from the same sources with extra
+    preprocessor definitions (e.g. the test build with short device waits,
+    ``-DMLA_STALL_TEST``).  Only tests load such a library; the product path
+    loads ``libmla_decode.so`` alone."""
+    out = os.path.join(LIBDIR, f"libmla_decode_{name}.so")
+    srcs = sources()
+    newest = max(os.path.getmtime(p) for p in srcs + _headers() + [__file__])
+    if os.path.exists(out) and os.path.getmtime(out) >= newest:
+        return out
+    bdir = os.path.join(BUILD, name)
+    os.makedirs(bdir, exist_ok=True)
+    os.makedirs(LIBDIR, exist_ok=True)
+    nvcc = _nvcc()
+    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
+        objs = list(ex.map(lambda s: _compile(nvcc, s, list(defines), bdir), srcs))
+    tmp = out + ".tmp"
+    r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

@@ -544,6 +544,13 @@ mla_status_t mla_plan_check_status(mla_plan_t plan) {
     return cuda_fail(plan, e, "read error word");
   if ((e = cudaMemset(plan->d_err, 0, sizeof(int32_t))) != cudaSuccess)
     return cuda_fail(plan, e, "clear error word");
+  // A launch that gave up on a wait may have left split-request counts
+  // behind (they return to zero only when a request is combined): clear
+  // them, so the next run of the same plan starts clean without a re-plan.
+  if (code != 0 &&
+      (e = cudaMemset(plan->d_counters, 0, sizeof(int32_t) * 8 * static_cast<size_t>(plan->max_batch))) !=
+          cudaSuccess)
+    return cuda_fail(plan, e, "clear split counters");
   if (code == kErrTimeout) return fail(plan, MLA_ERR_DEVICE_TIMEOUT, "a device wait timed out");
   if (code == kErrBounds) return fail(plan, MLA_ERR_DEVICE_BOUNDS, "a page id was out of range");
   return MLA_OK;

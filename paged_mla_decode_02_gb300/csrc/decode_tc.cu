@@ -68,6 +68,12 @@ namespace {
 
 using namespace tc;
 
+#ifdef MLA_STALL_TEST
+// Test build only: when nonzero, CTA 0's V producer leaves out its
+// g_stall_chunk-th copy (1-based), so the PV warp's wait for it runs out.
+__device__ int g_stall_chunk;
+#endif
+
 constexpr int kT = kTileTc;                 // 128 tokens per tile
 constexpr int kThreads = 384;
 constexpr int kSoftmaxWarps = 8;
@@ -146,6 +152,12 @@ static_assert(kNumBars * 8 + 16 + 4 * kMaxVSlots <= kBarBytes, "barrier area");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units: P values stay below 2^8
+// A tile applied with a reference more than kDropLog2 below the running one
+// (its owner had not yet seen the previous tile's far larger maximum) weighs
+// below 2^-(kDropLog2 - kRescaleThreshold) per token against the rows already
+// summed, beneath fp32 resolution; moving O up to its reference instead
+// could overflow.  Such a row keeps its state and its P row is zeroed.
+constexpr float kDropLog2 = 64.0f;
 constexpr int kMergeRegs = 8;               // split request slots whose weights stay in registers
 
 template <int C>
@@ -496,7 +508,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t full = bar_addr<C>(base, kVFull0 + slot);
         constexpr int kRowBytes = kFp8 ? 64 : 128;   // one row of a panel as copied
         const uint32_t dst = base + L::kOffV + slot * L::kVSlot + (kFp8 ? L::kVSlot / 2 : 0);
-        if (lane == 0) {
+#ifdef MLA_STALL_TEST
+        const bool skip = g_stall_chunk != 0 && blockIdx.x == 0 && vc + 1 == g_stall_chunk;
+#else
+        constexpr bool skip = false;
+#endif
+        if (lane == 0 && !skip) {
           if (kFp8) vrows[slot] = rows | ((((t - tok0) / kVChunkTok) & 1) << 16);
           mbar_arrive_expect_tx(full, ncopy * vbox * L::kVPanels * kRowBytes);
         }
@@ -504,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // lane c < ncopy issues copy c (lanes past it mirror the last one for the shuffle)
         const int tb = t + vbox * min(lane, ncopy - 1);
         const int page = __shfl_sync(0xffffffffu, pg_cur, (tb - tok0) / P);
-        if (lane < ncopy)
+        if (lane < ncopy && !skip)
           tma_load_3d(dst + lane * vbox * L::kVPanels * kRowBytes, &maps.ckv_v, 0, page * P + (tb % P),
                       L::kVPanels * rank, full);
         if (kFp8) {
@@ -871,19 +888,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i > 0) {
         // ---------- apply tile t = g0 + i - 1 (own or received), release it to PV ----------
         const int t = g0 + i - 1;
+        const int tb = L::kPBufs == 2 ? (t & 1) : 0;   // P buffer (and received info) of tile t
+        const bool recv = t % C != rank;
+        const uint32_t tpar = (recv_par >> tb) & 1;   // phase parity of tile t's receive barriers
         float mt, tlx, tlr;
-        if (t % C == rank) {
+        if (!recv) {
           mt = own_m;
           tlx = own_lx;
           tlr = own_lr;
         } else {
-          const int b = L::kPBufs == 2 ? (t & 1) : 0;   // P buffer (and received info) of tile t
+          const int b = tb;
           if (warp == 3 && lane == 0) {
             mbar_arrive_expect_tx(bar_addr<C>(base, kPRecvB0 + b), kPanel);
             mbar_arrive_expect_tx(bar_addr<C>(base, kPRecvP0 + b), kPanel);
             mbar_arrive_expect_tx(bar_addr<C>(base, kPRecv0 + b), kInfoBytes);
           }
-          if (!(ok = mbar_wait_warp(bar_addr<C>(base, kPRecv0 + b), (recv_par >> b) & 1, abort_flag)))
+          if (!(ok = mbar_wait_warp(bar_addr<C>(base, kPRecv0 + b), tpar, abort_flag)))
             break;
           recv_par ^= 1u << b;
           const float* info =
@@ -899,7 +919,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                             abort_flag)))
           break;
         const bool first = t == g0;
-        const float alpha = first ? 0.f : exp2f(m_last - mt);
+        const bool drop = !first && m_last - mt > kDropLog2;
+        if (__any_sync(0xffffffffu, drop)) {
+          // zero the dropped rows' P (this warp's token half) in this CTA's
+          // copy; a received panel must have landed first
+          if (recv && !(ok = mbar_wait_warp(bar_addr<C>(base, (hc == 0 ? kPRecvP0 : kPRecvB0) + tb), tpar,
+                                            abort_flag)))
+            break;
+          if (drop) {
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+              *reinterpret_cast<uint4*>(sm + L::kOffP + tb * L::kPStride + p_off + (ch << 4)) =
+                  make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        const float alpha = first ? 0.f : drop ? 1.f : exp2f(m_last - mt);
         if (!first && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O holds P . V of earlier tiles relative to m_last: move it to mt
           if (!(ok = mbar_wait_warp(bar_addr<C>(base, kPvDone0 + ((t - 1) & 1)), ((t - 1) >> 1) & 1,
@@ -917,10 +952,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_st_wait();
         }
-        lx = first ? tlx : lx * alpha + tlx;
-        lr = first ? tlr : lr * alpha + tlr;
-        m_prev = m_last;
-        m_last = mt;
+        if (!drop) {
+          lx = first ? tlx : lx * alpha + tlx;
+          lr = first ? tlr : lr * alpha + tlr;
+          m_prev = m_last;
+          m_last = mt;
+        }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_addr<C>(base, kPReady0 + (t & 1)));
@@ -1227,6 +1264,13 @@ cudaError_t decode_tc_max_workers(int* workers) {
   *workers = clusters;
   return cudaSuccess;
 }
+
+#ifdef MLA_STALL_TEST
+// Test build only: set the copy CTA 0's V producer leaves out (0: none).
+extern "C" int mla_test_set_stall(int chunk) {
+  return static_cast<int>(cudaMemcpyToSymbol(g_stall_chunk, &chunk, sizeof(chunk)));
+}
+#endif
 
 cudaError_t launch_decode_tc(const DecodeArgs& a, const TcMaps& maps, bool out_f32, bool kv_fp8,
                              cudaStream_t s) {

@@ -114,17 +114,18 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
 // prefix and a request's own suffix, say) combined into one: one warp per
 // row, 16 consecutive dims per lane (four 16-byte loads from each state), the
 // whole row read before it is written, so the output may alias an input.
+// The inputs may alias the outputs, so they are neither __restrict__ nor read
+// through the read-only path: plain loads (cached in L2 only).
 constexpr int kStatesWarps = 8;
 template <bool kOutF32>
 __global__ void __launch_bounds__(32 * kStatesWarps)
-    merge_states_kernel(const float* __restrict__ o_a, const float* __restrict__ lse_a,
-                        const float* __restrict__ o_b, const float* __restrict__ lse_b, void* out,
-                        float* lse_out, int rows) {
+    merge_states_kernel(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
+                        void* out, float* lse_out, int rows) {
   const int row = blockIdx.x * kStatesWarps + (threadIdx.x >> 5);
   if (row >= rows) return;
   const int lane = threadIdx.x & 31;
   const size_t base = static_cast<size_t>(row) * kDCkv + 16 * lane;
-  const float la = lse_a[row], lb = lse_b[row];
+  const float la = __ldcg(lse_a + row), lb = __ldcg(lse_b + row);
   const float M = fmaxf(la, lb);
   float wa = 0.f, wb = 0.f, lse = -INFINITY;
   if (M != -INFINITY) {
@@ -138,8 +139,8 @@ __global__ void __launch_bounds__(32 * kStatesWarps)
   float4 a4[4], b4[4];
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    a4[k] = __ldg(reinterpret_cast<const float4*>(o_a + base) + k);
-    b4[k] = __ldg(reinterpret_cast<const float4*>(o_b + base) + k);
+    a4[k] = __ldcg(reinterpret_cast<const float4*>(o_a + base) + k);
+    b4[k] = __ldcg(reinterpret_cast<const float4*>(o_b + base) + k);
   }
   float v[16];
 #pragma unroll

@@ -28,7 +28,10 @@ constexpr int kMaxWorkers = 512;
 constexpr int kMaxUnits = kMaxWorkers + kMaxBatch;
 constexpr int kMaxDevices = 64;
 
+// Status word at offset 0 (its own 256 bytes), then the plan blob, the split
+// partials and the counters of the current call.
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+constexpr size_t kBlobOffset = 256;
 
 struct DeviceSetup {
   bool done;
@@ -66,6 +69,8 @@ extern "C" mla_status_t mla_decode_noalloc(
   if (!q_nope || !q_pe || !ckv_cache || !kpe_cache || !out || !lse) return MLA_ERR_INVALID_ARG;
   if (kv_indptr_host[batch] > 0 && !kv_indices_dev) return MLA_ERR_INVALID_ARG;
   if (num_pages < 1 || !std::isfinite(kv_scale) || kv_scale <= 0.f) return MLA_ERR_INVALID_ARG;
+  // bf16 caches only: a scale other than 1 can only mean a quantised cache
+  if (kv_scale != 1.f) return MLA_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(ckv_cache) | reinterpret_cast<uintptr_t>(kpe_cache) |
        reinterpret_cast<uintptr_t>(q_nope) | reinterpret_cast<uintptr_t>(q_pe) |
        reinterpret_cast<uintptr_t>(out)) & 15)
@@ -97,6 +102,7 @@ extern "C" mla_status_t mla_decode_noalloc(
   }
 
   // ---- partition into static host memory ----
+  // (the blob goes to scratch offset kBlobOffset; the status word stays at 0)
   const size_t off_units = align_up(sizeof(PlanDev), 16);
   WorkUnit* units = reinterpret_cast<WorkUnit*>(g_host_blob + off_units);
   // worker offsets and merge entries follow the units, whose count is known
@@ -123,20 +129,22 @@ extern "C" mla_status_t mla_decode_noalloc(
   prm.n_slots = n_slots;
   std::memcpy(g_host_blob, &prm, sizeof(prm));
 
-  // ---- scratch layout for this call ----
-  const size_t off_opart = align_up(blob_bytes, 256);
+  // ---- scratch layout for this call: status word | blob | partials | counters ----
+  const size_t off_opart = align_up(kBlobOffset + blob_bytes, 256);
   const size_t off_lpart =
       align_up(off_opart + sizeof(float) * static_cast<size_t>(n_slots) * num_heads * kDCkv, 256);
   const size_t off_cnt = align_up(
       off_lpart + sizeof(float) * static_cast<size_t>(n_slots) * kLsePartCopies * num_heads, 256);
-  const size_t off_err = off_cnt + sizeof(int32_t) * 8 * static_cast<size_t>(batch);
-  const size_t need = off_err + sizeof(int32_t);
+  const size_t need = off_cnt + sizeof(int32_t) * 8 * static_cast<size_t>(batch);
   if (need > kScratchBytes) return MLA_ERR_CAPACITY;
 
-  // ---- upload, zero what must start at zero, launch ----
+  // ---- upload, zero the split counters, launch ----
+  // The status word is not cleared here: it keeps the first error of any call
+  // until a call with check_status != 0 reads and clears it.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned char* sc = su.scratch;
-  if ((e = cudaMemcpyAsync(sc, g_host_blob, blob_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
+  if ((e = cudaMemcpyAsync(sc + kBlobOffset, g_host_blob, blob_bytes, cudaMemcpyHostToDevice, s)) !=
+          cudaSuccess ||
       (e = cudaMemsetAsync(sc + off_cnt, 0, need - off_cnt, s)) != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_CUDA;
@@ -150,16 +158,16 @@ extern "C" mla_status_t mla_decode_noalloc(
   a.ckv = ckv_cache;
   a.kpe = kpe_cache;
   a.kv_indices = kv_indices_dev;
-  a.units = reinterpret_cast<const WorkUnit*>(sc + off_units);
-  a.worker_ptr = reinterpret_cast<const int32_t*>(sc + off_wptr);
-  a.params = reinterpret_cast<const PlanDev*>(sc);
+  a.units = reinterpret_cast<const WorkUnit*>(sc + kBlobOffset + off_units);
+  a.worker_ptr = reinterpret_cast<const int32_t*>(sc + kBlobOffset + off_wptr);
+  a.params = reinterpret_cast<const PlanDev*>(sc + kBlobOffset);
   a.out = out;
   a.lse = lse;
   a.o_part = reinterpret_cast<float*>(sc + off_opart);
   a.lse_part = reinterpret_cast<float*>(sc + off_lpart);
-  a.merge = reinterpret_cast<const MergeEntry*>(sc + off_merge);
+  a.merge = reinterpret_cast<const MergeEntry*>(sc + kBlobOffset + off_merge);
   a.counters = reinterpret_cast<int32_t*>(sc + off_cnt);
-  a.err = reinterpret_cast<int32_t*>(sc + off_err);
+  a.err = reinterpret_cast<int32_t*>(sc);
   a.num_pages = num_pages;
   a.num_heads = num_heads;
   a.kv_scale = 1.f;   // a bf16 cache: no dequantisation scale
@@ -170,9 +178,11 @@ extern "C" mla_status_t mla_decode_noalloc(
     return MLA_ERR_CUDA;
   }
   if (!check_status) return MLA_OK;
+  // the first error recorded since the last checking call (this one included)
   int32_t err = 0;
   if ((e = cudaMemcpyAsync(&err, a.err, sizeof(err), cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
-      (e = cudaStreamSynchronize(s)) != cudaSuccess) {
+      (e = cudaStreamSynchronize(s)) != cudaSuccess ||
+      (err != 0 && (e = cudaMemsetAsync(a.err, 0, sizeof(int32_t), s)) != cudaSuccess)) {
     cudaGetLastError();
     return MLA_ERR_CUDA;
   }

@@ -148,10 +148,17 @@ int fill_workers(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int
 
 int partition_units(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int n_workers,
                     int tile_tokens, WorkUnit* units, int32_t* worker_ptr) {
-  // Smallest budget the greedy fill meets, by bisection; one worker holding
-  // everything always fits.
-  long long total = 0;
-  for (int b = 0; b < batch; ++b) total += tiles_of(kv_len[b], tile_tokens);
+  // Smallest budget the greedy fill meets.  Whether the fill succeeds is not
+  // monotone in the budget (where a request is cut depends on it), so a
+  // bisection finds a feasible budget `hi` only; the smallest one is then
+  // looked for upward from the lower bound every partition obeys (the work
+  // spread evenly), at most kMaxScan budgets.  One worker holding everything
+  // always fits.
+  long long total = 0, nonempty = 0;
+  for (int b = 0; b < batch; ++b) {
+    total += tiles_of(kv_len[b], tile_tokens);
+    nonempty += kv_len[b] > 0;
+  }
   long long lo = 0;
   long long hi = kTileCost * total + static_cast<long long>(kUnitCost + kSplitCost) * (batch + n_workers);
   while (lo + 1 < hi) {
@@ -161,6 +168,13 @@ int partition_units(const int32_t* kv_indptr, const int32_t* kv_len, int batch, 
     else
       lo = mid;
   }
+  constexpr long long kMaxScan = 4096;
+  const long long bound = (kTileCost * total + kUnitCost * nonempty + n_workers - 1) / n_workers;
+  for (long long b = std::max(bound, hi - kMaxScan); b < hi; ++b)
+    if (fill_workers(kv_indptr, kv_len, batch, n_workers, tile_tokens, b, nullptr, nullptr) >= 0) {
+      hi = b;
+      break;
+    }
   return fill_workers(kv_indptr, kv_len, batch, n_workers, tile_tokens, hi, units, worker_ptr);
 }
 

@@ -71,7 +71,13 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 // Waits for the phase of `bar` with the given parity to complete.  Gives up
 // after ~kWaitLimitNs (or when another role of the CTA has given up and set
 // *abort), returning false.  No wait in the kernel can therefore hang.
+#ifdef MLA_STALL_TEST
+// Test build only (a separate library the product never loads): waits give up
+// after 1 ms, so a test can make one run out on purpose and check the status.
+constexpr uint64_t kWaitLimitNs = 1000000ull;      // 1 ms
+#else
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+#endif
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int* abort_flag) {
   if (mbar_test_wait(bar, parity)) return true;
@@ -91,7 +97,11 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
 // Drain wait used on the way out of a kernel: ignores the abort flag (copies
 // or MMAs already issued must land before the CTA exits) but still gives up
 // after kDrainLimitNs.
+#ifdef MLA_STALL_TEST
+constexpr uint64_t kDrainLimitNs = 20000000ull;    // 20 ms
+#else
 constexpr uint64_t kDrainLimitNs = 200000000ull;   // 0.2 s
+#endif
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 0;; ++i) {

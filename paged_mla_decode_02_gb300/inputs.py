@@ -170,6 +170,35 @@ def make_inputs(name: str, kv_len, num_heads: int, page_size: int, *,
                      kv_scale=float(kv_scale))
 
 
+def plant_dominant_tokens(x: MLAInputs, where, gap: float) -> MLAInputs:
+    """Make token ``pos`` of request ``b`` score about ``gap`` natural-log
+    units above the request's other tokens, in every head, for each (b, pos)
+    in ``where``.  Every head of such a request gets head 0's q_pe, and the
+    token's kpe row becomes that vector times gap / (sm_scale |q_pe|^2), so
+    the rope term of its score rises by about ``gap`` (the stored values are
+    rounded to the cache dtype; the exact scores follow from them).  An
+    attention-sink token at position 0, or one late sharp maximum, is the
+    case this builds.  Returns a modified copy."""
+    y = dataclasses.replace(x, q_pe=x.q_pe.copy(), kpe=x.kpe.copy())
+    for b, pos in where:
+        if not 0 <= pos < int(x.kv_len[b]):
+            raise ValueError(f"token {pos} is outside request {b}")
+        y.q_pe[b, ...] = y.q_pe[b, ..., :1, :] if y.q_pe.ndim == 3 else y.q_pe[b, :, :1, :]
+        u = _bits_to_f32(y.q_pe[b].reshape(-1, D_KPE)[0])
+        k = np.float32(gap / (x.sm_scale * float(np.dot(u.astype(np.float64), u))))
+        row = (u * k).reshape(1, D_KPE)
+        page = x.kv_indices[x.kv_indptr[b] + pos // x.page_size]
+        if x.kv_dtype == "bf16":
+            y.kpe[page, pos % x.page_size] = f32_to_bf16_bits(row)[0]
+        else:
+            y.kpe[page, pos % x.page_size] = f32_to_e4m3_codes(row / np.float32(x.kv_scale))[0]
+    return y
+
+
+def _bits_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
 def _ragged_lengths(rng):
     return rng.integers(1, 8193, size=128)
 

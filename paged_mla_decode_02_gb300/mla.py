@@ -64,6 +64,14 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     global _lib
     if _lib is not None:
         return _lib
+    _lib = bind_library(path)
+    return _lib
+
+
+def bind_library(path: str) -> ctypes.CDLL:
+    """Open a build of the library at ``path`` and declare the C signatures
+    on it (a separate handle; the module's own calls keep using
+    ``load_library``'s)."""
     if not os.path.exists(path):
         raise RuntimeError(f"{path} is missing: build it with "
                            "paged_mla_decode_02_gb300.build.build() (nvcc, sm_103a)")
@@ -107,7 +115,6 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.mla_decode_noalloc.restype = c_int
     lib.mla_decode_noalloc.argtypes = [_I32P, _VP, _I32P, c_int, c_int, c_int, c_float, _VP, _VP,
                                        _VP, _VP, c_float, c_int, _VP, c_int, _VP, c_int, _VP]
-    _lib = lib
     return lib
 
 

@@ -168,3 +168,49 @@ def test_partition_rejects_inconsistent_paging(lib):
     nz[0] = 1
     with pytest.raises(mla.MLAError):
         mla.mla_plan_partition_host(nz, lens, 4, 128, 16)
+
+
+def _greedy_fits(lens, W, T, budget, TILE=4, UNIT=8, SPLIT=4, MIN_PIECE=4):
+    """The planner's fill rule, restated: requests in order, whole while they
+    fit, else cut where the worker fills up (both pieces >= MIN_PIECE tiles)."""
+    w, used = 0, 0
+    for L in lens:
+        n = (int(L) + T - 1) // T
+        t, split = 0, False
+        while t < n:
+            if w >= W:
+                return False
+            whole = UNIT + TILE * (n - t) + (SPLIT if split else 0)
+            if used + whole <= budget:
+                used += whole
+                break
+            take = min((budget - used - UNIT - SPLIT) // TILE, n - t - MIN_PIECE)
+            if take < MIN_PIECE:
+                if used == 0:
+                    return False
+                w, used = w + 1, 0
+                continue
+            t += take
+            split = True
+            w, used = w + 1, 0
+    return True
+
+
+def test_partition_makespan_is_the_smallest_feasible_budget(lib):
+    # The fill's success is not monotone in the budget, so a bisection alone
+    # can stop above the best budget (one request of 19 tiles on 5 workers:
+    # 40 against 32).  The planner's largest worker cost must equal the
+    # smallest budget a linear scan finds.
+    T, P = 128, 64
+    rng = np.random.Generator(np.random.PCG64(23))
+    cases = [([19 * 128], 5)]
+    for _ in range(40):
+        B_ = int(rng.integers(1, 6))
+        cases.append((list(rng.integers(1, 40 * 128, size=B_)), int(rng.integers(1, 12))))
+    for lens, W in cases:
+        indptr, l32 = _batch(lens, P)
+        units, wptr, _, _ = mla.mla_plan_partition_host(indptr, l32, W, T, P)
+        cost = [sum(4 * ((u[2] - u[1] + T - 1) // T) + 8 + (4 if u[3] >= 0 else 0)
+                    for u in units[wptr[w]:wptr[w + 1]]) for w in range(W)]
+        best = next(b for b in range(1, 10 ** 6) if _greedy_fits(l32, W, T, b))
+        assert max(cost) <= best, (lens, W, max(cost), best)

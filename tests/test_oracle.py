@@ -125,6 +125,28 @@ def test_single_token_closed_form():
     assert np.allclose(lse, s0, rtol=0, atol=1e-12)
 
 
+def test_dominant_token_closed_form():
+    # one token scoring ~200 natural-log units above the rest: the softmax is
+    # that token alone (the others weigh below e^-190), so out is its ckv row
+    # and lse its score, computed here by scalar loops on the decoded values
+    x = I.make_inputs("dominant", [300, 130], 4, 64, seed=21)
+    y = I.plant_dominant_tokens(x, [(0, 0), (1, 129)], 200.0)
+    out, lse = O.mla_decode_inputs(y)
+
+    def bf16(bits):
+        return [float(v) for v in (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)]
+
+    for b, pos in ((0, 0), (1, 129)):
+        page = y.kv_indices[y.kv_indptr[b] + pos // 64]
+        c = bf16(y.ckv[page, pos % 64])
+        k = bf16(y.kpe[page, pos % 64])
+        for h in range(y.num_heads):
+            qn, qp = bf16(y.q_nope[b, h]), bf16(y.q_pe[b, h])
+            s = y.sm_scale * math.fsum([a * w for a, w in zip(qn, c)] + [a * w for a, w in zip(qp, k)])
+            assert abs(lse[b, h] - s) <= 1e-9 * max(1.0, abs(s))
+            assert np.allclose(out[b, h], c, rtol=0, atol=1e-12)
+
+
 def _uniform_error(attend_fn):
     rng = _rng(5)
     L = 29
