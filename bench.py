@@ -533,7 +533,7 @@ def main() -> None:
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="deepseek")
-    ap.add_argument("--kernel", default="default", choices=["default", "tcgen05", "mma_sync"])
+    ap.add_argument("--kernel", default="default", choices=["default", "tcgen05", "mma_sync", "pair"])
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--ref-step-budget", type=float, default=8.0)

@@ -61,7 +61,8 @@ typedef enum {
 typedef enum {
   MLA_KERNEL_DEFAULT = 0,     /* the tcgen05 / TMEM kernel */
   MLA_KERNEL_TCGEN05 = 1,     /* same as DEFAULT, named explicitly */
-  MLA_KERNEL_MMA_SYNC = 2     /* warp-level mma.sync kernel (legacy tensor path, for comparison) */
+  MLA_KERNEL_MMA_SYNC = 2,    /* warp-level mma.sync kernel (legacy tensor path, for comparison) */
+  MLA_KERNEL_PAIR = 3         /* tcgen05 kernel whose MMAs span a CTA pair (cta_group::2); bf16 caches */
 } mla_kernel_t;
 
 /* Plan statistics, filled by mla_plan_info. */

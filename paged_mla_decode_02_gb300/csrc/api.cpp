@@ -181,6 +181,20 @@ bool mla::encode_tc_maps(TcMaps* maps, const void* q_nope, const void* ckv_cache
                           8 / kTcCluster, kv_fp8);
 }
 
+// The CTA-pair kernel's tensor maps: the query of 64 heads per box (one per
+// CTA of the pair), K panels of one page, V chunks of four 64-dim panels.
+bool mla::encode_pair_maps(PairMaps* maps, const void* q_nope, const void* q_pe, const void* ckv_cache,
+                           const void* kpe_cache, int batch, int num_heads, int page_size, int num_pages) {
+  const uint64_t qrows = static_cast<uint64_t>(batch) * num_heads;
+  const uint64_t kvrows = static_cast<uint64_t>(num_pages) * page_size;
+  const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return encode_2d(&maps->q_nope, q_nope, bf, 2, qrows, kDCkv, 64, 64) &&
+         encode_2d(&maps->q_pe, q_pe, bf, 2, qrows, kDKpe, 64, 64) &&
+         encode_2d(&maps->ckv_k, ckv_cache, bf, 2, kvrows, kDCkv, page_size, 64) &&
+         encode_2d(&maps->kpe_k, kpe_cache, bf, 2, kvrows, kDKpe, page_size, 64) &&
+         encode_panels_3d(&maps->ckv_v, ckv_cache, kvrows, page_size >= kTcVChunkTok ? kTcVChunkTok : 16, 4);
+}
+
 extern "C" {
 
 const char* mla_status_string(mla_status_t s) {
@@ -206,14 +220,14 @@ mla_status_t mla_plan_create(int max_batch, int num_heads, int kernel, mla_plan_
   *out = nullptr;
   if (max_batch < 1 || num_heads < 1 || num_heads > kMaxHeads) return MLA_ERR_INVALID_ARG;
   if (kernel != MLA_KERNEL_DEFAULT && kernel != MLA_KERNEL_TCGEN05 &&
-      kernel != MLA_KERNEL_MMA_SYNC)
+      kernel != MLA_KERNEL_MMA_SYNC && kernel != MLA_KERNEL_PAIR)
     return MLA_ERR_INVALID_ARG;
   mla_plan_t p = new (std::nothrow) mla_plan_s();
   if (!p) return MLA_ERR_CUDA;
   p->max_batch = max_batch;
   p->num_heads = num_heads;
   p->kernel = kernel == MLA_KERNEL_DEFAULT ? MLA_KERNEL_TCGEN05 : kernel;
-  p->tile_tokens = p->kernel == MLA_KERNEL_MMA_SYNC ? kTileMma : kTileTc;
+  p->tile_tokens = p->kernel == MLA_KERNEL_MMA_SYNC ? kTileMma : p->kernel == MLA_KERNEL_PAIR ? kTilePair : kTileTc;
   cudaError_t e = cudaGetDevice(&p->device);
   if (e == cudaSuccess)
     e = cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
@@ -223,9 +237,11 @@ mla_status_t mla_plan_create(int max_batch, int num_heads, int kernel, mla_plan_
     return MLA_ERR_CUDA;
   }
   p->n_workers = workers_for(p->kernel, p->num_sms, num_heads);
-  if (p->kernel == MLA_KERNEL_TCGEN05) {
+  if (p->kernel == MLA_KERNEL_TCGEN05 || p->kernel == MLA_KERNEL_PAIR) {
     int resident = 0;
-    if ((e = decode_tc_max_workers(&resident)) != cudaSuccess || resident < 1) {
+    if ((e = p->kernel == MLA_KERNEL_PAIR ? decode_pair_max_workers(&resident) : decode_tc_max_workers(&resident)) !=
+            cudaSuccess ||
+        resident < 1) {
       delete p;
       cudaGetLastError();
       return MLA_ERR_CUDA;
@@ -439,6 +455,15 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
     return cuda_fail(plan, e, "cudaEventRecord");
   if (plan->kernel == MLA_KERNEL_MMA_SYNC) {
     e = launch_decode_mma(a, fp8, out_f32, s);
+  } else if (plan->kernel == MLA_KERNEL_PAIR) {
+    if (fp8)
+      return fail(plan, MLA_ERR_UNSUPPORTED,
+                  "the CTA-pair kernel takes bf16 caches; use MLA_KERNEL_TCGEN05 for fp8");
+    PairMaps maps;
+    if (!encode_pair_maps(&maps, q_nope, q_pe, ckv_cache, kpe_cache, plan->params.batch, plan->num_heads,
+                          plan->params.page_size, num_pages))
+      return fail(plan, MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    e = launch_decode_pair(a, maps, out_f32, s);
   } else {
     if (fp8 && plan->params.page_size < kTcVChunkTok)
       return fail(plan, MLA_ERR_UNSUPPORTED,
@@ -453,8 +478,9 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
   if (plan->prof_stop && (e = cudaEventRecord(plan->prof_stop, s)) != cudaSuccess)
     return cuda_fail(plan, e, "cudaEventRecord");
 
-  // The tcgen05 kernel combines split requests and fills empty ones itself.
-  if (plan->kernel != MLA_KERNEL_MMA_SYNC) return MLA_OK;
+  // The one-CTA tcgen05 kernel combines split requests and fills empty ones
+  // itself; after the others a merge kernel does it.
+  if (plan->kernel == MLA_KERNEL_TCGEN05) return MLA_OK;
   MergeArgs m{};
   m.merge = reinterpret_cast<const MergeEntry*>(blob + plan->off_merge);
   m.params = a.params;

@@ -16,6 +16,7 @@ constexpr int kMaxHeads = 128;
 // request may be partially filled).
 constexpr int kTileMma = 64;        // mma.sync kernel: 64-token tiles
 constexpr int kTileTc = 128;        // tcgen05 kernel: 128-token tiles
+constexpr int kTilePair = 256;      // CTA-pair tcgen05 kernel: 256-token tiles
 
 // One contiguous token range of one request, processed by one worker.
 struct WorkUnit {

@@ -234,7 +234,8 @@ extern "C" mla_status_t mla_plan_partition_host(
                                         head_dim_kpe, page_size, sm_scale, &why);
   if (st != MLA_OK) return st;
   if (num_workers < 1 || !units || !worker_ptr || !merge || !counts) return MLA_ERR_INVALID_ARG;
-  if (tile_tokens != mla::kTileMma && tile_tokens != mla::kTileTc) return MLA_ERR_UNSUPPORTED;
+  if (tile_tokens != mla::kTileMma && tile_tokens != mla::kTileTc && tile_tokens != mla::kTilePair)
+    return MLA_ERR_UNSUPPORTED;
   mla::Partition p;
   mla::partition_batch(kv_indptr_host, kv_len_host, batch, num_workers, tile_tokens, &p);
   if (static_cast<int>(p.units.size()) > units_cap || static_cast<int>(p.merge.size()) > merge_cap)

@@ -26,8 +26,9 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_CAPACITY, ERR_CUDA, ERR_DEVICE_TIMEOUT
 # mla_dtype_t
 DTYPE_BF16, DTYPE_FP8_E4M3, DTYPE_FP32 = 0, 1, 2
 # mla_kernel_t
-KERNEL_DEFAULT, KERNEL_TCGEN05, KERNEL_MMA_SYNC = 0, 1, 2
-KERNELS = {"default": KERNEL_DEFAULT, "tcgen05": KERNEL_TCGEN05, "mma_sync": KERNEL_MMA_SYNC}
+KERNEL_DEFAULT, KERNEL_TCGEN05, KERNEL_MMA_SYNC, KERNEL_PAIR = 0, 1, 2, 3
+KERNELS = {"default": KERNEL_DEFAULT, "tcgen05": KERNEL_TCGEN05, "mma_sync": KERNEL_MMA_SYNC,
+           "pair": KERNEL_PAIR}
 
 EXPORTED = ("mla_plan_create", "mla_decode_plan", "mla_decode_run", "mla_decode_run_host",
             "mla_plan_check_status", "mla_plan_info", "mla_plan_destroy", "mla_status_string",

@@ -69,7 +69,7 @@ def test_merge_states_in_place():
     assert torch.equal(a, ref[0]) and torch.equal(la, ref[1])
 
 
-@pytest.mark.parametrize("kernel", ["tcgen05", "mma_sync"])
+@pytest.mark.parametrize("kernel", ["pair", "tcgen05", "mma_sync"])
 @pytest.mark.parametrize("prefix_pages, suffix, heads, P", [
     (5, [37, 0, 200, 64], 16, 16),        # a request without a suffix of its own
     (40, [700, 1300, 5], 128, 64),        # a long shared prefix, 128 heads

@@ -13,7 +13,7 @@ from paged_mla_decode_02_gb300 import mla
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ["tcgen05", "mma_sync"]
+KERNELS = ["pair", "tcgen05", "mma_sync"]
 
 
 def _run_multi(x, d, kernel, out_dtype=torch.float32):

@@ -20,7 +20,7 @@ from paged_mla_decode_02_gb300 import mla
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ["tcgen05", "mma_sync"]
+KERNELS = ["pair", "tcgen05", "mma_sync"]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -249,6 +249,8 @@ def test_bad_arguments_are_errors():
 def test_full_size_config(kernel, cfg):
     # the launch configuration the bench times (the same plan over the whole
     # batch), every output element against the oracle
+    if kernel == "pair" and cfg == "fp8":
+        pytest.skip("the CTA-pair kernel takes bf16 caches (fp8 runs on the one-CTA kernel)")
     x = _config(cfg)
     d = to_device(x)
     out, lse = run_decode(x, d, kernel, torch.float32)

@@ -19,7 +19,7 @@ from paged_mla_decode_02_gb300 import mla
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ["tcgen05", "mma_sync"]
+KERNELS = ["pair", "tcgen05", "mma_sync"]
 GAPS = [40.0, 60.0, 100.0, 200.0]
 
 
@@ -77,4 +77,6 @@ def test_dominant_token_in_split_requests(kernel, gap):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_dominant_token_fp8_cache(kernel):
+    if kernel == "pair":
+        pytest.skip("the CTA-pair kernel takes bf16 caches")
     _check(_batch(100.0, 128, "fp8_e4m3"), kernel, "fp8 gap 100")
