@@ -59,8 +59,9 @@ typedef enum {
 } mla_dtype_t;
 
 typedef enum {
-  MLA_KERNEL_DEFAULT = 0,     /* the tcgen05 / TMEM kernel */
-  MLA_KERNEL_TCGEN05 = 1,     /* same as DEFAULT, named explicitly */
+  MLA_KERNEL_DEFAULT = 0,     /* MLA_KERNEL_PAIR for bf16 caches; an fp8 cache runs on the
+                                 tcgen05 kernel over the same plan */
+  MLA_KERNEL_TCGEN05 = 1,     /* one-CTA tcgen05 / TMEM kernel (bf16 and fp8 caches) */
   MLA_KERNEL_MMA_SYNC = 2,    /* warp-level mma.sync kernel (legacy tensor path, for comparison) */
   MLA_KERNEL_PAIR = 3         /* tcgen05 kernel whose MMAs span a CTA pair (cta_group::2); bf16 caches */
 } mla_kernel_t;
@@ -76,7 +77,7 @@ typedef struct {
   int32_t batch;
   int32_t num_heads;
   int32_t page_size;
-  int32_t kernel;             /* mla_kernel_t actually used */
+  int32_t kernel;             /* mla_kernel_t the partition is made for (DEFAULT: PAIR) */
   int32_t tile_tokens;        /* token granularity of the split (128 tcgen05, 64 mma.sync) */
   int64_t workspace_bytes;    /* device bytes owned by the plan */
 } mla_plan_info_t;
@@ -157,13 +158,15 @@ mla_status_t mla_decode_plan_multi(mla_plan_t plan, const int32_t* kv_indptr_hos
  * An FP8_E4M3 cache runs on the tcgen05 kernel with page_size 32 or 64 (each
  * copied tile is expanded to bf16 in shared memory; every e4m3 value is exact
  * in bf16), and on the mma.sync kernel with any page size; with the tcgen05
- * kernel and 16-token pages the call returns MLA_ERR_UNSUPPORTED.
+ * kernel and 16-token pages the call returns MLA_ERR_UNSUPPORTED.  A plan of
+ * MLA_KERNEL_PAIR returns MLA_ERR_UNSUPPORTED for an fp8 cache; a plan of
+ * MLA_KERNEL_DEFAULT runs it on the tcgen05 kernel.
  *   out       [batch, num_heads, 512]   out_dtype (BF16 or FP32)
  *   lse       [batch, num_heads]        fp32, natural log
  * Launches the decode kernel; with the tcgen05 kernel that is the only launch
  * (a request split across workers is combined by log-sum-exp in the epilogue
  * of its last-finishing unit, requests with kv_len 0 are filled by the same
- * kernel), with the mma.sync kernel a merge kernel follows.  The combination
+ * kernel), with the CTA-pair and mma.sync kernels a merge kernel follows.  The combination
  * order is fixed, so repeated runs give bit-identical results.
  * No allocation, no synchronisation, no host reads: capturable in a
  * CUDA graph (the graph keeps the pointers; re-planning with the same plan
@@ -304,8 +307,9 @@ mla_status_t mla_plan_check_status(mla_plan_t plan);
  * Profiling hook: when set (non-NULL cudaEvent_t handles created by the
  * caller on the plan's device), every mla_decode_run records start_event on
  * its stream immediately before the decode kernel and stop_event immediately
- * after it (before the mma.sync path's merge kernel), so the caller can time the decode
- * kernel alone with cudaEventElapsedTime.  Pass NULLs to stop recording.
+ * after it (before the merge kernel of the CTA-pair and mma.sync paths), so
+ * the caller can time the decode kernel alone with cudaEventElapsedTime.
+ * Pass NULLs to stop recording.
  * The events are borrowed; they must outlive the runs that record them.
  */
 mla_status_t mla_plan_set_profile_events(mla_plan_t plan, void* start_event, void* stop_event);

@@ -27,7 +27,8 @@ struct mla_plan_s {
   int num_sms = 0;
   int max_batch = 0;
   int num_heads = 0;
-  int kernel = MLA_KERNEL_TCGEN05;
+  int kernel = MLA_KERNEL_TCGEN05;   // the kernel the plan's partition is made for
+  int kernel_requested = MLA_KERNEL_DEFAULT;
   int tile_tokens = kTileTc;
   int n_workers = 0;
   int units_cap = 0;
@@ -226,7 +227,11 @@ mla_status_t mla_plan_create(int max_batch, int num_heads, int kernel, mla_plan_
   if (!p) return MLA_ERR_CUDA;
   p->max_batch = max_batch;
   p->num_heads = num_heads;
-  p->kernel = kernel == MLA_KERNEL_DEFAULT ? MLA_KERNEL_TCGEN05 : kernel;
+  // DEFAULT: the CTA-pair kernel for bf16 caches; fp8 caches run on the
+  // one-CTA tcgen05 kernel over the same partition (its 256-token unit
+  // boundaries are also 128-token tile boundaries)
+  p->kernel_requested = kernel;
+  p->kernel = kernel == MLA_KERNEL_DEFAULT ? MLA_KERNEL_PAIR : kernel;
   p->tile_tokens = p->kernel == MLA_KERNEL_MMA_SYNC ? kTileMma : p->kernel == MLA_KERNEL_PAIR ? kTilePair : kTileTc;
   cudaError_t e = cudaGetDevice(&p->device);
   if (e == cudaSuccess)
@@ -247,6 +252,16 @@ mla_status_t mla_plan_create(int max_batch, int num_heads, int kernel, mla_plan_
       return MLA_ERR_CUDA;
     }
     if (resident < p->n_workers) p->n_workers = resident;
+    // the tcgen05 kernel merges split requests in place, waiting on the
+    // other workers: all of them must be resident at once
+    if (kernel == MLA_KERNEL_DEFAULT) {
+      if ((e = decode_tc_max_workers(&resident)) != cudaSuccess || resident < 1) {
+        delete p;
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+      }
+      if (resident < p->n_workers) p->n_workers = resident;
+    }
   }
   p->units_cap = max_units(p->n_workers, max_batch);
   p->slots_cap = max_slots(p->n_workers, max_batch);
@@ -453,9 +468,10 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
   cudaError_t e;
   if (plan->prof_start && (e = cudaEventRecord(plan->prof_start, s)) != cudaSuccess)
     return cuda_fail(plan, e, "cudaEventRecord");
-  if (plan->kernel == MLA_KERNEL_MMA_SYNC) {
+  const int kern = fp8 && plan->kernel_requested == MLA_KERNEL_DEFAULT ? MLA_KERNEL_TCGEN05 : plan->kernel;
+  if (kern == MLA_KERNEL_MMA_SYNC) {
     e = launch_decode_mma(a, fp8, out_f32, s);
-  } else if (plan->kernel == MLA_KERNEL_PAIR) {
+  } else if (kern == MLA_KERNEL_PAIR) {
     if (fp8)
       return fail(plan, MLA_ERR_UNSUPPORTED,
                   "the CTA-pair kernel takes bf16 caches; use MLA_KERNEL_TCGEN05 for fp8");
@@ -480,7 +496,7 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
 
   // The one-CTA tcgen05 kernel combines split requests and fills empty ones
   // itself; after the others a merge kernel does it.
-  if (plan->kernel == MLA_KERNEL_TCGEN05) return MLA_OK;
+  if (kern == MLA_KERNEL_TCGEN05) return MLA_OK;
   MergeArgs m{};
   m.merge = reinterpret_cast<const MergeEntry*>(blob + plan->off_merge);
   m.params = a.params;

@@ -1,5 +1,5 @@
 // Paged MLA decode on a CTA pair: one tcgen05 MMA spans both SMs of a
-// cluster (cta_group::2).
+// cluster (cta_group::2), and the two SMs split the heads.
 //
 // Operation (absorbed multi-head latent attention, one query token, one
 // latent KV head of width 512 + 64, no causal mask -- "[WIP] support
@@ -8,39 +8,39 @@
 //   S   = sm_scale * (q_nope[b,h] . ckv_t + q_pe[b,h] . kpe_t)
 //   out = softmax(S) . ckv,   lse = ln sum exp(S).
 //
-// Both products are computed transposed, with the tokens or the latent dims
-// as the MMA's M = 256 rows split over the two SMs:
-//   S^T [256 tokens x 128 heads]  = K [256 tokens x 576] . Q^T         (QK)
-//   O^T [512 dims x 128 heads]   += V^T [512 dims x 256 tokens] . P^T (PV, two MMAs of M = 256)
-// For QK, CTA r holds the K rows of tokens [128 r, 128 r + 128) of each
-// 256-token tile and the query of heads [64 r, 64 r + 64) (the B operand is
-// split by N); it receives S^T of its own tokens for all heads.  For PV, CTA
-// r holds V and O^T for latent dims [256 r, 256 r + 256) and P^T of heads
-// [64 r, 64 r + 64).  So every score is computed once, the query is stored
-// once per pair, and the only data the pair exchanges per tile are the
-// per-head maxima and the half of P^T whose heads the other CTA holds
-// (16 KB each way per 256 tokens).
+// Both products are pair MMAs of M = 128 heads, each CTA holding 64 of them:
+//   S [128 heads x 256 tokens]  = Q [128 x 576] . K^T            (QK, N = 256)
+//   O [128 heads x 512 dims]   += P [128 x 256 tokens] . V        (PV, two MMAs of N = 256)
+// CTA r supplies the rows of heads [64 r, 64 r + 64) of A (the query, then
+// P) and half the N rows of B: for QK the K rows of tokens
+// [128 r, 128 r + 128) of each 256-token tile, for PV the V columns of latent
+// dims [256 r, 256 r + 256).  It receives the D rows of its own 64 heads,
+// all N columns: TMEM lane l < 64 holds head 64 r + l over columns
+// [0, N/2), lane 64 + l the same head over [N/2, N).  So every score and
+// every output element of a head lands in one SM: the softmax of a head
+// never leaves its CTA.  The pair exchanges only two signals per tile: "the
+// scores were read" (the issuer may overwrite the S buffer) and "P is
+// written" (the issuer may start P . V).
 //
-// Per CTA: warp 0 producer (TMA: the query once per unit, then K panels and
-// V chunks in exactly the order the MMAs consume them, through one ring of
-// 16 KB slots); warp 1 allocates TMEM and, in the even CTA, issues every MMA
-// of the pair (QK of tile g + 1, then PV of tile g, so the softmax of a tile
-// overlaps the next tile's scores); in the odd CTA it relays "P^T complete"
-// to the issuer; warps 2..9 softmax and epilogue (two warps per TMEM lane
-// quadrant, each owning 64 heads).
+// Per CTA: warp 0 K producer (the query once per unit, then the K panels of
+// every tile through a ring of 16 KB slots), warp 10 V producer (32-token V
+// chunks through a second ring); in the even CTA warp 1 issues every QK MMA
+// of the pair and warp 11 every PV MMA, so the softmax of tile g overlaps
+// the scores of tile g + 1 and the P . V of tile g - 1; warps 2..9 softmax
+// and epilogue: warp w reads TMEM lane quadrant w % 4 and column half
+// (w - 2) / 4, so each thread owns one head and 64 tokens of a tile, and the
+// four threads of a head combine their maxima through shared memory.
 //
-// TMEM columns: S^T double-buffered [0, 128) and [128, 256); O^T [256, 512)
-// (dims [256 r, 256 r + 128) then [256 r + 128, 256 r + 256), columns =
-// heads).
+// TMEM columns: S double-buffered [0, 128) and [128, 256); O [256, 512)
+// (lane l < 64: dims [0, 256) of head 64 r + l; lane 64 + l: dims [256, 512)).
 //
-// Softmax, per tile and head: the exact maximum over the tile's 256 tokens
-// (warp butterfly, four lane quadrants, then the other CTA), a reference
-// that moves only when that maximum exceeds it by more than 2^8 (then O^T
-// and the running sums are rescaled), p = 2^(s log2e sm_scale - reference)
-// rounded to bf16 for the MMA; the row sums are kept twice, exact and of the
-// rounded p (the output is divided by the latter, the lse uses the former).
-// Both CTAs derive every reference from the same values in the same order,
-// so they agree bit for bit.
+// Softmax, per tile and head: the exact maximum over the tile's 256 tokens,
+// a reference that moves only when that maximum exceeds it by more than 2^8
+// (then O and the running sums are scaled by 2^(old - new) < 1), p =
+// 2^(s log2e sm_scale - reference) rounded to bf16 for the MMA.  The row sums
+// are kept twice per thread, exact and of the rounded p, and added over the
+// four threads of a head at the end (the output is divided by the latter,
+// the lse uses the former).
 //
 // Every wait is bounded (2 s); on expiry the kernel records
 // MLA_ERR_DEVICE_TIMEOUT, lets its copies and MMAs land, frees TMEM and
@@ -58,19 +58,21 @@ namespace {
 using namespace tc;
 
 #ifdef MLA_STALL_TEST
-// Test build only: when nonzero, CTA 0's producer leaves out its
+// Test build only: when nonzero, CTA 0's V producer leaves out its
 // g_pair_stall-th ring copy (1-based), so the issuer's wait for it runs out.
 __device__ int g_pair_stall;
 #endif
 
 constexpr int kT = kTilePair;              // 256 tokens per tile
-constexpr int kHalfT = kT / 2;             // tokens per CTA for the scores
+constexpr int kHalfT = kT / 2;             // K rows per CTA
 constexpr int kThreads = 384;              // 12 warps
 constexpr int kFirstSoftmaxWarp = 2;
+constexpr int kSoftmaxWarps = 8;
 constexpr int kVProducerWarp = 10;
 constexpr int kPvIssuerWarp = 11;
-constexpr int kKSlots = 4, kVSlots = 3;    // rings of 16 KB slots
-constexpr int kPBufs = 1;                  // P^T buffers (2: by tile parity)
+constexpr int kKSlots = 4, kVSlots = 3;    // ring slots
+constexpr int kPBufs = 1;                  // P buffers (2: by tile parity)
+constexpr bool kStreamQ = false;           // query panels ride in the K slots instead of staying resident
 constexpr int kSlotBytes = 16384;
 constexpr int kVChunkTok = kTcVChunkTok;   // 32 tokens per V chunk
 constexpr int kChunksPerTile = kT / kVChunkTok;
@@ -84,15 +86,15 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units: p stays below 2^8
 // shared memory (offsets from the 1024-byte aligned base)
 constexpr int kOffQ = 0;                          // 9 panels x (64 heads x 128 B)
 constexpr int kQPanel = 64 * 128;
-constexpr int kOffP = kOffQ + 9 * kQPanel;        // P^T: 256 token rows x 128 B (64 heads)
-constexpr int kPBuf = kT * 128;            // one P^T buffer: 32 KB
+constexpr int kKSlotBytes = kSlotBytes + (kStreamQ ? kQPanel : 0);   // K panel (+ the query panel)
+constexpr int kOffP = kOffQ + (kStreamQ ? 0 : 9 * kQPanel);         // P: 4 token panels x (64 heads x 128 B)
+constexpr int kPPanel = 64 * 128;
+constexpr int kPBuf = 4 * kPPanel;                // one P buffer: 32 KB
 constexpr int kOffKRing = kOffP + kPBufs * kPBuf;
-constexpr int kOffVRing = kOffKRing + kKSlots * kSlotBytes;
-constexpr int kOffRed = kOffVRing + kVSlots * kSlotBytes;  // [4 quadrants][2 halves][32 lanes] float4
-constexpr int kOffX = kOffRed + 4 * 2 * 32 * 16;          // peer maxima [2 parities][2 halves][32 lanes] float2
-constexpr int kOffXs = kOffX + 2 * 2 * 32 * 8;            // peer sums [2 halves][32 lanes] float4
-constexpr int kOffRef = kOffXs + 2 * 32 * 16;             // ref[128], alpha[128], inv[128], lse[128]
-constexpr int kOffFlags = kOffRef + 4 * 128 * 4;          // abort, tmem slot, rescale flags
+constexpr int kOffVRing = kOffKRing + kKSlots * kKSlotBytes;
+constexpr int kOffRed = kOffVRing + kVSlots * kSlotBytes;  // maxima [2 parities][4 parts][64 heads] float
+constexpr int kOffSum = kOffRed + 2 * 4 * 64 * 4;          // sums [4 parts][64 heads] float2
+constexpr int kOffFlags = kOffSum + 4 * 64 * 8;           // abort, tmem slot
 constexpr int kOffBar = kOffFlags + 64;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOffKRing % 1024 == 0 && kOffVRing % 1024 == 0,
               "swizzle atoms");
@@ -104,16 +106,13 @@ enum Bar {
   kVEmpty0 = kVFull0 + kVSlots,  // [kVSlots] both
   kQFull = kVEmpty0 + kVSlots,   // even CTA: both query halves loaded (1 arrival + bytes)
   kQFree,                        // both: the unit's last QK completed
-  kSFull0,                       // [2] both: S^T buffer written
-  kSFree0 = kSFull0 + 2,         // [2] even CTA: S^T buffer read by all 16 softmax warps
+  kSFull0,                       // [2] both: S buffer written
+  kSFree0 = kSFull0 + 2,         // [2] even CTA: S buffer read by all 16 softmax warps
   kPvDone0 = kSFree0 + 2,        // [2] by tile parity, both: the tile's PV completed
-  kPIn0 = kPvDone0 + 2,          // [2] by tile parity, both: this CTA's P^T rows complete (8 warps + 16 KB from the peer)
-  kPeerReady0 = kPIn0 + 2,       // [2] by tile parity, even CTA: the odd CTA's kPIn completed
-  kOFree = kPeerReady0 + 2,                        // even CTA: both epilogues read O^T (16 arrivals)
-  kRed0,                         // [2] both: per head half, the four quadrant warps posted
-  kX0 = kRed0 + 2,               // [2 parities][2 halves] both: the peer's maxima landed
-  kXs0 = kX0 + 4,                // [2] both: the peer's sums landed
-  kRef = kXs0 + 2,               // both: references (or lse / 1/l) written by both combining warps
+  kPReady0 = kPvDone0 + 2,       // [2] by tile parity, even CTA: P written by all 16 softmax warps
+  kOFree = kPReady0 + 2,         // even CTA: both epilogues read O (16 arrivals)
+  kRed0,                         // [2] by tile parity, both: the 8 softmax warps posted their maxima
+  kSum = kRed0 + 2,              // both: the 8 softmax warps posted their sums
   kTail,                         // both: producer-local copy of a partial V chunk
   kTailReady,                    // even CTA: both CTAs zeroed the rows past the end of a partial V chunk
   kFinal,                        // even CTA: every QK MMA completed
@@ -127,31 +126,15 @@ __device__ __forceinline__ uint32_t bar(uint32_t base, int i) { return base + kO
 
 __device__ __forceinline__ int tiles_of(const WorkUnit& u) { return (u.tok_end - u.tok_begin + kT - 1) / kT; }
 
-// Reduce-scatter over the 32 lanes of a warp: v[64] holds one value per head
-// (heads 0..63 of this lane's token); afterwards lane l holds the reduction
-// over the warp of heads 2l and 2l + 1.  Step k (lane bit 4 - k) halves the
-// live values: the lane keeps the half its bit selects and adds the partner's
-// copy of it.
-template <int kCnt, int kMask, bool kMax>
-__device__ __forceinline__ void scatter_step(float (&v)[64], int lane) {
-  constexpr int kHalf = kCnt / 2;
-  const bool upper = (lane & kMask) != 0;
-#pragma unroll
-  for (int i = 0; i < kHalf; ++i) {
-    const float keep = upper ? v[i + kHalf] : v[i];
-    const float send = upper ? v[i] : v[i + kHalf];
-    const float got = __shfl_xor_sync(0xffffffffu, send, kMask);
-    v[i] = kMax ? fmaxf(keep, got) : keep + got;
-  }
-}
-template <bool kMax>
-__device__ __forceinline__ float2 warp_scatter(float (&v)[64], int lane) {
-  scatter_step<64, 16, kMax>(v, lane);
-  scatter_step<32, 8, kMax>(v, lane);
-  scatter_step<16, 4, kMax>(v, lane);
-  scatter_step<8, 2, kMax>(v, lane);
-  scatter_step<4, 1, kMax>(v, lane);
-  return make_float2(v[0], v[1]);
+// Arrive on a barrier of the even CTA (from the odd CTA through the cluster
+// window).  What the signal publishes lives in the arriving CTA: its reads of
+// S or O from its own TMEM are complete, or its P rows are written and fenced
+// for the tensor core of its own SM.
+__device__ __forceinline__ void arrive_lead(uint32_t local_bar, int rank) {
+  if (rank == 0)
+    mbar_arrive(local_bar);
+  else
+    mbar_arrive_remote(map_to_rank(local_bar, 0));
 }
 
 template <bool kOutF32>
@@ -163,33 +146,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = smem_u32(sm);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffFlags);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffFlags + 4);
-  volatile int* resc = reinterpret_cast<volatile int*>(sm + kOffFlags + 8);   // [2] rescale flags
-  float* ref_s = reinterpret_cast<float*>(sm + kOffRef);
-  float* alpha_s = ref_s + 128;
-  float* inv_s = ref_s + 256;
-  float* lse_s = ref_s + 384;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int worker = blockIdx.x >> 1;
   const int rank = static_cast<int>(cluster_ctarank());
-  const int peer = rank ^ 1;
   const PlanDev prm = *a.params;
   const int H = a.num_heads;
   const int P = prm.page_size;
   const int u0 = worker < prm.n_workers ? a.worker_ptr[worker] : 0;
   const int u1 = worker < prm.n_workers ? a.worker_ptr[worker + 1] : 0;
-  int n_tiles = 0;   // this worker's tiles over all its units
-  for (int ui = u0; ui < u1; ++ui) n_tiles += tiles_of(a.units[ui]);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
       if (i == kTailReady) cnt = 2;
-      if (i == kSFree0 || i == kSFree0 + 1 || i == kOFree) cnt = 16;
-      if (i == kPIn0 || i == kPIn0 + 1) cnt = 8;
-      if (i == kRed0 || i == kRed0 + 1) cnt = 4;
-      if (i == kRef) cnt = 2;
+      if (i == kSFree0 || i == kSFree0 + 1 || i == kPReady0 || i == kPReady0 + 1 || i == kOFree)
+        cnt = 2 * kSoftmaxWarps;
+      if (i == kRed0 || i == kRed0 + 1 || i == kSum) cnt = kSoftmaxWarps;
       mbar_init(bar(base, i), cnt);
     }
     fence_barrier_init();
@@ -213,12 +187,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= producers (both CTAs) =================
     // Warp 0 loads the query (once per unit) and the K panels of every tile
     // into the K ring; warp 10 loads the V chunks into the V ring.  The two
-    // streams (K mostly from DRAM, V mostly from L2, where the other CTA's K
-    // copies of the same tokens left it) run concurrently.  Each copy of
-    // both CTAs completes on the even CTA's full barrier of its slot, where
-    // the even CTA's producer announces the bytes of both (the odd CTA only
-    // issues its copies: an arrive at cluster scope per slot would cost a
-    // fence each).
+    // streams (K mostly from DRAM, V mostly from L2, where the K copies of
+    // the same tokens left it) run concurrently.  Each copy of both CTAs
+    // completes on the even CTA's full barrier of its slot, where the even
+    // CTA's producer announces the bytes of both (the odd CTA only issues
+    // its copies: an arrive at cluster scope per slot would cost a fence
+    // each).
     const bool is_k = warp == 0;
     int rp = 0;            // slots of this ring used so far
     int tail_uses = 0;
@@ -226,8 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int q_units = 0;       // query loads issued
     const int vbox = P >= kVChunkTok ? kVChunkTok : 16;
     const int nslots = is_k ? kKSlots : kVSlots;
-    const int full0 = is_k ? kKFull0 : kVFull0, empty0 = is_k ? kKEmpty0 : kVEmpty0;
-    const int ring = is_k ? kOffKRing : kOffVRing;
+    const int empty0 = is_k ? kKEmpty0 : kVEmpty0;
     auto next_slot = [&](int& slot) -> bool {
       slot = rp % nslots;
       const uint32_t par = ((rp / nslots) & 1) ^ 1;
@@ -281,14 +254,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         int slot;
         if (!(ok = next_slot(slot))) return false;
         const uint32_t full = map_to_rank(bar(base, kKFull0 + slot), lead);
-        if (lane == 0 && rank == 0) mbar_arrive_expect_tx(bar(base, kKFull0 + slot), nbox_both * P * 128);
+        if (lane == 0 && rank == 0)
+          mbar_arrive_expect_tx(bar(base, kKFull0 + slot), nbox_both * P * 128 + (kStreamQ ? 2 * kQPanel : 0));
         __syncwarp();
+        const uint32_t sbase = base + kOffKRing + slot * kKSlotBytes;
         if (lane < nbox) {
-          const uint32_t dst = base + kOffKRing + slot * kSlotBytes + lane * P * 128;
+          const uint32_t dst = sbase + lane * P * 128;
           if (j < 8)
             tma_load_2d_pair(dst, &maps.ckv_k, 64 * j, page * P, full);
           else
             tma_load_2d_pair(dst, &maps.kpe_k, 0, page * P, full);
+        } else if (kStreamQ && lane == 31) {
+          // this CTA's 64 query heads, dims [64 j, 64 j + 64) (rows past the
+          // batch are zero-filled)
+          const int row = v.req * H + 64 * rank;
+          if (j < 8)
+            tma_load_2d_pair(sbase + kSlotBytes, &maps.q_nope, 64 * j, row, full);
+          else
+            tma_load_2d_pair(sbase + kSlotBytes, &maps.q_pe, 0, row, full);
         }
       }
       return true;
@@ -335,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = mbar_wait_cl_warp(bar(base, kTailReady), tail_uses & 1, abort_flag))) return false;
             if (lane == 0) mbar_arrive(bar(base, kVFull0 + slot));
           } else if (lane == 0) {
-            mbar_arrive_cluster(map_to_rank(bar(base, kTailReady), lead));
+            mbar_arrive_remote(map_to_rank(bar(base, kTailReady), lead));
           }
           ++tail_uses;
         }
@@ -348,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n && ok; ++i) {
         const int pages = tile_pages(v, i);
         if (is_k) {
-          if (i == 0 && !emit_q(v)) break;
+          if (!kStreamQ && i == 0 && !emit_q(v)) break;
           if (!emit_k(v, i, pages)) break;
         } else if (!emit_v(v, i, pages)) {
           break;
@@ -360,20 +343,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================= MMA issuers (even CTA, whole warp, lane 0 issues) =================
     // Warp 1 issues the QK products of every tile, panel by panel from the K
     // ring; warp 11 the PV products, chunk by chunk from the V ring, once
-    // the tile's P^T is complete in both CTAs.  Two issuers, because an
-    // issuing thread cannot run ahead of the tensor pipe: the waits and
-    // commits of one overlap the other's MMAs.
+    // the tile's P is written in both CTAs.  Two issuers, because an issuing
+    // thread cannot run ahead of the tensor pipe: the waits and commits of
+    // one overlap the other's MMAs.
     const uint32_t issue = lane == 0;
     bool ok = true;
     if (warp == 1) {
-      constexpr uint32_t id_qk = idesc_bf16_f32(256, 128, false, false);
+      constexpr uint32_t id_qk = idesc_bf16_f32(128, 256, false, false);
       const uint64_t q_desc0 = smem_desc(base + kOffQ, 16, 1024, kSw128);
       const uint64_t k_desc0 = smem_desc(base + kOffKRing, 16, 1024, kSw128);
       int kc = 0, g = 0, unit_k = 0;
       for (int ui = u0; ui < u1 && ok; ++ui, ++unit_k) {
         const WorkUnit v = a.units[ui];
         const int n = tiles_of(v);
-        if (!(ok = mbar_wait_warp(bar(base, kQFull), unit_k & 1, abort_flag))) break;
+        if (!kStreamQ && !(ok = mbar_wait_warp(bar(base, kQFull), unit_k & 1, abort_flag))) break;
         for (int i = 0; i < n && ok; ++i, ++g) {
           if (g >= 2 && !(ok = mbar_wait_cl_warp(bar(base, kSFree0 + (g & 1)), ((g - 2) >> 1) & 1, abort_flag)))
             break;
@@ -383,8 +366,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int slot = kc % kKSlots;
             if (!(ok = mbar_wait_warp(bar(base, kKFull0 + slot), (kc / kKSlots) & 1, abort_flag))) break;
             tc_fence_after();
-            const uint64_t adesc = k_desc0 + static_cast<uint64_t>((slot * kSlotBytes) >> 4);
-            const uint64_t bdesc = q_desc0 + static_cast<uint64_t>((j * kQPanel) >> 4);
+            const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((slot * kKSlotBytes) >> 4);
+            const uint64_t adesc = kStreamQ ? bdesc + static_cast<uint64_t>(kSlotBytes >> 4)
+                                            : q_desc0 + static_cast<uint64_t>((j * kQPanel) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_pair(d, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2), id_qk,
@@ -395,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           commit_pair(bar(base, kSFull0 + (g & 1)), 3, issue);
         }
         if (!ok) break;
-        commit_pair(bar(base, kQFree), 3, issue);   // the unit's query no longer read
+        if (!kStreamQ) commit_pair(bar(base, kQFree), 3, issue);   // the unit's query no longer read
       }
       if (!ok && lane == 0) report_error(a.err, kErrTimeout);
       // drain: every MMA issued completes before TMEM is freed
@@ -403,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_wait_cl_drain(bar(base, kFinal), 0);
       __syncwarp();
     } else {
-      constexpr uint32_t id_pv = idesc_bf16_f32(256, 128, true, true);
+      constexpr uint32_t id_pv = idesc_bf16_f32(128, 256, false, true);
       const uint64_t p_desc0 = smem_desc(base + kOffP, 16, 1024, kSw128);
       const bool v32 = P >= kVChunkTok;
       const uint64_t v_desc0 = smem_desc(base + kOffVRing, v32 ? 4096 : 2048, 1024, kSw128);
@@ -412,26 +396,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ui = u0; ui < u1 && ok; ++ui, ++unit_k) {
         const WorkUnit v = a.units[ui];
         const int n = tiles_of(v);
-        // the first PV of a unit overwrites O^T: the previous epilogue must be done
+        // the first PV of a unit overwrites O: the previous epilogue must be done
         if (unit_k > 0 && !(ok = mbar_wait_cl_warp(bar(base, kOFree), (unit_k - 1) & 1, abort_flag))) break;
         for (int i = 0; i < n && ok; ++i, ++g) {
-          if (!(ok = mbar_wait_warp(bar(base, kPIn0 + (g & 1)), (g >> 1) & 1, abort_flag) &&
-                     mbar_wait_cl_warp(bar(base, kPeerReady0 + (g & 1)), (g >> 1) & 1, abort_flag)))
-            break;
+          if (!(ok = mbar_wait_cl_warp(bar(base, kPReady0 + (g & 1)), (g >> 1) & 1, abort_flag))) break;
           tc_fence_after();
           const int valid = min(kT, v.tok_end - (v.tok_begin + i * kT));
           const int nch = (valid + kVChunkTok - 1) / kVChunkTok;
+          const uint32_t pbuf = (g % kPBufs) * kPBuf;
           for (int c = 0; c < nch; ++c, ++vc) {
             const int slot = vc % kVSlots;
             if (!(ok = mbar_wait_warp(bar(base, kVFull0 + slot), (vc / kVSlots) & 1, abort_flag))) break;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
-              const uint64_t bdesc = p_desc0 + static_cast<uint64_t>(
-                                                   ((kPBufs == 2 ? (g & 1) : 0) * kPBuf + (kVChunkTok * c + 16 * kk) * 128) >> 4);
+              const int t = kVChunkTok * c + 16 * kk;   // first token of the K step
+              const uint64_t adesc =
+                  p_desc0 + static_cast<uint64_t>((pbuf + (t >> 6) * kPPanel + (t & 63) * 2) >> 4);
 #pragma unroll
               for (int bb = 0; bb < 2; ++bb) {
-                const uint64_t adesc =
+                const uint64_t bdesc =
                     v_desc0 + static_cast<uint64_t>((slot * kSlotBytes + kk * v_kstep + bb * v_block) >> 4);
                 mma_pair(tmem + kColO + 128 * bb, adesc, bdesc, id_pv, (i == 0 && c == 0 && kk == 0) ? 0u : 1u,
                          issue);
@@ -448,298 +432,187 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_wait_cl_drain(bar(base, kFinalPv), 0);
       __syncwarp();
     }
-  } else if (warp == 1) {
-    // ================= relay (odd CTA): "my P^T rows are complete" =================
-    bool ok = true;
-    for (int g = 0; g < n_tiles && ok; ++g) {
-      if (!(ok = mbar_wait_warp(bar(base, kPIn0 + (g & 1)), (g >> 1) & 1, abort_flag))) break;
-      if (lane == 0) mbar_arrive_cluster(map_to_rank(bar(base, kPeerReady0 + (g & 1)), lead));
-      __syncwarp();
-    }
-    if (!ok && lane == 0) report_error(a.err, kErrTimeout);
-  } else if (warp == kPvIssuerWarp) {
+  } else if (warp == 1 || warp == kPvIssuerWarp) {
     // (odd CTA: no role)
   } else {
     // ================= softmax / epilogue (warps 2..9, both CTAs) =================
     const int sw = warp - kFirstSoftmaxWarp;
-    const int q = warp & 3;                  // TMEM lane quadrant: tokens (S^T) or dims (O^T)
-    const int hh = sw >> 2;                  // heads [64 hh, 64 hh + 64)
-    const bool combiner = q == 0;            // one warp per head half combines and exchanges
+    const int q = warp & 3;                  // TMEM lane quadrant
+    const int ch = sw >> 2;                  // S columns [64 ch, 64 ch + 64), O columns [128 ch, 128 ch + 128)
+    const int hl = 32 * (q & 1) + lane;      // head within this CTA
+    const int h = 64 * rank + hl;
+    const int tq = q >> 1;                   // S: tokens [128 tq, 128 tq + 128) of the tile; O: dims [256 tq, ..)
+    const int part = 2 * tq + ch;            // which of the head's four threads this is
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const float c = prm.sm_scale * a.kv_scale * kLog2e;
-    const int h0 = 64 * hh + 2 * lane;       // the two heads this lane reduces into
-    // P^T rows of heads [64 hh, ..) live in CTA hh
-    const bool p_local = hh == rank;
-    int nred = 0;
+    float* red = reinterpret_cast<float*>(sm + kOffRed);
+    float2* sums = reinterpret_cast<float2*>(sm + kOffSum);
     bool ok = true;
     int g = 0, unit_k = 0;
     for (int ui = u0; ui < u1 && ok; ++ui, ++unit_k) {
       const WorkUnit u = a.units[ui];
       const int n = tiles_of(u);
-      float lx0 = 0.f, lx1 = 0.f, lr0 = 0.f, lr1 = 0.f;
+      float ref = 0.f;                       // the head's reference (the same in its four threads)
+      float lx = 0.f, lr = 0.f;              // this thread's share of the row sums
       for (int i = 0; i < n && ok; ++i, ++g) {
         const bool first = i == 0;
-        // ---- scores of this lane's token, 64 heads ----
+        // ---- scores: this thread's head, 64 tokens ----
         if (!(ok = mbar_wait_warp(bar(base, kSFull0 + (g & 1)), (g >> 1) & 1, abort_flag))) break;
         tc_fence_after();
         float y[64];
+        float mx = -INFINITY;
         {
           uint32_t v0[32], v1[32];
-          tmem_ld32(lane_addr + kColS + 128 * (g & 1) + 64 * hh, v0);
-          tmem_ld32(lane_addr + kColS + 128 * (g & 1) + 64 * hh + 32, v1);
+          const uint32_t col = kColS + 128 * (g & 1) + 64 * ch;
+          tmem_ld32(lane_addr + col, v0);
+          tmem_ld32(lane_addr + col + 32, v1);
           tmem_ld_wait();
-          const int tok = u.tok_begin + i * kT + kHalfT * rank + 32 * q + lane;
-          const bool valid = tok < u.tok_end;
+          const int nvalid = u.tok_end - (u.tok_begin + i * kT + kHalfT * tq + 64 * ch);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            y[j] = valid ? __uint_as_float(v0[j]) * c : -INFINITY;
-            y[32 + j] = valid ? __uint_as_float(v1[j]) * c : -INFINITY;
+            y[j] = j < nvalid ? __uint_as_float(v0[j]) * c : -INFINITY;
+            y[32 + j] = 32 + j < nvalid ? __uint_as_float(v1[j]) * c : -INFINITY;
           }
+#pragma unroll
+          for (int j = 0; j < 64; ++j) mx = fmaxf(mx, y[j]);
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          if (rank == 0)
-            mbar_arrive(bar(base, kSFree0 + (g & 1)));
-          else
-            mbar_arrive_cluster(map_to_rank(bar(base, kSFree0 + (g & 1)), lead));
-        }
-        // ---- per-head maximum over the tile: warp, quadrants, then the peer ----
-        {
-          float t[64];
-#pragma unroll
-          for (int j = 0; j < 64; ++j) t[j] = y[j];
-          const float2 mx = warp_scatter<true>(t, lane);
-          float4* red = reinterpret_cast<float4*>(sm + kOffRed);
-          *reinterpret_cast<float2*>(red + (q * 2 + hh) * 32 + lane) = mx;
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(base, kRed0 + hh));
-          if (combiner) {
-            if (!(ok = mbar_wait_warp(bar(base, kRed0 + hh), nred & 1, abort_flag))) break;
-            float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-              const float2 o = *reinterpret_cast<const float2*>(red + (qq * 2 + hh) * 32 + lane);
-              m0 = fmaxf(m0, o.x);
-              m1 = fmaxf(m1, o.y);
-            }
-            const int xp = g & 1;
-            float2* xs = reinterpret_cast<float2*>(sm + kOffX) + (xp * 2 + hh) * 32;
-            const uint32_t xbar = bar(base, kX0 + xp * 2 + hh);
-            if (lane == 0) mbar_arrive_expect_tx(xbar, 32 * 8);
-            __syncwarp();
-            st_async_peer_v2f(map_to_rank(smem_u32(xs + lane), peer), m0, m1, map_to_rank(xbar, peer));
-            if (!(ok = mbar_wait_warp(xbar, (g >> 1) & 1, abort_flag))) break;
-            const float2 pm = xs[lane];
-            m0 = fmaxf(m0, pm.x);
-            m1 = fmaxf(m1, pm.y);
-            float r0 = ref_s[h0], r1 = ref_s[h0 + 1];
-            const float n0 = first || m0 > r0 + kRescaleThreshold ? m0 : r0;
-            const float n1 = first || m1 > r1 + kRescaleThreshold ? m1 : r1;
-            const float a0 = first ? 1.f : exp2f(r0 - n0), a1 = first ? 1.f : exp2f(r1 - n1);
-            ref_s[h0] = n0;
-            ref_s[h0 + 1] = n1;
-            alpha_s[h0] = a0;
-            alpha_s[h0 + 1] = a1;
-            const bool moved = (h0 < H && a0 != 1.f) || (h0 + 1 < H && a1 != 1.f);
-            const bool any = __any_sync(0xffffffffu, moved);
-            if (lane == 0) resc[hh] = any && !first;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(base, kRef));
-          }
-          if (!(ok = mbar_wait_warp(bar(base, kRef), nred & 1, abort_flag))) break;
-          ++nred;
+        if (lane == 0) arrive_lead(bar(base, kSFree0 + (g & 1)), rank);
+        // ---- the head's maximum over the tile (its four threads) ----
+        float* rd = red + (g & 1) * 4 * 64;
+        rd[part * 64 + hl] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(base, kRed0 + (g & 1)));
+        if (!(ok = mbar_wait_warp(bar(base, kRed0 + (g & 1)), (g >> 1) & 1, abort_flag))) break;
+        const float mt = fmaxf(fmaxf(rd[hl], rd[64 + hl]), fmaxf(rd[128 + hl], rd[192 + hl]));
+        // the reference moves up only (alpha < 1): nothing is ever scaled up
+        float alpha = 1.f;
+        if (first) {
+          ref = mt;
+        } else if (mt > ref + kRescaleThreshold) {
+          alpha = exp2f(ref - mt);
+          ref = mt;
         }
         // ---- p = 2^(y - reference), rounded to bf16; row sums ----
         uint32_t pk[32];
         {
-          float px[64], pr[64];
-#pragma unroll
-          for (int j4 = 0; j4 < 16; ++j4) {
-            const float4 m4 = reinterpret_cast<const float4*>(ref_s + 64 * hh)[j4];
-            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) px[4 * j4 + e] = fast_exp2(y[4 * j4 + e] - mm[e]);
-          }
+          float sx = 0.f, sr = 0.f;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(px[2 * j], px[2 * j + 1]);
+            const float p0 = fast_exp2(y[2 * j] - ref), p1 = fast_exp2(y[2 * j + 1] - ref);
+            const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
             const uint32_t w = *reinterpret_cast<const uint32_t*>(&b2);
             pk[j] = w;
-            pr[2 * j] = __uint_as_float(w << 16);
-            pr[2 * j + 1] = __uint_as_float(w & 0xffff0000u);
+            sx += p0 + p1;
+            sr += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
           }
-          const float2 sx = warp_scatter<false>(px, lane);
-          const float2 sr = warp_scatter<false>(pr, lane);
-          const float a0 = alpha_s[h0], a1 = alpha_s[h0 + 1];
-          lx0 = first ? sx.x : fmaf(lx0, a0, sx.x);
-          lx1 = first ? sx.y : fmaf(lx1, a1, sx.y);
-          lr0 = first ? sr.x : fmaf(lr0, a0, sr.x);
-          lr1 = first ? sr.y : fmaf(lr1, a1, sr.y);
+          lx = first ? sx : fmaf(lx, alpha, sx);
+          lr = first ? sr : fmaf(lr, alpha, sr);
         }
-        // ---- the P^T buffer free (PV of the tile that used it done); for a
-        // rescale, also the previous tile's PV (O^T current) ----
-        const bool rescale = !first && (resc[0] | resc[1]);
+        // ---- the P buffer free (PV of the tile that used it done); for a
+        // rescale, also the previous tile's PV (O current) ----
+        const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
         {
           const int tw = rescale ? g - 1 : g - kPBufs;
           if (tw >= 0 && !(ok = mbar_wait_warp(bar(base, kPvDone0 + (tw & 1)), (tw >> 1) & 1, abort_flag))) break;
-          if (rescale && kPBufs == 2 && g >= 2 &&
-              !(ok = mbar_wait_warp(bar(base, kPvDone0 + (g & 1)), ((g - 2) >> 1) & 1, abort_flag)))
-            break;
         }
         tc_fence_after();
         if (rescale) {
-          // O^T rows of this quadrant's dims, block hh: column h times alpha[h]
+          // this thread's 128 columns of O (its head), times alpha
 #pragma unroll 1
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t o[32];
-            const uint32_t col = kColO + 128 * hh + 32 * cc;
+            const uint32_t col = kColO + 128 * ch + 32 * cc;
             tmem_ld32(lane_addr + col, o);
             tmem_ld_wait();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha_s[32 * cc + j]);
+            for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
             tmem_st32(lane_addr + col, o);
           }
           tmem_st_wait();
         }
-        // ---- P^T row of this lane's token (64 heads = 128 bytes) ----
+        // ---- P row of this head over this thread's 64 tokens: one 128-byte
+        // row of token panel 2 tq + ch (K-major, 128-byte swizzle) ----
         {
-          const uint32_t p_in_self = bar(base, kPIn0 + (g & 1));
-          const uint32_t p_in_dst = p_local ? p_in_self : map_to_rank(p_in_self, peer);
-          const int row = kHalfT * rank + 32 * q + lane;
-          const int pb = kOffP + (kPBufs == 2 ? (g & 1) : 0) * kPBuf;
-          const uint32_t rowaddr = base + pb + row * 128;
-          if (p_local) {
+          unsigned char* prow = sm + kOffP + (g % kPBufs) * kPBuf + part * kPPanel + hl * 128;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-              *reinterpret_cast<uint4*>(sm + pb + row * 128 + ((ch ^ (row & 7)) << 4)) =
-                  make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            fence_proxy_async_smem();
-          } else {
-            const uint32_t rrow = map_to_rank(rowaddr, peer);
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-              st_async_peer(rrow + ((ch ^ (row & 7)) << 4),
-                            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]), p_in_dst);
-          }
+          for (int k = 0; k < 8; ++k)
+            *reinterpret_cast<uint4*>(prow + ((k ^ (hl & 7)) << 4)) =
+                make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+          fence_proxy_async_smem();
           tc_fence_before();
           __syncwarp();
-          // one local warp announces the 16 KB of rows the peer sends here
-          if (lane == 0) {
-            if (sw == 0)
-              mbar_arrive_expect_tx(p_in_self, 128 * 128);
-            else
-              mbar_arrive(p_in_self);
-          }
+          if (lane == 0) arrive_lead(bar(base, kPReady0 + (g & 1)), rank);
         }
       }
       if (!ok) break;
       // ================= epilogue of the unit =================
       {
-        float4* red = reinterpret_cast<float4*>(sm + kOffRed);
-        red[(q * 2 + hh) * 32 + lane] = make_float4(lx0, lr0, lx1, lr1);
+        sums[part * 64 + hl] = make_float2(lx, lr);
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(base, kRed0 + hh));
-        if (combiner) {
-          if (!(ok = mbar_wait_warp(bar(base, kRed0 + hh), nred & 1, abort_flag))) break;
-          float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (lane == 0) mbar_arrive(bar(base, kSum));
+        if (!(ok = mbar_wait_warp(bar(base, kSum), unit_k & 1, abort_flag))) break;
+        float sx = 0.f, sr = 0.f;
 #pragma unroll
-          for (int qq = 0; qq < 4; ++qq) {
-            const float4 o = red[(qq * 2 + hh) * 32 + lane];
-            s.x += o.x;
-            s.y += o.y;
-            s.z += o.z;
-            s.w += o.w;
-          }
-          float4* xs = reinterpret_cast<float4*>(sm + kOffXs) + hh * 32;
-          const uint32_t xbar = bar(base, kXs0 + hh);
-          if (lane == 0) mbar_arrive_expect_tx(xbar, 32 * 16);
-          __syncwarp();
-          st_async_peer(map_to_rank(smem_u32(xs + lane), peer),
-                        make_uint4(__float_as_uint(s.x), __float_as_uint(s.y), __float_as_uint(s.z),
-                                   __float_as_uint(s.w)),
-                        map_to_rank(xbar, peer));
-          if (!(ok = mbar_wait_warp(xbar, unit_k & 1, abort_flag))) break;
-          const float4 o = xs[lane];
-          const float lx_0 = s.x + o.x, lr_0 = s.y + o.y, lx_1 = s.z + o.z, lr_1 = s.w + o.w;
-          const float ls0 = (ref_s[h0] + log2f(lx_0)) * kLn2, ls1 = (ref_s[h0 + 1] + log2f(lx_1)) * kLn2;
-          lse_s[h0] = ls0;
-          lse_s[h0 + 1] = ls1;
-          inv_s[h0] = a.kv_scale / lr_0;
-          inv_s[h0 + 1] = a.kv_scale / lr_1;
-          if (rank == 0) {
-            const bool split = u.out_slot >= 0;
-            if (h0 < H) {
-              if (split) a.lse_part[lse_part_offset(u.out_slot, 0, h0, H)] = ls0;
-              else a.lse[static_cast<size_t>(u.req) * H + h0] = ls0;
-            }
-            if (h0 + 1 < H) {
-              if (split) a.lse_part[lse_part_offset(u.out_slot, 0, h0 + 1, H)] = ls1;
-              else a.lse[static_cast<size_t>(u.req) * H + h0 + 1] = ls1;
-            }
-          }
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(base, kRef));
+        for (int pp = 0; pp < 4; ++pp) {
+          const float2 s = sums[pp * 64 + hl];
+          sx += s.x;
+          sr += s.y;
         }
-        if (!(ok = mbar_wait_warp(bar(base, kRef), nred & 1, abort_flag))) break;
-        ++nred;
+        const float ls = (ref + log2f(sx)) * kLn2;
+        const float inv = a.kv_scale / sr;
+        const bool split = u.out_slot >= 0;
+        if (part == 0 && h < H) {
+          if (split)
+            a.lse_part[lse_part_offset(u.out_slot, 0, h, H)] = ls;
+          else
+            a.lse[static_cast<size_t>(u.req) * H + h] = ls;
+        }
         if (!(ok = mbar_wait_warp(bar(base, kPvDone0 + ((g - 1) & 1)), ((g - 1) >> 1) & 1, abort_flag))) break;
         tc_fence_after();
-        // O^T: this lane's latent dim, all heads of block hh
-        const int d = 256 * rank + 128 * hh + 32 * q + lane;
-        const bool split = u.out_slot >= 0;
+        // O: this thread's head, dims [256 tq + 128 ch, + 128)
+        const int d0 = kHalfT * 2 * tq + 128 * ch;
 #pragma unroll 1
         for (int cc = 0; cc < 4; ++cc) {
           uint32_t o[32];
-          tmem_ld32(lane_addr + kColO + 128 * hh + 32 * cc, o);
+          tmem_ld32(lane_addr + kColO + 128 * ch + 32 * cc, o);
           tmem_ld_wait();
-          if (split) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int h = 32 * cc + j;
-              if (h < H) a.o_part[part_offset(u.out_slot, h, d, H)] = __uint_as_float(o[j]) * inv_s[h];
-            }
-          } else if (kOutF32) {
-            float* out = static_cast<float*>(a.out);
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * inv);
+          if (h < H) {
+            const int d = d0 + 32 * cc;
+            if (split) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int h = 32 * cc + j;
-              if (h < H) out[(static_cast<size_t>(u.req) * H + h) * kDCkv + d] = __uint_as_float(o[j]) * inv_s[h];
-            }
-          } else {
-            // pairs of heads: even lanes store dims (d, d+1) of head h, odd
-            // lanes dims (d-1, d) of head h+1 (4-byte bf16x2 stores)
-            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-            const bool odd = lane & 1;
+              for (int j = 0; j < 4; ++j) st_global_v8(a.o_part + part_offset(u.out_slot, h, d + 8 * j, H), &o[8 * j]);
+            } else if (kOutF32) {
+              float* dst = static_cast<float*>(a.out) + (static_cast<size_t>(u.req) * H + h) * kDCkv + d;
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-              const int h = 32 * cc + j;
-              const float v0 = __uint_as_float(o[j]) * inv_s[h];
-              const float v1 = __uint_as_float(o[j + 1]) * inv_s[h + 1];
-              const float got = __shfl_xor_sync(0xffffffffu, odd ? v0 : v1, 1);
-              const int hs = odd ? h + 1 : h;
-              const int ds = odd ? d - 1 : d;
-              const __nv_bfloat162 b2 = odd ? __floats2bfloat162_rn(got, v1) : __floats2bfloat162_rn(v0, got);
-              if (hs < H)
-                *reinterpret_cast<__nv_bfloat162*>(out + (static_cast<size_t>(u.req) * H + hs) * kDCkv + ds) = b2;
+              for (int j = 0; j < 4; ++j) st_global_v8(dst + 8 * j, &o[8 * j]);
+            } else {
+              uint32_t w[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const __nv_bfloat162 b2 =
+                    __floats2bfloat162_rn(__uint_as_float(o[2 * j]), __uint_as_float(o[2 * j + 1]));
+                w[j] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) + (static_cast<size_t>(u.req) * H + h) * kDCkv + d;
+              st_global_v8(dst, &w[0]);
+              st_global_v8(dst + 16, &w[8]);
             }
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          if (rank == 0)
-            mbar_arrive(bar(base, kOFree));
-          else
-            mbar_arrive_cluster(map_to_rank(bar(base, kOFree), lead));
-        }
+        if (lane == 0) arrive_lead(bar(base, kOFree), rank);
       }
     }
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
   }
 
-  // On a device error some copies or remote stores may still be in flight
-  // toward this CTA: give them time to land before it leaves.
+  // On a device error some copies may still be in flight toward this CTA:
+  // give them time to land before it leaves.
   if (*abort_flag) {
     const uint64_t t0 = globaltimer_ns();
     while (globaltimer_ns() - t0 < 200000ull) {

@@ -20,71 +20,130 @@ constexpr int kChunk = 32;                     // dims per block
 constexpr int kChunks = kDCkv / kChunk;        // grid.y
 
 // One block per (request, 32-dim chunk).  The partials are read in their
-// [slot][d/4][h][d%4] layout, consecutive threads on consecutive heads
+// [slot][d/8][h][d%8] layout, consecutive threads on consecutive heads
 // (coalesced); the merged chunk is staged in shared memory and written out
-// row by row, 64 or 128 contiguous bytes per head.
+// row by row, 64 or 128 contiguous bytes per head.  A long request can have
+// a partial from every worker, so the slots are spread over the threads too:
+// the per-head maximum and weight sum are reduced by G adjacent lanes per
+// head, and with fewer than 32 heads the weighted sum is split over S thread
+// groups (each in slot order, the groups then added in group order), every
+// group loading kAhead slots before accumulating them.
 template <bool kOutF32>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a) {
   const int e = blockIdx.x;
   if (e >= a.params->n_merge) return;
   const MergeEntry me = a.merge[e];
   const int H = a.num_heads;
+  const int n = me.n_slots;
   const int dq = blockIdx.y;
   __shared__ float tile[kMaxHeads][kChunk + 1];
   __shared__ float s_max[kMaxHeads], s_inv[kMaxHeads];
+  __shared__ float4 s_part[kMergeThreads];
   const int t = threadIdx.x;
-  if (t < H) {
+  constexpr int kAhead = 4;
+  {
+    int G = 1;   // lanes per head: a power of two, G * H <= threads
+    while (G < 32 && 2 * G * H <= kMergeThreads) G *= 2;
+    const int h = t / G, g = t % G;
+    const bool act = h < H;
     float M = -INFINITY, wsum = 0.f;
-    for (int i = 0; i < me.n_slots; ++i)
-      M = fmaxf(M, a.lse_part[lse_part_offset(me.first_slot + i, 0, t, H)]);
-    for (int i = 0; i < me.n_slots; ++i)
-      wsum += __expf(a.lse_part[lse_part_offset(me.first_slot + i, 0, t, H)] - M);
-    s_max[t] = M;
-    s_inv[t] = me.n_slots > 0 ? 1.f / wsum : 0.f;
-    if (dq == 0) a.lse[static_cast<size_t>(me.req) * H + t] = me.n_slots > 0 ? M + __logf(wsum) : -INFINITY;
+    if (act)
+      for (int i = g; i < n; i += G) M = fmaxf(M, a.lse_part[lse_part_offset(me.first_slot + i, 0, h, H)]);
+    for (int off = G / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    if (act)
+      for (int i = g; i < n; i += G) wsum += __expf(a.lse_part[lse_part_offset(me.first_slot + i, 0, h, H)] - M);
+    for (int off = G / 2; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+    if (act && g == 0) {
+      s_max[h] = M;
+      s_inv[h] = n > 0 ? 1.f / wsum : 0.f;
+      if (dq == 0) a.lse[static_cast<size_t>(me.req) * H + h] = n > 0 ? M + __logf(wsum) : -INFINITY;
+    }
   }
   __syncthreads();
-  // (kChunk / 4) * H <= kItems * kMergeThreads items of 4 dims; each thread
-  // issues the loads of all its items for one slot before accumulating.
-  constexpr int kItems = (kChunk / 4) * kMaxHeads / kMergeThreads;
-  float4 acc[kItems];
-  int hk[kItems], dk[kItems];
-#pragma unroll
-  for (int k = 0; k < kItems; ++k) {
-    acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int idx = t + k * kMergeThreads;
-    const int dg = idx / H;
-    hk[k] = idx - dg * H;
-    dk[k] = idx < (kChunk / 4) * H ? dq * kChunk + 4 * dg : -1;
-  }
-  for (int i = 0; i < me.n_slots; ++i) {
-    const int slot = me.first_slot + i;
-    float4 o[kItems];
-    float l[kItems];
+  const int items = (kChunk / 4) * H;   // 4-dim items of this chunk
+  if (items >= kMergeThreads) {
+    // (kChunk / 4) * H <= kItems * kMergeThreads: several items per thread
+    constexpr int kItems = (kChunk / 4) * kMaxHeads / kMergeThreads;
+    float4 acc[kItems];
+    int hk[kItems], dk[kItems];
 #pragma unroll
     for (int k = 0; k < kItems; ++k) {
-      if (dk[k] >= 0) {
-        o[k] = *reinterpret_cast<const float4*>(a.o_part + part_offset(slot, hk[k], dk[k], H));
-        l[k] = a.lse_part[lse_part_offset(slot, 0, hk[k], H)];
-      }
+      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int idx = t + k * kMergeThreads;
+      const int dg = idx / H;
+      hk[k] = idx - dg * H;
+      dk[k] = idx < items ? dq * kChunk + 4 * dg : -1;
+    }
+    for (int i0 = 0; i0 < n; i0 += kAhead) {
+      float4 o[kAhead][kItems];
+      float l[kAhead][kItems];
+#pragma unroll
+      for (int j = 0; j < kAhead; ++j)
+#pragma unroll
+        for (int k = 0; k < kItems; ++k)
+          if (dk[k] >= 0 && i0 + j < n) {
+            o[j][k] = *reinterpret_cast<const float4*>(a.o_part + part_offset(me.first_slot + i0 + j, hk[k], dk[k], H));
+            l[j][k] = a.lse_part[lse_part_offset(me.first_slot + i0 + j, 0, hk[k], H)];
+          }
+#pragma unroll
+      for (int j = 0; j < kAhead; ++j)
+#pragma unroll
+        for (int k = 0; k < kItems; ++k)
+          if (dk[k] >= 0 && i0 + j < n) {
+            const float w = __expf(l[j][k] - s_max[hk[k]]);
+            acc[k].x += w * o[j][k].x; acc[k].y += w * o[j][k].y; acc[k].z += w * o[j][k].z; acc[k].w += w * o[j][k].w;
+          }
     }
 #pragma unroll
     for (int k = 0; k < kItems; ++k) {
       if (dk[k] >= 0) {
-        const float w = __expf(l[k] - s_max[hk[k]]);
-        acc[k].x += w * o[k].x; acc[k].y += w * o[k].y; acc[k].z += w * o[k].z; acc[k].w += w * o[k].w;
+        const int h = hk[k], c = dk[k] - dq * kChunk;
+        const float inv = s_inv[h];
+        tile[h][c] = acc[k].x * inv;
+        tile[h][c + 1] = acc[k].y * inv;
+        tile[h][c + 2] = acc[k].z * inv;
+        tile[h][c + 3] = acc[k].w * inv;
       }
     }
-  }
+  } else {
+    // one item per thread; S groups of threads take every S-th slot
+    int S = 1;
+    while (2 * S * items <= kMergeThreads) S *= 2;
+    const int item = t % items, sg = t / items;
+    const int dg = item / H, h = item - dg * H, d = dq * kChunk + 4 * dg;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (sg < S) {
+      for (int i0 = sg; i0 < n; i0 += S * kAhead) {
+        float4 o[kAhead];
+        float l[kAhead];
 #pragma unroll
-  for (int k = 0; k < kItems; ++k) {
-    if (dk[k] >= 0) {
-      const int h = hk[k], c = dk[k] - dq * kChunk;
+        for (int j = 0; j < kAhead; ++j)
+          if (i0 + S * j < n) {
+            o[j] = *reinterpret_cast<const float4*>(a.o_part + part_offset(me.first_slot + i0 + S * j, h, d, H));
+            l[j] = a.lse_part[lse_part_offset(me.first_slot + i0 + S * j, 0, h, H)];
+          }
+#pragma unroll
+        for (int j = 0; j < kAhead; ++j)
+          if (i0 + S * j < n) {
+            const float w = __expf(l[j] - s_max[h]);
+            acc.x += w * o[j].x; acc.y += w * o[j].y; acc.z += w * o[j].z; acc.w += w * o[j].w;
+          }
+      }
+    }
+    s_part[t] = acc;
+    __syncthreads();
+    if (t < items) {
+      float4 sum = s_part[t];
+      for (int q = 1; q < S; ++q) {
+        const float4 v = s_part[t + q * items];
+        sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+      }
+      const int c = 4 * dg;
       const float inv = s_inv[h];
-      tile[h][c] = acc[k].x * inv;
-      tile[h][c + 1] = acc[k].y * inv;
-      tile[h][c + 2] = acc[k].z * inv;
-      tile[h][c + 3] = acc[k].w * inv;
+      tile[h][c] = sum.x * inv;
+      tile[h][c + 1] = sum.y * inv;
+      tile[h][c + 2] = sum.z * inv;
+      tile[h][c + 3] = sum.w * inv;
     }
   }
   __syncthreads();

@@ -454,6 +454,15 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
+// Arrive on an mbarrier of another CTA of the cluster, releasing at CTA
+// scope: the arriving thread's shared-memory and TMEM accesses are ordered
+// before the arrive.  With the SM's TMA copies in flight, the cluster-scope
+// form above took 1-2 us per arrive (it waits on memory traffic the signal
+// does not publish); this one takes as long as a local arrive.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(
                    cluster_bar),

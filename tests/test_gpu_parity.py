@@ -261,6 +261,39 @@ def test_full_size_config(kernel, cfg):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("cfg", ["deepseek", "fp8"])
+def test_default_kernel_full_size(cfg):
+    # DEFAULT plans for the CTA-pair kernel; a bf16 cache runs on it, an fp8
+    # cache on the one-CTA kernel over the same (256-token) partition
+    x = _config(cfg)
+    d = to_device(x)
+    dec = mla.MLADecoder(x.batch, x.num_heads, "default")
+    out, lse = run_decode(x, d, "default", torch.float32, decoder=dec)
+    info = dec.info()
+    assert info["kernel"] == mla.KERNEL_PAIR and info["tile_tokens"] == 256
+    dec.close()
+    ref_out, ref_lse = _oracle(cfg)
+    assert_parity(out, lse, ref_out, ref_lse, cfg + " default")
+    del d
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("lens", [[20000, 1, 777, 0, 300], [9000] * 9 + [40]])
+def test_default_kernel_fp8_split_requests(lens):
+    # the one-CTA kernel combining split requests in place over a partition
+    # made for the CTA pair; repeated runs are bit-identical
+    x = I.make_inputs("default_fp8", lens, 128, 64, seed=23, kv_dtype="fp8_e4m3")
+    d = to_device(x)
+    dec = mla.MLADecoder(x.batch, x.num_heads, "default")
+    o0, l0 = run_decode(x, d, "default", torch.float32, decoder=dec)
+    assert dec.info()["num_partial_slots"] > 0, "the batch was meant to split requests"
+    o1, l1 = run_decode(x, d, "default", torch.float32, decoder=dec)
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)
+    dec.close()
+    ref_out, ref_lse = O.mla_decode_inputs(x)
+    assert_parity(o0, l0, ref_out, ref_lse, "default fp8 splits")
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("cfg, lens, heads, P", [
     ("split_many", [20000, 1, 777], 128, 16),  # one request over ~two dozen units
