@@ -111,23 +111,43 @@ class L2Flush:
         self.r.view(torch.float32).sum()   # the read pass, reduced as fp32 words: no widened copy
 
 
-PROFILE = os.path.join(ROOT, "profiles", "decode_tc_deepseek.json")
-KERNEL_SOURCES = ["decode_tc.cu", "tc_utils.cuh", "device_utils.cuh", "kernels.h", "mla_internal.h"]
+# DRAM traffic of the dominant kernel per launch on the deepseek workload, from
+# the committed ncu summaries: (summary, the sources the figure was taken of)
+PROFILES = {
+    "pair": ("decode_pair_deepseek.json",
+             ["decode_pair.cu", "tc_utils.cuh", "device_utils.cuh", "kernels.h", "mla_internal.h"]),
+    "tcgen05": ("decode_tc_deepseek.json",
+                ["decode_tc.cu", "tc_utils.cuh", "device_utils.cuh", "kernels.h", "mla_internal.h"]),
+}
+KERNEL_NAMES = {1: "tcgen05", 2: "mma_sync", 3: "pair"}   # mla_kernel_t values
 
 
-def profiled_traffic(workload: str) -> float | None:
-    """DRAM bytes per launch of the tcgen05 kernel from the committed ncu
-    summary, or None when the summary is for another workload or the kernel
-    sources changed since it was taken (hash recorded beside the figure)."""
+def kernel_run(plan_kernel: int, requested: str, kv_dtype: str) -> str:
+    """The decode kernel a run launches: a DEFAULT plan is made for the
+    CTA-pair kernel and runs an fp8 cache on the one-CTA kernel."""
+    if requested == "default" and kv_dtype != "bf16":
+        return "tcgen05"
+    return KERNEL_NAMES[plan_kernel]
+
+
+def profiled_traffic(workload: str, kernel: str) -> float | None:
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, or None when there is none for this kernel and workload or the
+    kernel sources changed since it was taken (hash recorded beside the
+    figure)."""
     import hashlib
-    if workload != "deepseek" or not os.path.exists(PROFILE):
+    if workload != "deepseek" or kernel not in PROFILES:
+        return None
+    name, sources = PROFILES[kernel]
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
         return None
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in sources:
         h.update(f.encode())
         with open(os.path.join(ROOT, "paged_mla_decode_02_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
-    vals = json.load(open(PROFILE))
+    vals = json.load(open(path))
     if vals.get("source_sha256") != h.hexdigest() or "dram_bytes_per_launch" not in vals:
         return None
     return float(vals["dram_bytes_per_launch"])
@@ -691,6 +711,7 @@ def main() -> None:
 
     nbytes, flops = algorithmic(x)
     hbm, bf, bfs, peak_src = peaks()
+    run_kernel = kernel_run(info["kernel"], args.kernel, x.kv_dtype)
     kern_us = statistics.mean(kern_ms) * 1000.0
     achieved_gbs = nbytes / (kern_us * 1e-6) / 1e9
     achieved_tf = flops / (kern_us * 1e-6) / 1e12
@@ -702,10 +723,9 @@ def main() -> None:
             "peak": hbm if bound == "hbm" else bf,
             "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
             "peak_source": peak_src,
-            "traffic": (profiled_traffic(args.config)
-                        if info["kernel"] == mla.KERNEL_TCGEN05 else None),
+            "traffic": profiled_traffic(args.config, run_kernel),
             "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
-            "kernel": "mla_decode (split-KV decode kernel)",
+            "kernel": f"mla_decode ({run_kernel} decode kernel)",
             "kernel_us": kern_us,
             "algorithmic_bytes": nbytes, "algorithmic_flops": flops,
             "achieved_tflops": achieved_tf, "achieved_gbs": achieved_gbs,
@@ -729,10 +749,10 @@ def main() -> None:
                     "d2h_bytes_per_step": int(out_h.numel() * out_h.element_size()
                                               + lse_h.numel() * 4)},
             # tcgen05: one kernel per step (split requests merged in its epilogue);
-            # mma.sync: decode + merge
-            "gpu_launches": (1 if info["kernel"] == mla.KERNEL_TCGEN05 else 2) * args.steps,
+            # CTA pair and mma.sync: decode + merge
+            "gpu_launches": (1 if run_kernel == "tcgen05" else 2) * args.steps,
             "wall_s_timed": wall, "plan_us": plan_us,
-            "kernel": info["kernel"], "plan": info,
+            "kernel": run_kernel, "plan": info,
             "timing": {"method": "each timed step replays the run from a CUDA graph; CUDA events "
                                  "on the launching stream around each replay; L2 flushed before "
                                  "each cold replay, outside the events",

@@ -30,6 +30,9 @@ constexpr int kChunks = kDCkv / kChunk;        // grid.y
 // group loading kAhead slots before accumulating them.
 template <bool kOutF32>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a) {
+  // launched as a programmatic dependent of the decode kernel: wait for it
+  // (a no-op in a plain launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int e = blockIdx.x;
   if (e >= a.params->n_merge) return;
   const MergeEntry me = a.merge[e];
@@ -244,12 +247,20 @@ cudaError_t launch_merge_states(const float* o_a, const float* lse_a, const floa
 
 cudaError_t launch_merge(const MergeArgs& a, bool out_f32, cudaStream_t s) {
   if (a.merge_cap <= 0) return cudaSuccess;
-  dim3 grid(a.merge_cap, kChunks);
-  if (out_f32)
-    merge_kernel<true><<<grid, kMergeThreads, 0, s>>>(a);
-  else
-    merge_kernel<false><<<grid, kMergeThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the merge grid may be scheduled while the
+  // decode kernel before it in the stream is still running (on SMs that
+  // kernel has left); each block waits for that kernel to complete, and its
+  // writes to be visible, before it reads a partial.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.merge_cap, kChunks);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return out_f32 ? cudaLaunchKernelEx(&cfg, merge_kernel<true>, a) : cudaLaunchKernelEx(&cfg, merge_kernel<false>, a);
 }
 
 }  // namespace mla
