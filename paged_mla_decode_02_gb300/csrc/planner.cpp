@@ -9,12 +9,12 @@
 //
 // Split policy: requests are laid end to end and dealt to the n_workers
 // workers in order, each worker taking a contiguous run of them.  The plan
-// minimises the largest worker cost under a simple model (quarter tiles): a
-// tile costs kTileCost, every work unit kUnitCost more (the pipeline refills
-// and an epilogue runs), and a unit of a split request kSplitCost more again
-// (its share goes out to memory and is merged).  A request is cut only where
-// a worker fills up, and only into pieces of at least kMinPiece tiles.  A
-// request covered by one unit
+// minimises the largest worker cost under a simple model (quarter tiles, see
+// plan_costs): a tile costs `tile`, every work unit `unit` more (the pipeline
+// refills and an epilogue runs), and a unit of a split request `split` more
+// again (its share goes out to memory and is merged).  A request is cut only
+// where a worker fills up, and only into pieces of at least `min_piece`
+// tiles.  A request covered by one unit
 // writes its final output directly; a request cut into several units writes
 // one partial (O, lse) per unit, combined by log-sum-exp, the combination
 // that cascade attention relies on ("[V1][Core] FlashInfer attention backend
@@ -83,12 +83,13 @@ constexpr int tiles_of(int32_t len, int tile_tokens) { return (len + tile_tokens
 // Greedy fill at makespan `budget` (cost units).  Requests are taken in
 // order; a worker takes whole requests while they fit, and the first one that
 // does not is cut so that the worker is full, when both pieces keep at least
-// kMinPiece tiles (else the next worker starts with it).  Writes the
+// min_piece tiles (else the next worker starts with it).  Writes the
 // units (req, token range, page base, length) and the worker offsets when
 // `units` is non-null.  Returns the number of units, or -1 when the batch
 // needs more than n_workers workers at this budget.
 int fill_workers(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int n_workers,
                  int tile_tokens, long long budget, WorkUnit* units, int32_t* worker_ptr) {
+  const PlanCosts c = plan_costs(tile_tokens);
   int w = 0, nu = 0;
   long long used = 0;   // cost taken by worker w
   if (worker_ptr) worker_ptr[0] = 0;
@@ -118,17 +119,17 @@ int fill_workers(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int
     while (t < n) {
       if (w >= n_workers) return -1;
       const int rest = n - t;
-      const long long whole = kUnitCost + static_cast<long long>(kTileCost) * rest + (split ? kSplitCost : 0);
+      const long long whole = c.unit + static_cast<long long>(c.tile) * rest + (split ? c.split : 0);
       if (used + whole <= budget) {
         emit(b, t, n);
         used += whole;
         break;
       }
       // tiles that fit as a piece of a split request; both pieces keep at
-      // least kMinPiece tiles
-      const long long room = (budget - used - kUnitCost - kSplitCost) / kTileCost;
-      const long long take = std::min<long long>(room, rest - kMinPiece);
-      if (take < kMinPiece) {
+      // least min_piece tiles
+      const long long room = (budget - used - c.unit - c.split) / c.tile;
+      const long long take = std::min<long long>(room, rest - c.min_piece);
+      if (take < c.min_piece) {
         if (used == 0) return -1;   // not even an empty worker takes a piece
         next_worker();              // the next worker starts with this request
         continue;
@@ -154,13 +155,14 @@ int partition_units(const int32_t* kv_indptr, const int32_t* kv_len, int batch, 
   // looked for upward from the lower bound every partition obeys (the work
   // spread evenly), at most kMaxScan budgets.  One worker holding everything
   // always fits.
+  const PlanCosts c = plan_costs(tile_tokens);
   long long total = 0, nonempty = 0;
   for (int b = 0; b < batch; ++b) {
     total += tiles_of(kv_len[b], tile_tokens);
     nonempty += kv_len[b] > 0;
   }
   long long lo = 0;
-  long long hi = kTileCost * total + static_cast<long long>(kUnitCost + kSplitCost) * (batch + n_workers);
+  long long hi = c.tile * total + static_cast<long long>(c.unit + c.split) * (batch + n_workers);
   while (lo + 1 < hi) {
     const long long mid = lo + (hi - lo) / 2;
     if (fill_workers(kv_indptr, kv_len, batch, n_workers, tile_tokens, mid, nullptr, nullptr) >= 0)
@@ -169,7 +171,7 @@ int partition_units(const int32_t* kv_indptr, const int32_t* kv_len, int batch, 
       lo = mid;
   }
   constexpr long long kMaxScan = 4096;
-  const long long bound = (kTileCost * total + kUnitCost * nonempty + n_workers - 1) / n_workers;
+  const long long bound = (c.tile * total + c.unit * nonempty + n_workers - 1) / n_workers;
   for (long long b = std::max(bound, hi - kMaxScan); b < hi; ++b)
     if (fill_workers(kv_indptr, kv_len, batch, n_workers, tile_tokens, b, nullptr, nullptr) >= 0) {
       hi = b;

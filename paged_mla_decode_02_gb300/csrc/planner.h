@@ -22,14 +22,19 @@ mla_status_t validate_batch(const int32_t* kv_indptr, const int32_t* kv_len, int
                             int head_dim_ckv, int head_dim_kpe, int page_size,
                             float sm_scale, std::string* why);
 
-// Cost model of the split, in quarter tiles: one tile costs kTileCost, a work
-// unit kUnitCost on top (pipeline fill and epilogue), a unit of a split
-// request kSplitCost more (its share is stored and merged).  Requests are cut
-// only into pieces of at least kMinPiece tiles.
-constexpr int kTileCost = 4;
-constexpr int kUnitCost = 8;
-constexpr int kSplitCost = 4;
-constexpr int kMinPiece = 4;
+// Cost model of the split, in quarter tiles: one tile costs `tile`, a work
+// unit `unit` on top (pipeline fill and epilogue), a unit of a split request
+// `split` more (its share is stored and merged).  Requests are cut only into
+// pieces of at least `min_piece` tiles.  The constants were picked by A/B on
+// the GPU for each kernel's tile: 128-token tiles (the one-CTA tcgen05
+// kernel) and 256-token tiles (the CTA-pair kernel, whose tile takes about as
+// long as a unit's fill).
+struct PlanCosts {
+  int tile, unit, split, min_piece;
+};
+constexpr PlanCosts plan_costs(int tile_tokens) {
+  return tile_tokens >= 256 ? PlanCosts{4, 4, 2, 2} : PlanCosts{4, 8, 4, 4};
+}
 
 // Deals the requests' tile_tokens-token tiles to n_workers workers (each a
 // contiguous run of requests, cut into work units at request boundaries) so

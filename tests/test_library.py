@@ -170,9 +170,14 @@ def test_partition_rejects_inconsistent_paging(lib):
         mla.mla_plan_partition_host(nz, lens, 4, 128, 16)
 
 
-def _greedy_fits(lens, W, T, budget, TILE=4, UNIT=8, SPLIT=4, MIN_PIECE=4):
+# the planner's cost constants (tile, unit, split, minimum piece) per tile size
+COSTS = {128: (4, 8, 4, 4), 256: (4, 4, 2, 2)}
+
+
+def _greedy_fits(lens, W, T, budget):
     """The planner's fill rule, restated: requests in order, whole while they
     fit, else cut where the worker fills up (both pieces >= MIN_PIECE tiles)."""
+    TILE, UNIT, SPLIT, MIN_PIECE = COSTS[T]
     w, used = 0, 0
     for L in lens:
         n = (int(L) + T - 1) // T
@@ -196,21 +201,23 @@ def _greedy_fits(lens, W, T, budget, TILE=4, UNIT=8, SPLIT=4, MIN_PIECE=4):
     return True
 
 
-def test_partition_makespan_is_the_smallest_feasible_budget(lib):
+@pytest.mark.parametrize("T", [128, 256])
+def test_partition_makespan_is_the_smallest_feasible_budget(lib, T):
     # The fill's success is not monotone in the budget, so a bisection alone
     # can stop above the best budget (one request of 19 tiles on 5 workers:
     # 40 against 32).  The planner's largest worker cost must equal the
     # smallest budget a linear scan finds.
-    T, P = 128, 64
+    P = 64
+    TILE, UNIT, SPLIT, _ = COSTS[T]
     rng = np.random.Generator(np.random.PCG64(23))
-    cases = [([19 * 128], 5)]
+    cases = [([19 * T], 5)]
     for _ in range(40):
         B_ = int(rng.integers(1, 6))
-        cases.append((list(rng.integers(1, 40 * 128, size=B_)), int(rng.integers(1, 12))))
+        cases.append((list(rng.integers(1, 40 * T, size=B_)), int(rng.integers(1, 12))))
     for lens, W in cases:
         indptr, l32 = _batch(lens, P)
         units, wptr, _, _ = mla.mla_plan_partition_host(indptr, l32, W, T, P)
-        cost = [sum(4 * ((u[2] - u[1] + T - 1) // T) + 8 + (4 if u[3] >= 0 else 0)
+        cost = [sum(TILE * ((u[2] - u[1] + T - 1) // T) + UNIT + (SPLIT if u[3] >= 0 else 0)
                     for u in units[wptr[w]:wptr[w + 1]]) for w in range(W)]
         best = next(b for b in range(1, 10 ** 6) if _greedy_fits(l32, W, T, b))
         assert max(cost) <= best, (lens, W, max(cost), best)
