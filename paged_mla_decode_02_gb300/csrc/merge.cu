@@ -16,8 +16,11 @@ namespace mla {
 namespace {
 
 constexpr int kMergeThreads = 256;
-constexpr int kChunk = 32;                     // dims per block
-constexpr int kChunks = kDCkv / kChunk;        // grid.y
+constexpr int kChunk = 32;                     // dims per block (the largest)
+// Fewer heads, narrower chunks: with H <= 32 a block takes 8 dims, so a
+// request spreads over 64 blocks and each block's threads split its slots
+// into more groups.
+__host__ __device__ inline int merge_chunk(int H) { return H <= 32 ? 8 : kChunk; }
 
 // One block per (request, 32-dim chunk).  The partials are read in their
 // [slot][d/8][h][d%8] layout, consecutive threads on consecutive heads
@@ -39,6 +42,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
   const int H = a.num_heads;
   const int n = me.n_slots;
   const int dq = blockIdx.y;
+  const int C = merge_chunk(H);
   __shared__ float tile[kMaxHeads][kChunk + 1];
   __shared__ float s_max[kMaxHeads], s_inv[kMaxHeads];
   __shared__ float4 s_part[kMergeThreads];
@@ -49,13 +53,32 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
     while (G < 32 && 2 * G * H <= kMergeThreads) G *= 2;
     const int h = t / G, g = t % G;
     const bool act = h < H;
+    // one pass, running maximum and the weight sum relative to it; four
+    // slots' loads issued before they are folded in
     float M = -INFINITY, wsum = 0.f;
     if (act)
-      for (int i = g; i < n; i += G) M = fmaxf(M, a.lse_part[lse_part_offset(me.first_slot + i, 0, h, H)]);
-    for (int off = G / 2; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    if (act)
-      for (int i = g; i < n; i += G) wsum += __expf(a.lse_part[lse_part_offset(me.first_slot + i, 0, h, H)] - M);
-    for (int off = G / 2; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+      for (int i0 = g; i0 < n; i0 += 4 * G) {
+        float l[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          l[j] = i0 + j * G < n ? a.lse_part[lse_part_offset(me.first_slot + i0 + j * G, 0, h, H)] : -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (l[j] == -INFINITY) continue;
+          const float Mn = fmaxf(M, l[j]);
+          wsum = wsum * __expf(M - Mn) + __expf(l[j] - Mn);
+          M = Mn;
+        }
+      }
+    for (int off = G / 2; off > 0; off >>= 1) {
+      const float M2 = __shfl_xor_sync(0xffffffffu, M, off);
+      const float w2 = __shfl_xor_sync(0xffffffffu, wsum, off);
+      const float Mn = fmaxf(M, M2);
+      if (Mn != -INFINITY) {
+        wsum = (M == -INFINITY ? 0.f : wsum * __expf(M - Mn)) + (M2 == -INFINITY ? 0.f : w2 * __expf(M2 - Mn));
+        M = Mn;
+      }
+    }
     if (act && g == 0) {
       s_max[h] = M;
       s_inv[h] = n > 0 ? 1.f / wsum : 0.f;
@@ -63,7 +86,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
     }
   }
   __syncthreads();
-  const int items = (kChunk / 4) * H;   // 4-dim items of this chunk
+  const int items = (C / 4) * H;   // 4-dim items of this chunk
   if (items >= kMergeThreads) {
     // (kChunk / 4) * H <= kItems * kMergeThreads: several items per thread
     constexpr int kItems = (kChunk / 4) * kMaxHeads / kMergeThreads;
@@ -75,7 +98,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
       const int idx = t + k * kMergeThreads;
       const int dg = idx / H;
       hk[k] = idx - dg * H;
-      dk[k] = idx < items ? dq * kChunk + 4 * dg : -1;
+      dk[k] = idx < items ? dq * C + 4 * dg : -1;
     }
     for (int i0 = 0; i0 < n; i0 += kAhead) {
       float4 o[kAhead][kItems];
@@ -100,7 +123,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
 #pragma unroll
     for (int k = 0; k < kItems; ++k) {
       if (dk[k] >= 0) {
-        const int h = hk[k], c = dk[k] - dq * kChunk;
+        const int h = hk[k], c = dk[k] - dq * C;
         const float inv = s_inv[h];
         tile[h][c] = acc[k].x * inv;
         tile[h][c + 1] = acc[k].y * inv;
@@ -109,24 +132,26 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
       }
     }
   } else {
-    // one item per thread; S groups of threads take every S-th slot
+    // one item per thread; S groups of threads take every S-th slot, each
+    // loading kAheadSmall slots before folding them in
+    constexpr int kAheadSmall = 8;
     int S = 1;
     while (2 * S * items <= kMergeThreads) S *= 2;
     const int item = t % items, sg = t / items;
-    const int dg = item / H, h = item - dg * H, d = dq * kChunk + 4 * dg;
+    const int dg = item / H, h = item - dg * H, d = dq * C + 4 * dg;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (sg < S) {
-      for (int i0 = sg; i0 < n; i0 += S * kAhead) {
-        float4 o[kAhead];
-        float l[kAhead];
+      for (int i0 = sg; i0 < n; i0 += S * kAheadSmall) {
+        float4 o[kAheadSmall];
+        float l[kAheadSmall];
 #pragma unroll
-        for (int j = 0; j < kAhead; ++j)
+        for (int j = 0; j < kAheadSmall; ++j)
           if (i0 + S * j < n) {
             o[j] = *reinterpret_cast<const float4*>(a.o_part + part_offset(me.first_slot + i0 + S * j, h, d, H));
             l[j] = a.lse_part[lse_part_offset(me.first_slot + i0 + S * j, 0, h, H)];
           }
 #pragma unroll
-        for (int j = 0; j < kAhead; ++j)
+        for (int j = 0; j < kAheadSmall; ++j)
           if (i0 + S * j < n) {
             const float w = __expf(l[j] - s_max[h]);
             acc.x += w * o[j].x; acc.y += w * o[j].y; acc.z += w * o[j].z; acc.w += w * o[j].w;
@@ -152,21 +177,21 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
   __syncthreads();
   const size_t row0 = static_cast<size_t>(me.req) * H;
   if (kOutF32) {
-    for (int idx = t; idx < H * (kChunk / 4); idx += kMergeThreads) {
-      const int h = idx / (kChunk / 4), q = idx % (kChunk / 4);
-      *reinterpret_cast<float4*>(static_cast<float*>(a.out) + (row0 + h) * kDCkv + dq * kChunk + 4 * q) =
+    for (int idx = t; idx < H * (C / 4); idx += kMergeThreads) {
+      const int h = idx / (C / 4), q = idx % (C / 4);
+      *reinterpret_cast<float4*>(static_cast<float*>(a.out) + (row0 + h) * kDCkv + dq * C + 4 * q) =
           make_float4(tile[h][4 * q], tile[h][4 * q + 1], tile[h][4 * q + 2], tile[h][4 * q + 3]);
     }
   } else {
-    for (int idx = t; idx < H * (kChunk / 8); idx += kMergeThreads) {
-      const int h = idx / (kChunk / 8), q = idx % (kChunk / 8);
+    for (int idx = t; idx < H * (C / 8); idx += kMergeThreads) {
+      const int h = idx / (C / 8), q = idx % (C / 8);
       uint32_t w[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const __nv_bfloat162 b2 = __floats2bfloat162_rn(tile[h][8 * q + 2 * k], tile[h][8 * q + 2 * k + 1]);
         w[k] = *reinterpret_cast<const uint32_t*>(&b2);
       }
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + (row0 + h) * kDCkv + dq * kChunk + 8 * q) =
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + (row0 + h) * kDCkv + dq * C + 8 * q) =
           make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
@@ -252,7 +277,7 @@ cudaError_t launch_merge(const MergeArgs& a, bool out_f32, cudaStream_t s) {
   // kernel has left); each block waits for that kernel to complete, and its
   // writes to be visible, before it reads a partial.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.merge_cap, kChunks);
+  cfg.gridDim = dim3(a.merge_cap, kDCkv / merge_chunk(a.num_heads));
   cfg.blockDim = dim3(kMergeThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
