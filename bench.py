@@ -122,10 +122,11 @@ PROFILES = {
 KERNEL_NAMES = {1: "tcgen05", 2: "mma_sync", 3: "pair"}   # mla_kernel_t values
 
 
-def kernel_run(plan_kernel: int, requested: str, kv_dtype: str) -> str:
+def kernel_run(plan_kernel: int, requested: str, kv_dtype: str, page_size: int) -> str:
     """The decode kernel a run launches: a DEFAULT plan is made for the
-    CTA-pair kernel and runs an fp8 cache on the one-CTA kernel."""
-    if requested == "default" and kv_dtype != "bf16":
+    CTA-pair kernel and runs an fp8 cache with 16-token pages on the one-CTA
+    kernel."""
+    if requested == "default" and kv_dtype != "bf16" and page_size < 32:
         return "tcgen05"
     return KERNEL_NAMES[plan_kernel]
 
@@ -711,7 +712,7 @@ def main() -> None:
 
     nbytes, flops = algorithmic(x)
     hbm, bf, bfs, peak_src = peaks()
-    run_kernel = kernel_run(info["kernel"], args.kernel, x.kv_dtype)
+    run_kernel = kernel_run(info["kernel"], args.kernel, x.kv_dtype, x.page_size)
     kern_us = statistics.mean(kern_ms) * 1000.0
     achieved_gbs = nbytes / (kern_us * 1e-6) / 1e9
     achieved_tf = flops / (kern_us * 1e-6) / 1e12

@@ -59,11 +59,12 @@ typedef enum {
 } mla_dtype_t;
 
 typedef enum {
-  MLA_KERNEL_DEFAULT = 0,     /* MLA_KERNEL_PAIR for bf16 caches; an fp8 cache runs on the
-                                 tcgen05 kernel over the same plan */
+  MLA_KERNEL_DEFAULT = 0,     /* MLA_KERNEL_PAIR (an fp8 cache with 16-token pages runs on
+                                 the tcgen05 kernel over the same plan, which rejects it) */
   MLA_KERNEL_TCGEN05 = 1,     /* one-CTA tcgen05 / TMEM kernel (bf16 and fp8 caches) */
   MLA_KERNEL_MMA_SYNC = 2,    /* warp-level mma.sync kernel (legacy tensor path, for comparison) */
-  MLA_KERNEL_PAIR = 3         /* tcgen05 kernel whose MMAs span a CTA pair (cta_group::2); bf16 caches */
+  MLA_KERNEL_PAIR = 3         /* tcgen05 kernel whose MMAs span a CTA pair (cta_group::2); bf16
+                                 caches, and fp8 caches with page_size >= 32 (f16 MMAs) */
 } mla_kernel_t;
 
 /* Plan statistics, filled by mla_plan_info. */
@@ -158,9 +159,11 @@ mla_status_t mla_decode_plan_multi(mla_plan_t plan, const int32_t* kv_indptr_hos
  * An FP8_E4M3 cache runs on the tcgen05 kernel with page_size 32 or 64 (each
  * copied tile is expanded to bf16 in shared memory; every e4m3 value is exact
  * in bf16), and on the mma.sync kernel with any page size; with the tcgen05
- * kernel and 16-token pages the call returns MLA_ERR_UNSUPPORTED.  A plan of
- * MLA_KERNEL_PAIR returns MLA_ERR_UNSUPPORTED for an fp8 cache; a plan of
- * MLA_KERNEL_DEFAULT runs it on the tcgen05 kernel.
+ * kernel and 16-token pages the call returns MLA_ERR_UNSUPPORTED.  The
+ * CTA-pair kernel (and so MLA_KERNEL_DEFAULT) takes fp8 caches with 32- or
+ * 64-token pages: each copied tile is expanded to f16 in shared memory and
+ * the query converted to f16 under a power-of-two scale per head row; with
+ * 16-token pages it returns MLA_ERR_UNSUPPORTED.
  *   out       [batch, num_heads, 512]   out_dtype (BF16 or FP32)
  *   lse       [batch, num_heads]        fp32, natural log
  * Launches the decode kernel; with the tcgen05 kernel that is the only launch

@@ -183,17 +183,23 @@ bool mla::encode_tc_maps(TcMaps* maps, const void* q_nope, const void* ckv_cache
 }
 
 // The CTA-pair kernel's tensor maps: the query of 64 heads per box (one per
-// CTA of the pair), K panels of one page, V chunks of four 64-dim panels.
+// CTA of the pair), K panels of one page, V chunks of four 64-dim panels
+// (an fp8 cache: byte maps, 64-byte swizzle).
 bool mla::encode_pair_maps(PairMaps* maps, const void* q_nope, const void* q_pe, const void* ckv_cache,
-                           const void* kpe_cache, int batch, int num_heads, int page_size, int num_pages) {
+                           const void* kpe_cache, int batch, int num_heads, int page_size, int num_pages,
+                           bool kv_fp8) {
   const uint64_t qrows = static_cast<uint64_t>(batch) * num_heads;
   const uint64_t kvrows = static_cast<uint64_t>(num_pages) * page_size;
   const CUtensorMapDataType bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType kt = kv_fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : bf;
+  const CUtensorMapSwizzle ks = kv_fp8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  const int eb = kv_fp8 ? 1 : 2;
   return encode_2d(&maps->q_nope, q_nope, bf, 2, qrows, kDCkv, 64, 64) &&
          encode_2d(&maps->q_pe, q_pe, bf, 2, qrows, kDKpe, 64, 64) &&
-         encode_2d(&maps->ckv_k, ckv_cache, bf, 2, kvrows, kDCkv, page_size, 64) &&
-         encode_2d(&maps->kpe_k, kpe_cache, bf, 2, kvrows, kDKpe, page_size, 64) &&
-         encode_panels_3d(&maps->ckv_v, ckv_cache, kvrows, page_size >= kTcVChunkTok ? kTcVChunkTok : 16, 4);
+         encode_2d(&maps->ckv_k, ckv_cache, kt, eb, kvrows, kDCkv, page_size, 64, ks) &&
+         encode_2d(&maps->kpe_k, kpe_cache, kt, eb, kvrows, kDKpe, page_size, 64, ks) &&
+         encode_panels_3d(&maps->ckv_v, ckv_cache, kvrows, page_size >= kTcVChunkTok ? kTcVChunkTok : 16, 4,
+                          kv_fp8);
 }
 
 extern "C" {
@@ -468,18 +474,22 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
   cudaError_t e;
   if (plan->prof_start && (e = cudaEventRecord(plan->prof_start, s)) != cudaSuccess)
     return cuda_fail(plan, e, "cudaEventRecord");
-  const int kern = fp8 && plan->kernel_requested == MLA_KERNEL_DEFAULT ? MLA_KERNEL_TCGEN05 : plan->kernel;
+  // DEFAULT: the pair kernel, for an fp8 cache with pages of 32 or more
+  // tokens; 16-token fp8 pages go to the one-CTA kernel (which rejects them)
+  const int kern = fp8 && plan->kernel_requested == MLA_KERNEL_DEFAULT && plan->params.page_size < kTcVChunkTok
+                       ? MLA_KERNEL_TCGEN05
+                       : plan->kernel;
   if (kern == MLA_KERNEL_MMA_SYNC) {
     e = launch_decode_mma(a, fp8, out_f32, s);
   } else if (kern == MLA_KERNEL_PAIR) {
-    if (fp8)
+    if (fp8 && plan->params.page_size < kTcVChunkTok)
       return fail(plan, MLA_ERR_UNSUPPORTED,
-                  "the CTA-pair kernel takes bf16 caches; use MLA_KERNEL_TCGEN05 for fp8");
+                  "the CTA-pair kernel takes fp8 caches with page_size >= 32; use MLA_KERNEL_MMA_SYNC");
     PairMaps maps;
     if (!encode_pair_maps(&maps, q_nope, q_pe, ckv_cache, kpe_cache, plan->params.batch, plan->num_heads,
-                          plan->params.page_size, num_pages))
+                          plan->params.page_size, num_pages, fp8))
       return fail(plan, MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    e = launch_decode_pair(a, maps, out_f32, s);
+    e = launch_decode_pair(a, maps, out_f32, fp8, s);
   } else {
     if (fp8 && plan->params.page_size < kTcVChunkTok)
       return fail(plan, MLA_ERR_UNSUPPORTED,

@@ -42,11 +42,20 @@
 // four threads of a head at the end (the output is divided by the latter,
 // the lse uses the former).
 //
+// fp8 (e4m3) caches (pages of 32 or 64 tokens): the copies land as codes in
+// the upper half of each ring slot and are expanded in place to f16 -- in the
+// even CTA by the issuing warp itself while the previous MMAs run, in the odd
+// CTA by warps 1 and 11, which then signal the even CTA -- and both products
+// take f16 operands: the query converted once per unit (a power-of-two scale
+// per head row), P rounded to f16.
+//
 // Every wait is bounded (2 s); on expiry the kernel records
 // MLA_ERR_DEVICE_TIMEOUT, lets its copies and MMAs land, frees TMEM and
 // returns.  Page ids outside [0, num_pages) are recorded as
 // MLA_ERR_DEVICE_BOUNDS and never dereferenced.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "device_utils.cuh"
 #include "kernels.h"
@@ -72,7 +81,6 @@ constexpr int kVProducerWarp = 10;
 constexpr int kPvIssuerWarp = 11;
 constexpr int kKSlots = 4, kVSlots = 3;    // ring slots
 constexpr int kPBufs = 1;                  // P buffers (2: by tile parity)
-constexpr bool kStreamQ = false;           // query panels ride in the K slots instead of staying resident
 constexpr int kSlotBytes = 16384;
 constexpr int kVChunkTok = kTcVChunkTok;   // 32 tokens per V chunk
 constexpr int kChunksPerTile = kT / kVChunkTok;
@@ -86,15 +94,15 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units: p stays below 2^8
 // shared memory (offsets from the 1024-byte aligned base)
 constexpr int kOffQ = 0;                          // 9 panels x (64 heads x 128 B)
 constexpr int kQPanel = 64 * 128;
-constexpr int kKSlotBytes = kSlotBytes + (kStreamQ ? kQPanel : 0);   // K panel (+ the query panel)
-constexpr int kOffP = kOffQ + (kStreamQ ? 0 : 9 * kQPanel);         // P: 4 token panels x (64 heads x 128 B)
+constexpr int kOffP = kOffQ + 9 * kQPanel;        // P: 4 token panels x (64 heads x 128 B)
 constexpr int kPPanel = 64 * 128;
 constexpr int kPBuf = 4 * kPPanel;                // one P buffer: 32 KB
 constexpr int kOffKRing = kOffP + kPBufs * kPBuf;
-constexpr int kOffVRing = kOffKRing + kKSlots * kKSlotBytes;
+constexpr int kOffVRing = kOffKRing + kKSlots * kSlotBytes;
 constexpr int kOffRed = kOffVRing + kVSlots * kSlotBytes;  // maxima [2 parities][4 parts][64 heads] float
 constexpr int kOffSum = kOffRed + 2 * 4 * 64 * 4;          // sums [4 parts][64 heads] float2
-constexpr int kOffFlags = kOffSum + 4 * 64 * 8;           // abort, tmem slot
+constexpr int kOffQRed = kOffSum + 4 * 64 * 8;            // fp8: query row maxima [4 parts][64 heads] float
+constexpr int kOffFlags = kOffQRed + 4 * 64 * 4;          // abort, tmem slot
 constexpr int kOffBar = kOffFlags + 64;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOffKRing % 1024 == 0 && kOffVRing % 1024 == 0,
               "swizzle atoms");
@@ -117,6 +125,12 @@ enum Bar {
   kTailReady,                    // even CTA: both CTAs zeroed the rows past the end of a partial V chunk
   kFinal,                        // even CTA: every QK MMA completed
   kFinalPv,                      // even CTA: every PV MMA completed
+  // fp8 caches only
+  kKLand0,                       // [kKSlots] this CTA's e4m3 K copy landed (1 arrival + bytes)
+  kVLand0 = kKLand0 + kKSlots,   // [kVSlots] this CTA's e4m3 V copy landed
+  kQLand = kVLand0 + kVSlots,    // this CTA's query landed (1 arrival + bytes)
+  kQRed,                         // the 8 softmax warps posted their query row maxima
+  kQReady,                       // even CTA: both CTAs' query converted to f16 (16 arrivals)
   kNumBars
 };
 constexpr int kSmemBytes = kOffBar + 8 * kNumBars + 1024;   // + alignment slack
@@ -137,7 +151,96 @@ __device__ __forceinline__ void arrive_lead(uint32_t local_bar, int rank) {
     mbar_arrive_remote(map_to_rank(local_bar, 0));
 }
 
-template <bool kOutF32>
+// ---------------------------------------------------------------------------
+// fp8 (e4m3) caches.  The MMAs then take f16 operands: an e4m3 code converts
+// to f16 exactly in one instruction per pair (to bf16 it takes four), the
+// query is converted to f16 once per unit under a power-of-two scale per
+// head row (its largest magnitude lands in [2^14, 2^15): f16 keeps bf16's 8
+// significant bits and more), and P, in [0, 2^8], is rounded to f16.
+// ---------------------------------------------------------------------------
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4)                                   // D format: f32
+         | (static_cast<uint32_t>(a_mn) << 15)       // A, B format: f16 (0)
+         | (static_cast<uint32_t>(b_mn) << 16)
+         | (static_cast<uint32_t>(N >> 3) << 17)
+         | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Two e4m3 codes (the low byte of the 16-bit half first) -> two f16, the PTX
+// conversion instruction for this pair of formats (exact: every e4m3 value
+// is an f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t word, int half) {
+  uint16_t lo16, hi16;
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(lo16), "=h"(hi16) : "r"(word));
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(half ? hi16 : lo16));
+  return r;
+}
+// 16 e4m3 codes -> 16 f16 (two 16-byte words).
+__device__ __forceinline__ void e4m3x16_to_f16x16(const uint4& in, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    o[2 * i] = e4m3x2_to_f16x2(w[i], 0);
+    o[2 * i + 1] = e4m3x2_to_f16x2(w[i], 1);
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// A copy lands as rows of 64 codes in the upper half of a 16 KB slot, 64-byte
+// swizzled (16-byte chunk c of row r at c ^ ((r >> 1) & 3)); a warp expands it
+// in place to the f16 rows of the 128-byte-swizzled panel the MMA reads
+// (chunk c of row r at c ^ (r & 7)), one lane per row.  Every step reads its
+// 32 rows before any lane writes, and its writes end below the rows later
+// steps read (f16 rows [32 t, 32 t + 32) end at byte 4096 (t + 1); the codes
+// of row 32 (t + 1) start at 8192 + 2048 (t + 1)).
+__device__ __forceinline__ void expand_row_f16(unsigned char* dst_row, int r, const uint4 (&q)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint4 lo, hi;
+    e4m3x16_to_f16x16(q[k], lo, hi);
+    *reinterpret_cast<uint4*>(dst_row + (((2 * k) ^ (r & 7)) << 4)) = lo;
+    *reinterpret_cast<uint4*>(dst_row + (((2 * k + 1) ^ (r & 7)) << 4)) = hi;
+  }
+}
+// A slot is expanded by one warp: every lane first reads all its rows' codes
+// (16 chunks), then converts and writes them, so all reads precede all writes
+// and the loads are in flight together.
+// K panel: 128 token rows of 64 dims; lane l takes rows l, l + 32, l + 64, l + 96.
+__device__ __forceinline__ void expand_k_panel_f16(unsigned char* slot, int lane) {
+  uint4 q[4][4];
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const int r = 32 * t + lane;
+    const uint4* src = reinterpret_cast<const uint4*>(slot + 8192 + 64 * r);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) q[t][k] = src[k ^ ((r >> 1) & 3)];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int t = 0; t < 4; ++t) expand_row_f16(slot + 128 * (32 * t + lane), 32 * t + lane, q[t]);
+  __syncwarp();
+}
+// V chunk: 4 panels of 32 token rows (codes of panel p at 8192 + 2048 p), lane
+// l takes row l of every panel; rows at and past rows_valid (beyond the
+// request's last token) become zeros.
+__device__ __forceinline__ void expand_v_chunk_f16(unsigned char* slot, int lane, int rows_valid) {
+  uint4 q[4][4];
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    const uint4* src = reinterpret_cast<const uint4*>(slot + 8192 + 2048 * p + 64 * lane);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) q[p][k] = lane < rows_valid ? src[k ^ ((lane >> 1) & 3)] : make_uint4(0, 0, 0, 0);
+  }
+  __syncwarp();
+#pragma unroll
+  for (int p = 0; p < 4; ++p) expand_row_f16(slot + 4096 * p + 128 * lane, lane, q[p]);
+  __syncwarp();
+}
+
+template <bool kOutF32, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_pair_kernel(const DecodeArgs a, const __grid_constant__ PairMaps maps) {
   extern __shared__ unsigned char smem_raw[];
@@ -163,7 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (i == kTailReady) cnt = 2;
       if (i == kSFree0 || i == kSFree0 + 1 || i == kPReady0 || i == kPReady0 + 1 || i == kOFree)
         cnt = 2 * kSoftmaxWarps;
-      if (i == kRed0 || i == kRed0 + 1 || i == kSum) cnt = kSoftmaxWarps;
+      if (i == kRed0 || i == kRed0 + 1 || i == kSum || i == kQRed) cnt = kSoftmaxWarps;
+      if (i == kQReady) cnt = 2 * kSoftmaxWarps;
+      // fp8: a slot's full barrier counts the odd CTA's expansion (the even
+      // CTA's own is done by the issuing warp itself)
       mbar_init(bar(base, i), cnt);
     }
     fence_barrier_init();
@@ -192,7 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // completes on the even CTA's full barrier of its slot, where the even
     // CTA's producer announces the bytes of both (the odd CTA only issues
     // its copies: an arrive at cluster scope per slot would cost a fence
-    // each).
+    // each).  With an fp8 cache every copy lands as e4m3 codes in the upper
+    // half of its slot, on a barrier of this CTA (kKLand / kVLand), and warps
+    // 1 / 11 expand it to f16 before the MMAs read it.
     const bool is_k = warp == 0;
     int rp = 0;            // slots of this ring used so far
     int tail_uses = 0;
@@ -229,6 +337,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto emit_q = [&](const WorkUnit& v) -> bool {
       if (q_units > 0 && !(ok = mbar_wait_warp(bar(base, kQFree), (q_units - 1) & 1, abort_flag))) return false;
       ++q_units;
+      if constexpr (kFp8) {
+        // this CTA's query lands here; the softmax warps convert it to f16
+        if (lane == 0) mbar_arrive_expect_tx(bar(base, kQLand), 9 * kQPanel);
+        __syncwarp();
+        if (lane < 9) {
+          const int row = v.req * H + 64 * rank;   // rows past the batch are zero-filled
+          if (lane < 8)
+            tma_load_2d(base + kOffQ + lane * kQPanel, &maps.q_nope, 64 * lane, row, bar(base, kQLand));
+          else
+            tma_load_2d(base + kOffQ + 8 * kQPanel, &maps.q_pe, 0, row, bar(base, kQLand));
+        }
+        return true;
+      }
       if (lane == 0 && rank == 0) mbar_arrive_expect_tx(bar(base, kQFull), 2 * 9 * kQPanel);
       __syncwarp();
       if (lane < 9) {
@@ -253,25 +374,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 9; ++j) {
         int slot;
         if (!(ok = next_slot(slot))) return false;
+        if constexpr (kFp8) {
+          const uint32_t land = bar(base, kKLand0 + slot);
+          if (lane == 0) mbar_arrive_expect_tx(land, nbox * P * 64);
+          __syncwarp();
+          if (lane < nbox) {
+            const uint32_t dst = base + kOffKRing + slot * kSlotBytes + 8192 + lane * P * 64;
+            if (j < 8)
+              tma_load_2d(dst, &maps.ckv_k, 64 * j, page * P, land);
+            else
+              tma_load_2d(dst, &maps.kpe_k, 0, page * P, land);
+          }
+          continue;
+        }
         const uint32_t full = map_to_rank(bar(base, kKFull0 + slot), lead);
         if (lane == 0 && rank == 0)
-          mbar_arrive_expect_tx(bar(base, kKFull0 + slot), nbox_both * P * 128 + (kStreamQ ? 2 * kQPanel : 0));
+          mbar_arrive_expect_tx(bar(base, kKFull0 + slot), nbox_both * P * 128);
         __syncwarp();
-        const uint32_t sbase = base + kOffKRing + slot * kKSlotBytes;
         if (lane < nbox) {
-          const uint32_t dst = sbase + lane * P * 128;
+          const uint32_t dst = base + kOffKRing + slot * kSlotBytes + lane * P * 128;
           if (j < 8)
             tma_load_2d_pair(dst, &maps.ckv_k, 64 * j, page * P, full);
           else
             tma_load_2d_pair(dst, &maps.kpe_k, 0, page * P, full);
-        } else if (kStreamQ && lane == 31) {
-          // this CTA's 64 query heads, dims [64 j, 64 j + 64) (rows past the
-          // batch are zero-filled)
-          const int row = v.req * H + 64 * rank;
-          if (j < 8)
-            tma_load_2d_pair(sbase + kSlotBytes, &maps.q_nope, 64 * j, row, full);
-          else
-            tma_load_2d_pair(sbase + kSlotBytes, &maps.q_pe, 0, row, full);
         }
       }
       return true;
@@ -284,6 +409,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rows <= 0) break;
         int slot;
         if (!(ok = next_slot(slot))) return false;
+        if constexpr (kFp8) {
+          // 32 rows of 4 x 64 codes (a page holds whole chunks: P >= 32); rows
+          // past kv_len are zeroed by the expansion
+          const uint32_t land = bar(base, kVLand0 + slot);
+          const int page = __shfl_sync(0xffffffffu, pages, (t - tok0) / P);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(land, kVChunkTok * 4 * 64);
+            tma_load_3d(base + kOffVRing + slot * kSlotBytes + 8192, &maps.ckv_v, 0, page * P + (t % P), 4 * rank,
+                        land);
+          }
+          __syncwarp();
+          continue;
+        }
         const uint32_t full = map_to_rank(bar(base, kVFull0 + slot), lead);
         if (stalled()) continue;
         const int ncopy = (rows + vbox - 1) / vbox;
@@ -331,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < n && ok; ++i) {
         const int pages = tile_pages(v, i);
         if (is_k) {
-          if (!kStreamQ && i == 0 && !emit_q(v)) break;
+          if (i == 0 && !emit_q(v)) break;
           if (!emit_k(v, i, pages)) break;
         } else if (!emit_v(v, i, pages)) {
           break;
@@ -349,14 +487,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t issue = lane == 0;
     bool ok = true;
     if (warp == 1) {
-      constexpr uint32_t id_qk = idesc_bf16_f32(128, 256, false, false);
+      constexpr uint32_t id_qk = kFp8 ? idesc_f16_f32(128, 256, false, false) : idesc_bf16_f32(128, 256, false, false);
       const uint64_t q_desc0 = smem_desc(base + kOffQ, 16, 1024, kSw128);
       const uint64_t k_desc0 = smem_desc(base + kOffKRing, 16, 1024, kSw128);
       int kc = 0, g = 0, unit_k = 0;
       for (int ui = u0; ui < u1 && ok; ++ui, ++unit_k) {
         const WorkUnit v = a.units[ui];
         const int n = tiles_of(v);
-        if (!kStreamQ && !(ok = mbar_wait_warp(bar(base, kQFull), unit_k & 1, abort_flag))) break;
+        // the unit's query: loaded (bf16) or converted to f16 in both CTAs (fp8)
+        if (!(ok = kFp8 ? mbar_wait_cl_warp(bar(base, kQReady), unit_k & 1, abort_flag)
+                        : mbar_wait_warp(bar(base, kQFull), unit_k & 1, abort_flag)))
+          break;
         for (int i = 0; i < n && ok; ++i, ++g) {
           if (g >= 2 && !(ok = mbar_wait_cl_warp(bar(base, kSFree0 + (g & 1)), ((g - 2) >> 1) & 1, abort_flag)))
             break;
@@ -364,11 +505,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d = tmem + kColS + 128 * (g & 1);
           for (int j = 0; j < 9; ++j, ++kc) {
             const int slot = kc % kKSlots;
-            if (!(ok = mbar_wait_warp(bar(base, kKFull0 + slot), (kc / kKSlots) & 1, abort_flag))) break;
+            const uint32_t par = (kc / kKSlots) & 1;
+            if constexpr (kFp8) {
+              // this CTA's copy expanded here (while the previous panel's MMAs
+              // run), the odd CTA's by its warp 1
+              if (!(ok = mbar_wait_warp(bar(base, kKLand0 + slot), par, abort_flag))) break;
+              expand_k_panel_f16(sm + kOffKRing + slot * kSlotBytes, lane);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (!(ok = mbar_wait_cl_warp(bar(base, kKFull0 + slot), par, abort_flag))) break;
+            } else if (!(ok = mbar_wait_warp(bar(base, kKFull0 + slot), par, abort_flag))) {
+              break;
+            }
             tc_fence_after();
-            const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((slot * kKSlotBytes) >> 4);
-            const uint64_t adesc = kStreamQ ? bdesc + static_cast<uint64_t>(kSlotBytes >> 4)
-                                            : q_desc0 + static_cast<uint64_t>((j * kQPanel) >> 4);
+            const uint64_t adesc = q_desc0 + static_cast<uint64_t>((j * kQPanel) >> 4);
+            const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((slot * kSlotBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               mma_pair(d, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2), id_qk,
@@ -379,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           commit_pair(bar(base, kSFull0 + (g & 1)), 3, issue);
         }
         if (!ok) break;
-        if (!kStreamQ) commit_pair(bar(base, kQFree), 3, issue);   // the unit's query no longer read
+        commit_pair(bar(base, kQFree), 3, issue);   // the unit's query no longer read
       }
       if (!ok && lane == 0) report_error(a.err, kErrTimeout);
       // drain: every MMA issued completes before TMEM is freed
@@ -387,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_wait_cl_drain(bar(base, kFinal), 0);
       __syncwarp();
     } else {
-      constexpr uint32_t id_pv = idesc_bf16_f32(128, 256, false, true);
+      constexpr uint32_t id_pv = kFp8 ? idesc_f16_f32(128, 256, false, true) : idesc_bf16_f32(128, 256, false, true);
       const uint64_t p_desc0 = smem_desc(base + kOffP, 16, 1024, kSw128);
       const bool v32 = P >= kVChunkTok;
       const uint64_t v_desc0 = smem_desc(base + kOffVRing, v32 ? 4096 : 2048, 1024, kSw128);
@@ -406,7 +557,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t pbuf = (g % kPBufs) * kPBuf;
           for (int c = 0; c < nch; ++c, ++vc) {
             const int slot = vc % kVSlots;
-            if (!(ok = mbar_wait_warp(bar(base, kVFull0 + slot), (vc / kVSlots) & 1, abort_flag))) break;
+            const uint32_t par = (vc / kVSlots) & 1;
+            if constexpr (kFp8) {
+              if (!(ok = mbar_wait_warp(bar(base, kVLand0 + slot), par, abort_flag))) break;
+              const int rows = min(kVChunkTok, valid - kVChunkTok * c);
+              expand_v_chunk_f16(sm + kOffVRing + slot * kSlotBytes, lane, rows);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (!(ok = mbar_wait_cl_warp(bar(base, kVFull0 + slot), par, abort_flag))) break;
+            } else if (!(ok = mbar_wait_warp(bar(base, kVFull0 + slot), par, abort_flag))) {
+              break;
+            }
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
@@ -433,7 +594,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
   } else if (warp == 1 || warp == kPvIssuerWarp) {
-    // (odd CTA: no role)
+    // ================= odd CTA: fp8 expanders (else no role) =================
+    // Warp 1 expands this CTA's K copies and warp 11 its V chunks, in the
+    // order the even CTA's issuers consume them, each then arriving on the
+    // even CTA's full barrier of the slot.
+    if constexpr (kFp8) {
+      const bool is_k = warp == 1;
+      bool ok = true;
+      int cnt = 0;   // copies of this ring expanded
+      for (int ui = u0; ui < u1 && ok; ++ui) {
+        const WorkUnit v = a.units[ui];
+        const int n = tiles_of(v);
+        for (int i = 0; i < n && ok; ++i) {
+          const int valid = min(kT, v.tok_end - (v.tok_begin + i * kT));
+          const int per_tile = is_k ? 9 : (valid + kVChunkTok - 1) / kVChunkTok;
+          for (int c = 0; c < per_tile; ++c, ++cnt) {
+            const int nsl = is_k ? kKSlots : kVSlots;
+            const int slot = cnt % nsl;
+            if (!(ok = mbar_wait_warp(bar(base, (is_k ? kKLand0 : kVLand0) + slot), (cnt / nsl) & 1, abort_flag)))
+              break;
+            unsigned char* sl = sm + (is_k ? kOffKRing : kOffVRing) + slot * kSlotBytes;
+            const int rows = min(kVChunkTok, valid - kVChunkTok * c);
+            if (is_k)
+              expand_k_panel_f16(sl, lane);
+            else
+              expand_v_chunk_f16(sl, lane, rows);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(map_to_rank(bar(base, (is_k ? kKFull0 : kVFull0) + slot), lead));
+          }
+        }
+      }
+      if (!ok && lane == 0) report_error(a.err, kErrTimeout);
+    }
   } else {
     // ================= softmax / epilogue (warps 2..9, both CTAs) =================
     const int sw = warp - kFirstSoftmaxWarp;
@@ -454,6 +647,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n = tiles_of(u);
       float ref = 0.f;                       // the head's reference (the same in its four threads)
       float lx = 0.f, lr = 0.f;              // this thread's share of the row sums
+      float cq = c;                          // score scale of this thread's head
+      if constexpr (kFp8) {
+        // ---- the unit's query (this CTA's 64 heads) from bf16 to f16 in
+        // place: row hl is scaled by 2^e so that its largest magnitude lies
+        // in [2^14, 2^15), and the scores by 2^-e.  The head's four threads
+        // take 16-byte chunks part, part + 4, .. of the row's 72 (9 panels x
+        // 8, 128-byte swizzle) ----
+        if (!(ok = mbar_wait_warp(bar(base, kQLand), unit_k & 1, abort_flag))) break;
+        const unsigned char* qrow = sm + kOffQ + hl * 128;
+        auto qchunk = [&](int idx) -> uint4* {
+          return reinterpret_cast<uint4*>(const_cast<unsigned char*>(qrow) + (idx >> 3) * kQPanel +
+                                          (((idx & 7) ^ (hl & 7)) << 4));
+        };
+        float mx = 0.f;
+        for (int idx = part; idx < 72; idx += 4) {
+          const uint4 v = *qchunk(idx);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xffff0000u))));
+        }
+        float* qred = reinterpret_cast<float*>(sm + kOffQRed);
+        qred[part * 64 + hl] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(base, kQRed));
+        if (!(ok = mbar_wait_warp(bar(base, kQRed), unit_k & 1, abort_flag))) break;
+        const float rm = fmaxf(fmaxf(qred[hl], qred[64 + hl]), fmaxf(qred[128 + hl], qred[192 + hl]));
+        // rows of zeros (heads past H) keep e = 0
+        int e = 0;
+        if (rm > 0.f && rm < INFINITY) e = min(max(14 - (((__float_as_int(rm) >> 23) & 0xff) - 127), -100), 100);
+        const float up = __int_as_float((127 + e) << 23);
+        for (int idx = part; idx < 72; idx += 4) {
+          uint4* ch = qchunk(idx);
+          const uint4 v = *ch;
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const __half2 h2 = __floats2half2_rn(__uint_as_float(w[k] << 16) * up, __uint_as_float(w[k] & 0xffff0000u) * up);
+            o[k] = *reinterpret_cast<const uint32_t*>(&h2);
+          }
+          *ch = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) arrive_lead(bar(base, kQReady), rank);
+        cq = c * __int_as_float((127 - e) << 23);
+      }
       for (int i = 0; i < n && ok; ++i, ++g) {
         const bool first = i == 0;
         // ---- scores: this thread's head, 64 tokens ----
@@ -470,8 +711,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nvalid = u.tok_end - (u.tok_begin + i * kT + kHalfT * tq + 64 * ch);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            y[j] = j < nvalid ? __uint_as_float(v0[j]) * c : -INFINITY;
-            y[32 + j] = 32 + j < nvalid ? __uint_as_float(v1[j]) * c : -INFINITY;
+            y[j] = j < nvalid ? __uint_as_float(v0[j]) * cq : -INFINITY;
+            y[32 + j] = 32 + j < nvalid ? __uint_as_float(v1[j]) * cq : -INFINITY;
           }
 #pragma unroll
           for (int j = 0; j < 64; ++j) mx = fmaxf(mx, y[j]);
@@ -501,11 +742,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const float p0 = fast_exp2(y[2 * j] - ref), p1 = fast_exp2(y[2 * j + 1] - ref);
-            const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
-            const uint32_t w = *reinterpret_cast<const uint32_t*>(&b2);
-            pk[j] = w;
             sx += p0 + p1;
-            sr += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+            if constexpr (kFp8) {
+              const __half2 h2 = __floats2half2_rn(p0, p1);
+              pk[j] = *reinterpret_cast<const uint32_t*>(&h2);
+              const float2 f2 = __half22float2(h2);
+              sr += f2.x + f2.y;
+            } else {
+              const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(&b2);
+              pk[j] = w;
+              sr += __uint_as_float(w << 16) + __uint_as_float(w & 0xffff0000u);
+            }
           }
           lx = first ? sx : fmaf(lx, alpha, sx);
           lr = first ? sr : fmaf(lr, alpha, sr);
@@ -637,12 +885,12 @@ extern "C" int mla_test_set_pair_stall(int copy) {
 #endif
 
 namespace {
-template <bool kOutF32>
+template <bool kOutF32, bool kFp8>
 cudaError_t set_pair_attributes() {
   static bool done = false;   // set once, before any stream capture
   if (!done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<kOutF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(decode_pair_kernel<kOutF32, kFp8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
     done = true;
   }
@@ -666,26 +914,35 @@ cudaLaunchConfig_t pair_config(int clusters, cudaLaunchAttribute* attr) {
 
 cudaError_t decode_pair_max_workers(int* workers) {
   *workers = 0;
-  cudaError_t e = set_pair_attributes<true>();
-  if (e == cudaSuccess) e = set_pair_attributes<false>();
+  cudaError_t e = set_pair_attributes<true, false>();
+  if (e == cudaSuccess) e = set_pair_attributes<false, false>();
+  if (e == cudaSuccess) e = set_pair_attributes<true, true>();
+  if (e == cudaSuccess) e = set_pair_attributes<false, true>();
   if (e != cudaSuccess) return e;
+  // the instantiations share the launch shape and the shared-memory size
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config(1, attr);
-  int clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&clusters, decode_pair_kernel<false>, &cfg);
+  int clusters = 0, clusters_fp8 = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, decode_pair_kernel<false, false>, &cfg);
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&clusters_fp8, decode_pair_kernel<false, true>, &cfg);
   if (e != cudaSuccess) return e;
-  *workers = clusters;
+  *workers = clusters < clusters_fp8 ? clusters : clusters_fp8;
   return cudaSuccess;
 }
 
-cudaError_t launch_decode_pair(const DecodeArgs& a, const PairMaps& maps, bool out_f32, cudaStream_t s) {
-  cudaError_t e = out_f32 ? set_pair_attributes<true>() : set_pair_attributes<false>();
+cudaError_t launch_decode_pair(const DecodeArgs& a, const PairMaps& maps, bool out_f32, bool kv_fp8,
+                               cudaStream_t s) {
+  cudaError_t e = kv_fp8 ? (out_f32 ? set_pair_attributes<true, true>() : set_pair_attributes<false, true>())
+                         : (out_f32 ? set_pair_attributes<true, false>() : set_pair_attributes<false, false>());
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute attr[1];
   cudaLaunchConfig_t cfg = pair_config(a.n_workers, attr);
   cfg.stream = s;
-  return out_f32 ? cudaLaunchKernelEx(&cfg, decode_pair_kernel<true>, a, maps)
-                 : cudaLaunchKernelEx(&cfg, decode_pair_kernel<false>, a, maps);
+  if (kv_fp8)
+    return out_f32 ? cudaLaunchKernelEx(&cfg, decode_pair_kernel<true, true>, a, maps)
+                   : cudaLaunchKernelEx(&cfg, decode_pair_kernel<false, true>, a, maps);
+  return out_f32 ? cudaLaunchKernelEx(&cfg, decode_pair_kernel<true, false>, a, maps)
+                 : cudaLaunchKernelEx(&cfg, decode_pair_kernel<false, false>, a, maps);
 }
 
 }  // namespace mla

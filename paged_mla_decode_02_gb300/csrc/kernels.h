@@ -89,16 +89,20 @@ cudaError_t decode_tc_max_workers(int* workers);
 // CTA-pair kernel (one tcgen05 MMA over both SMs of a cluster, cta_group::2):
 // persistent, one pair per worker; split requests leave normalised partials
 // (part_offset layout, lse copy 0) for launch_merge.
+// An fp8 (e4m3) cache is read through byte maps with a 64-byte swizzle (the
+// same boxes in elements) and needs page_size >= 32.
 struct PairMaps {
   CUtensorMap q_nope;   // [B*H, 512] bf16, box 64 x 64 (64 heads)
   CUtensorMap q_pe;     // [B*H, 64] bf16, box 64 x 64
-  CUtensorMap ckv_k;    // [pages*P, 512] bf16, box 64 x P
-  CUtensorMap kpe_k;    // [pages*P, 64] bf16, box 64 x P
+  CUtensorMap ckv_k;    // [pages*P, 512] bf16 / e4m3, box 64 x P
+  CUtensorMap kpe_k;    // [pages*P, 64] bf16 / e4m3, box 64 x P
   CUtensorMap ckv_v;    // (64, pages*P, 8 panels) view of ckv, box 64 x min(P, 32) x 4 panels
 };
-cudaError_t launch_decode_pair(const DecodeArgs& a, const PairMaps& maps, bool out_f32, cudaStream_t s);
+cudaError_t launch_decode_pair(const DecodeArgs& a, const PairMaps& maps, bool out_f32, bool kv_fp8,
+                               cudaStream_t s);
 bool encode_pair_maps(PairMaps* maps, const void* q_nope, const void* q_pe, const void* ckv_cache,
-                      const void* kpe_cache, int batch, int num_heads, int page_size, int num_pages);
+                      const void* kpe_cache, int batch, int num_heads, int page_size, int num_pages,
+                      bool kv_fp8);
 cudaError_t decode_pair_max_workers(int* workers);
 
 // LSE merge of split partials (and zero-fill of empty requests); the mma.sync

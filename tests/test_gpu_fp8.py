@@ -1,7 +1,9 @@
-"""fp8 (e4m3) caches on both kernels against the oracle on the dequantised
-values: the tcgen05 kernel expands each copied tile to bf16 in shared memory
-(every e4m3 value is exact in bf16) and folds kv_scale into the scores and
-the output; the mma.sync kernel converts while staging."""
+"""fp8 (e4m3) caches on every kernel against the oracle on the dequantised
+values: the CTA-pair kernel expands each copied tile to f16 in shared memory
+and multiplies in f16 (the query converted once per unit under a
+power-of-two row scale, P rounded to f16), the one-CTA tcgen05 kernel expands
+to bf16 (every e4m3 value is exact in both), both fold kv_scale into the
+scores and the output; the mma.sync kernel converts while staging."""
 from __future__ import annotations
 
 import numpy as np
@@ -15,7 +17,7 @@ from paged_mla_decode_02_gb300 import mla
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = ["tcgen05", "mma_sync"]
+KERNELS = ["pair", "tcgen05", "mma_sync"]
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -45,12 +47,33 @@ def test_fp8_tcgen05_matches_bf16_cache_of_the_same_values():
     assert np.abs(o8 - o16).max() < 1e-4 and np.abs(l8 - l16).max() < 1e-4
 
 
-def test_fp8_tcgen05_rejects_16_token_pages():
+@pytest.mark.parametrize("kernel", ["pair", "tcgen05", "default"])
+def test_fp8_tensor_core_kernels_reject_16_token_pages(kernel):
     x = I.make_inputs("f8p16", [40, 9], 16, 16, seed=2, kv_dtype="fp8_e4m3")
     d = to_device(x)
     with pytest.raises(mla.MLAError) as ei:
-        run_decode(x, d, "tcgen05", torch.float32)
+        run_decode(x, d, kernel, torch.float32)
     assert ei.value.status == mla.ERR_UNSUPPORTED
+
+
+def test_fp8_pair_query_row_scales():
+    """Query rows of very different magnitudes (2^-20 .. 2^4 times N(0,1), one
+    row of zeros): each row is converted to f16 under its own power-of-two
+    scale, so every row keeps its precision (unscaled, f16 would flush the
+    small rows' values below 2^-24 to zero)."""
+    x = I.make_inputs("f8q", [700, 130], 128, 64, seed=43, kv_dtype="fp8_e4m3")
+    rng = np.random.Generator(np.random.PCG64(7))
+    exps = rng.integers(-20, 5, size=(x.batch, x.num_heads)).astype(np.float64)
+    exps[0, 5] = np.nan                                   # a zero row
+    for name in ("q_nope", "q_pe"):
+        q = O.decode_bf16(getattr(x, name))
+        f = np.where(np.isnan(exps), 0.0, np.exp2(np.nan_to_num(exps)))[..., None]
+        q32 = torch.from_numpy((q * f).astype(np.float32)).to(torch.bfloat16)
+        setattr(x, name, q32.view(torch.int16).numpy().view(np.uint16))
+    d = to_device(x)
+    out, lse = run_decode(x, d, "pair", torch.float32)
+    ref_out, ref_lse = O.mla_decode_inputs(x)
+    assert_parity(out, lse, ref_out, ref_lse, "fp8 pair, scaled query rows")
 
 
 @pytest.mark.parametrize("kernel", KERNELS)

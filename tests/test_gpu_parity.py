@@ -249,8 +249,6 @@ def test_bad_arguments_are_errors():
 def test_full_size_config(kernel, cfg):
     # the launch configuration the bench times (the same plan over the whole
     # batch), every output element against the oracle
-    if kernel == "pair" and cfg == "fp8":
-        pytest.skip("the CTA-pair kernel takes bf16 caches (fp8 runs on the one-CTA kernel)")
     x = _config(cfg)
     d = to_device(x)
     out, lse = run_decode(x, d, kernel, torch.float32)
@@ -263,8 +261,7 @@ def test_full_size_config(kernel, cfg):
 
 @pytest.mark.parametrize("cfg", ["deepseek", "fp8"])
 def test_default_kernel_full_size(cfg):
-    # DEFAULT plans for the CTA-pair kernel; a bf16 cache runs on it, an fp8
-    # cache on the one-CTA kernel over the same (256-token) partition
+    # DEFAULT plans for the CTA-pair kernel, which runs both caches here
     x = _config(cfg)
     d = to_device(x)
     dec = mla.MLADecoder(x.batch, x.num_heads, "default")
@@ -280,8 +277,8 @@ def test_default_kernel_full_size(cfg):
 
 @pytest.mark.parametrize("lens", [[20000, 1, 777, 0, 300], [9000] * 9 + [40]])
 def test_default_kernel_fp8_split_requests(lens):
-    # the one-CTA kernel combining split requests in place over a partition
-    # made for the CTA pair; repeated runs are bit-identical
+    # fp8 split requests on the default kernel (partials combined by the merge
+    # kernel); repeated runs are bit-identical
     x = I.make_inputs("default_fp8", lens, 128, 64, seed=23, kv_dtype="fp8_e4m3")
     d = to_device(x)
     dec = mla.MLADecoder(x.batch, x.num_heads, "default")

@@ -77,6 +77,4 @@ def test_dominant_token_in_split_requests(kernel, gap):
 
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_dominant_token_fp8_cache(kernel):
-    if kernel == "pair":
-        pytest.skip("the CTA-pair kernel takes bf16 caches")
     _check(_batch(100.0, 128, "fp8_e4m3"), kernel, "fp8 gap 100")
