@@ -43,11 +43,12 @@
 // the lse uses the former).
 //
 // fp8 (e4m3) caches (pages of 32 or 64 tokens): the copies land as codes in
-// the upper half of each ring slot and are expanded in place to f16 -- in the
-// even CTA by the issuing warp itself while the previous MMAs run, in the odd
-// CTA by warps 1 and 11, which then signal the even CTA -- and both products
-// take f16 operands: the query converted once per unit (a power-of-two scale
-// per head row), P rounded to f16.
+// the upper half of each ring slot and are expanded in place to f16 -- K
+// panels in the even CTA by the QK issuer while the previous MMAs run and in
+// the odd CTA by its warp 1, V chunks by the V producers one copy behind
+// their issue point -- and both products take f16 operands: the query
+// converted once per unit (a power-of-two scale per head row), P rounded to
+// f16.
 //
 // Every wait is bounded (2 s); on expiry the kernel records
 // MLA_ERR_DEVICE_TIMEOUT, lets its copies and MMAs land, frees TMEM and
@@ -268,8 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         cnt = 2 * kSoftmaxWarps;
       if (i == kRed0 || i == kRed0 + 1 || i == kSum || i == kQRed) cnt = kSoftmaxWarps;
       if (i == kQReady) cnt = 2 * kSoftmaxWarps;
-      // fp8: a slot's full barrier counts the odd CTA's expansion (the even
-      // CTA's own is done by the issuing warp itself)
+      // fp8: a K slot's full barrier counts the odd CTA's expansion (the even
+      // CTA's own is done by the QK issuer itself); a V slot's counts both
+      // CTAs' V producers
+      if (kFp8 && i >= kVFull0 && i < kVFull0 + kVSlots) cnt = 2;
       mbar_init(bar(base, i), cnt);
     }
     fence_barrier_init();
@@ -299,12 +302,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     // CTA's producer announces the bytes of both (the odd CTA only issues
     // its copies: an arrive at cluster scope per slot would cost a fence
     // each).  With an fp8 cache every copy lands as e4m3 codes in the upper
-    // half of its slot, on a barrier of this CTA (kKLand / kVLand), and warps
-    // 1 / 11 expand it to f16 before the MMAs read it.
+    // half of its slot, on a barrier of this CTA (kKLand / kVLand), and is
+    // expanded to f16 before the MMAs read it: K panels by warp 1 (the QK
+    // issuer in the even CTA), V chunks by this warp, one copy behind.
     const bool is_k = warp == 0;
     int rp = 0;            // slots of this ring used so far
     int tail_uses = 0;
     bool ok = true;
+    // fp8 V: the chunk issued last, expanded once the next one is issued
+    int pend_rp = -1, pend_rows = 0;
+    auto expand_pending_v = [&]() -> bool {
+      if (pend_rp < 0) return true;
+      const int slot = pend_rp % kVSlots;
+      if (!(ok = mbar_wait_warp(bar(base, kVLand0 + slot), (pend_rp / kVSlots) & 1, abort_flag))) return false;
+      expand_v_chunk_f16(sm + kOffVRing + slot * kSlotBytes, lane, pend_rows);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) arrive_lead(bar(base, kVFull0 + slot), rank);
+      pend_rp = -1;
+      return true;
+    };
     int q_units = 0;       // query loads issued
     const int vbox = P >= kVChunkTok ? kVChunkTok : 16;
     const int nslots = is_k ? kKSlots : kVSlots;
@@ -410,8 +427,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int slot;
         if (!(ok = next_slot(slot))) return false;
         if constexpr (kFp8) {
-          // 32 rows of 4 x 64 codes (a page holds whole chunks: P >= 32); rows
-          // past kv_len are zeroed by the expansion
+          // 32 rows of 4 x 64 codes (a page holds whole chunks: P >= 32); the
+          // previous chunk is expanded (rows past kv_len zeroed) while this
+          // one is in flight, then both CTAs' expansions count on the even
+          // CTA's full barrier
           const uint32_t land = bar(base, kVLand0 + slot);
           const int page = __shfl_sync(0xffffffffu, pages, (t - tok0) / P);
           if (lane == 0) {
@@ -420,6 +439,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         land);
           }
           __syncwarp();
+          if (!expand_pending_v()) return false;
+          pend_rp = rp - 1;
+          pend_rows = rows;
           continue;
         }
         const uint32_t full = map_to_rank(bar(base, kVFull0 + slot), lead);
@@ -476,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    if (kFp8 && !is_k && ok) expand_pending_v();
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
   } else if ((warp == 1 || warp == kPvIssuerWarp) && rank == 0) {
     // ================= MMA issuers (even CTA, whole warp, lane 0 issues) =================
@@ -559,11 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int slot = vc % kVSlots;
             const uint32_t par = (vc / kVSlots) & 1;
             if constexpr (kFp8) {
-              if (!(ok = mbar_wait_warp(bar(base, kVLand0 + slot), par, abort_flag))) break;
-              const int rows = min(kVChunkTok, valid - kVChunkTok * c);
-              expand_v_chunk_f16(sm + kOffVRing + slot * kSlotBytes, lane, rows);
-              fence_proxy_async_smem();
-              __syncwarp();
+              // expanded in both CTAs by their V producers
               if (!(ok = mbar_wait_cl_warp(bar(base, kVFull0 + slot), par, abort_flag))) break;
             } else if (!(ok = mbar_wait_warp(bar(base, kVFull0 + slot), par, abort_flag))) {
               break;
@@ -595,11 +614,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 || warp == kPvIssuerWarp) {
     // ================= odd CTA: fp8 expanders (else no role) =================
-    // Warp 1 expands this CTA's K copies and warp 11 its V chunks, in the
-    // order the even CTA's issuers consume them, each then arriving on the
-    // even CTA's full barrier of the slot.
-    if constexpr (kFp8) {
-      const bool is_k = warp == 1;
+    // Warp 1 expands this CTA's K copies in the order the even CTA's QK
+    // issuer consumes them, each then arriving on the even CTA's full barrier
+    // of the slot (V chunks are expanded by the V producers).
+    if (kFp8 && warp == 1) {
+      const bool is_k = true;
       bool ok = true;
       int cnt = 0;   // copies of this ring expanded
       for (int ui = u0; ui < u1 && ok; ++ui) {
