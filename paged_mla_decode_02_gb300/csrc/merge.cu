@@ -22,178 +22,165 @@ constexpr int kChunk = 32;                     // dims per block (the largest)
 // into more groups.
 __host__ __device__ inline int merge_chunk(int H) { return H <= 32 ? 8 : kChunk; }
 
-// One block per (request, 32-dim chunk).  The partials are read in their
-// [slot][d/8][h][d%8] layout, consecutive threads on consecutive heads
-// (coalesced); the merged chunk is staged in shared memory and written out
-// row by row, 64 or 128 contiguous bytes per head.  A long request can have
-// a partial from every worker, so the slots are spread over the threads too:
-// the per-head maximum and weight sum are reduced by G adjacent lanes per
-// head, and with fewer than 32 heads the weighted sum is split over S thread
-// groups (each in slot order, the groups then added in group order), every
-// group loading kAhead slots before accumulating them.
+// Work items: (merged request, chunk of C dims), looped over by the grid in
+// strides (the grid is sized for the plan's capacity, so a re-planned batch
+// replays with the same launch and no block idles on an empty item).  The
+// partials are read in their [slot][d/8][h][d%8] layout, consecutive threads
+// on consecutive heads (coalesced); the merged chunk is staged in shared
+// memory and written out row by row, 16 or 64 contiguous bytes per head.
+// Each thread folds the slots into a running (maximum, weight sum, weighted
+// output) in slot order, a partial and its log-sum-exp loaded together,
+// two (four with few heads) slots at a time: an item takes one memory round
+// trip per two (four) slots.  With few heads the slots are split over S thread groups (every
+// S-th slot) whose states are then combined in group order.
+__device__ __forceinline__ void fold_state(float& M, float& W, float4& acc, float l, const float4& o) {
+  if (l == -INFINITY) return;   // a partial with no weight
+  const float Mn = fmaxf(M, l);
+  const float sa = __expf(M - Mn), sb = __expf(l - Mn);   // M = -inf: sa = 0 (acc, W are 0)
+  acc.x = acc.x * sa + o.x * sb;
+  acc.y = acc.y * sa + o.y * sb;
+  acc.z = acc.z * sa + o.z * sb;
+  acc.w = acc.w * sa + o.w * sb;
+  W = W * sa + sb;
+  M = Mn;
+}
+
 template <bool kOutF32>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a) {
   // launched as a programmatic dependent of the decode kernel: wait for it
   // (a no-op in a plain launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int e = blockIdx.x;
-  if (e >= a.params->n_merge) return;
-  const MergeEntry me = a.merge[e];
   const int H = a.num_heads;
-  const int n = me.n_slots;
-  const int dq = blockIdx.y;
   const int C = merge_chunk(H);
+  const int nchunk = kDCkv / C;
+  const int n_items = a.params->n_merge * nchunk;
+  const int items = (C / 4) * H;   // 4-dim items of one chunk
   __shared__ float tile[kMaxHeads][kChunk + 1];
-  __shared__ float s_max[kMaxHeads], s_inv[kMaxHeads];
-  __shared__ float4 s_part[kMergeThreads];
+  __shared__ float4 s_acc[kMergeThreads];
+  __shared__ float2 s_mw[kMergeThreads];
   const int t = threadIdx.x;
-  constexpr int kAhead = 4;
-  {
-    int G = 1;   // lanes per head: a power of two, G * H <= threads
-    while (G < 32 && 2 * G * H <= kMergeThreads) G *= 2;
-    const int h = t / G, g = t % G;
-    const bool act = h < H;
-    // one pass, running maximum and the weight sum relative to it; four
-    // slots' loads issued before they are folded in
-    float M = -INFINITY, wsum = 0.f;
-    if (act)
-      for (int i0 = g; i0 < n; i0 += 4 * G) {
-        float l[4];
+  for (int w = blockIdx.x; w < n_items; w += gridDim.x) {
+    const int e = w / nchunk, dq = w - e * nchunk;
+    const MergeEntry me = a.merge[e];
+    const int n = me.n_slots;
+    const size_t row0 = static_cast<size_t>(me.req) * H;
+    if (items >= kMergeThreads) {
+      // several items per thread
+      constexpr int kItems = (kChunk / 4) * kMaxHeads / kMergeThreads;
+      constexpr int kAhead = 2;
+      float4 acc[kItems];
+      float M[kItems], W[kItems];
+      int hk[kItems], dg[kItems];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          l[j] = i0 + j * G < n ? a.lse_part[lse_part_offset(me.first_slot + i0 + j * G, 0, h, H)] : -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (l[j] == -INFINITY) continue;
-          const float Mn = fmaxf(M, l[j]);
-          wsum = wsum * __expf(M - Mn) + __expf(l[j] - Mn);
-          M = Mn;
-        }
+      for (int k = 0; k < kItems; ++k) {
+        acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        M[k] = -INFINITY;
+        W[k] = 0.f;
+        const int idx = t + k * kMergeThreads;
+        dg[k] = idx < items ? idx / H : -1;
+        hk[k] = idx - (idx / H) * H;
       }
-    for (int off = G / 2; off > 0; off >>= 1) {
-      const float M2 = __shfl_xor_sync(0xffffffffu, M, off);
-      const float w2 = __shfl_xor_sync(0xffffffffu, wsum, off);
-      const float Mn = fmaxf(M, M2);
-      if (Mn != -INFINITY) {
-        wsum = (M == -INFINITY ? 0.f : wsum * __expf(M - Mn)) + (M2 == -INFINITY ? 0.f : w2 * __expf(M2 - Mn));
-        M = Mn;
+      for (int i0 = 0; i0 < n; i0 += kAhead) {
+        float4 o[kAhead][kItems];
+        float l[kAhead][kItems];
+#pragma unroll
+        for (int j = 0; j < kAhead; ++j)
+#pragma unroll
+          for (int k = 0; k < kItems; ++k)
+            if (dg[k] >= 0 && i0 + j < n) {
+              const int slot = me.first_slot + i0 + j;
+              o[j][k] = *reinterpret_cast<const float4*>(a.o_part + part_offset(slot, hk[k], dq * C + 4 * dg[k], H));
+              l[j][k] = a.lse_part[lse_part_offset(slot, 0, hk[k], H)];
+            }
+#pragma unroll
+        for (int j = 0; j < kAhead; ++j)
+#pragma unroll
+          for (int k = 0; k < kItems; ++k)
+            if (dg[k] >= 0 && i0 + j < n) fold_state(M[k], W[k], acc[k], l[j][k], o[j][k]);
       }
-    }
-    if (act && g == 0) {
-      s_max[h] = M;
-      s_inv[h] = n > 0 ? 1.f / wsum : 0.f;
-      if (dq == 0) a.lse[static_cast<size_t>(me.req) * H + h] = n > 0 ? M + __logf(wsum) : -INFINITY;
-    }
-  }
-  __syncthreads();
-  const int items = (C / 4) * H;   // 4-dim items of this chunk
-  if (items >= kMergeThreads) {
-    // (kChunk / 4) * H <= kItems * kMergeThreads: several items per thread
-    constexpr int kItems = (kChunk / 4) * kMaxHeads / kMergeThreads;
-    float4 acc[kItems];
-    int hk[kItems], dk[kItems];
 #pragma unroll
-    for (int k = 0; k < kItems; ++k) {
-      acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-      const int idx = t + k * kMergeThreads;
-      const int dg = idx / H;
-      hk[k] = idx - dg * H;
-      dk[k] = idx < items ? dq * C + 4 * dg : -1;
-    }
-    for (int i0 = 0; i0 < n; i0 += kAhead) {
-      float4 o[kAhead][kItems];
-      float l[kAhead][kItems];
-#pragma unroll
-      for (int j = 0; j < kAhead; ++j)
-#pragma unroll
-        for (int k = 0; k < kItems; ++k)
-          if (dk[k] >= 0 && i0 + j < n) {
-            o[j][k] = *reinterpret_cast<const float4*>(a.o_part + part_offset(me.first_slot + i0 + j, hk[k], dk[k], H));
-            l[j][k] = a.lse_part[lse_part_offset(me.first_slot + i0 + j, 0, hk[k], H)];
-          }
-#pragma unroll
-      for (int j = 0; j < kAhead; ++j)
-#pragma unroll
-        for (int k = 0; k < kItems; ++k)
-          if (dk[k] >= 0 && i0 + j < n) {
-            const float w = __expf(l[j][k] - s_max[hk[k]]);
-            acc[k].x += w * o[j][k].x; acc[k].y += w * o[j][k].y; acc[k].z += w * o[j][k].z; acc[k].w += w * o[j][k].w;
-          }
-    }
-#pragma unroll
-    for (int k = 0; k < kItems; ++k) {
-      if (dk[k] >= 0) {
-        const int h = hk[k], c = dk[k] - dq * C;
-        const float inv = s_inv[h];
+      for (int k = 0; k < kItems; ++k) {
+        if (dg[k] < 0) continue;
+        const int h = hk[k], c = 4 * dg[k];
+        const float inv = W[k] > 0.f ? 1.f / W[k] : 0.f;
         tile[h][c] = acc[k].x * inv;
         tile[h][c + 1] = acc[k].y * inv;
         tile[h][c + 2] = acc[k].z * inv;
         tile[h][c + 3] = acc[k].w * inv;
+        if (dq == 0 && dg[k] == 0) a.lse[row0 + h] = W[k] > 0.f ? M[k] + __logf(W[k]) : -INFINITY;
+      }
+    } else {
+      // one item per thread; S groups of threads take every S-th slot, each
+      // loading kAheadSmall slots before folding them in
+      constexpr int kAheadSmall = 4;
+      int S = 1;
+      while (2 * S * items <= kMergeThreads) S *= 2;
+      const int item = t % items, sg = t / items;
+      const int dgi = item / H, h = item - dgi * H, d = dq * C + 4 * dgi;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      float M = -INFINITY, W = 0.f;
+      if (sg < S) {
+        for (int i0 = sg; i0 < n; i0 += S * kAheadSmall) {
+          float4 o[kAheadSmall];
+          float l[kAheadSmall];
+#pragma unroll
+          for (int j = 0; j < kAheadSmall; ++j)
+            if (i0 + S * j < n) {
+              o[j] = *reinterpret_cast<const float4*>(a.o_part + part_offset(me.first_slot + i0 + S * j, h, d, H));
+              l[j] = a.lse_part[lse_part_offset(me.first_slot + i0 + S * j, 0, h, H)];
+            }
+#pragma unroll
+          for (int j = 0; j < kAheadSmall; ++j)
+            if (i0 + S * j < n) fold_state(M, W, acc, l[j], o[j]);
+        }
+      }
+      s_acc[t] = acc;
+      s_mw[t] = make_float2(M, W);
+      __syncthreads();
+      if (t < items) {
+        for (int q = 1; q < S; ++q) {
+          const float2 mw = s_mw[t + q * items];
+          if (mw.y <= 0.f) continue;
+          const float4 aq = s_acc[t + q * items];
+          const float Mn = fmaxf(M, mw.x);
+          const float sa = __expf(M - Mn), sb = __expf(mw.x - Mn);
+          acc.x = acc.x * sa + aq.x * sb;
+          acc.y = acc.y * sa + aq.y * sb;
+          acc.z = acc.z * sa + aq.z * sb;
+          acc.w = acc.w * sa + aq.w * sb;
+          W = W * sa + mw.y * sb;
+          M = Mn;
+        }
+        const int c = 4 * dgi;
+        const float inv = W > 0.f ? 1.f / W : 0.f;
+        tile[h][c] = acc.x * inv;
+        tile[h][c + 1] = acc.y * inv;
+        tile[h][c + 2] = acc.z * inv;
+        tile[h][c + 3] = acc.w * inv;
+        if (dq == 0 && dgi == 0) a.lse[row0 + h] = W > 0.f ? M + __logf(W) : -INFINITY;
       }
     }
-  } else {
-    // one item per thread; S groups of threads take every S-th slot, each
-    // loading kAheadSmall slots before folding them in
-    constexpr int kAheadSmall = 8;
-    int S = 1;
-    while (2 * S * items <= kMergeThreads) S *= 2;
-    const int item = t % items, sg = t / items;
-    const int dg = item / H, h = item - dg * H, d = dq * C + 4 * dg;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (sg < S) {
-      for (int i0 = sg; i0 < n; i0 += S * kAheadSmall) {
-        float4 o[kAheadSmall];
-        float l[kAheadSmall];
-#pragma unroll
-        for (int j = 0; j < kAheadSmall; ++j)
-          if (i0 + S * j < n) {
-            o[j] = *reinterpret_cast<const float4*>(a.o_part + part_offset(me.first_slot + i0 + S * j, h, d, H));
-            l[j] = a.lse_part[lse_part_offset(me.first_slot + i0 + S * j, 0, h, H)];
-          }
-#pragma unroll
-        for (int j = 0; j < kAheadSmall; ++j)
-          if (i0 + S * j < n) {
-            const float w = __expf(l[j] - s_max[h]);
-            acc.x += w * o[j].x; acc.y += w * o[j].y; acc.z += w * o[j].z; acc.w += w * o[j].w;
-          }
-      }
-    }
-    s_part[t] = acc;
     __syncthreads();
-    if (t < items) {
-      float4 sum = s_part[t];
-      for (int q = 1; q < S; ++q) {
-        const float4 v = s_part[t + q * items];
-        sum.x += v.x; sum.y += v.y; sum.z += v.z; sum.w += v.w;
+    if (kOutF32) {
+      for (int idx = t; idx < H * (C / 4); idx += kMergeThreads) {
+        const int h = idx / (C / 4), q = idx % (C / 4);
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + (row0 + h) * kDCkv + dq * C + 4 * q) =
+            make_float4(tile[h][4 * q], tile[h][4 * q + 1], tile[h][4 * q + 2], tile[h][4 * q + 3]);
       }
-      const int c = 4 * dg;
-      const float inv = s_inv[h];
-      tile[h][c] = sum.x * inv;
-      tile[h][c + 1] = sum.y * inv;
-      tile[h][c + 2] = sum.z * inv;
-      tile[h][c + 3] = sum.w * inv;
-    }
-  }
-  __syncthreads();
-  const size_t row0 = static_cast<size_t>(me.req) * H;
-  if (kOutF32) {
-    for (int idx = t; idx < H * (C / 4); idx += kMergeThreads) {
-      const int h = idx / (C / 4), q = idx % (C / 4);
-      *reinterpret_cast<float4*>(static_cast<float*>(a.out) + (row0 + h) * kDCkv + dq * C + 4 * q) =
-          make_float4(tile[h][4 * q], tile[h][4 * q + 1], tile[h][4 * q + 2], tile[h][4 * q + 3]);
-    }
-  } else {
-    for (int idx = t; idx < H * (C / 8); idx += kMergeThreads) {
-      const int h = idx / (C / 8), q = idx % (C / 8);
-      uint32_t w[4];
+    } else {
+      for (int idx = t; idx < H * (C / 8); idx += kMergeThreads) {
+        const int h = idx / (C / 8), q = idx % (C / 8);
+        uint32_t wv[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const __nv_bfloat162 b2 = __floats2bfloat162_rn(tile[h][8 * q + 2 * k], tile[h][8 * q + 2 * k + 1]);
-        w[k] = *reinterpret_cast<const uint32_t*>(&b2);
+        for (int k = 0; k < 4; ++k) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(tile[h][8 * q + 2 * k], tile[h][8 * q + 2 * k + 1]);
+          wv[k] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + (row0 + h) * kDCkv + dq * C + 8 * q) =
+            make_uint4(wv[0], wv[1], wv[2], wv[3]);
       }
-      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + (row0 + h) * kDCkv + dq * C + 8 * q) =
-          make_uint4(w[0], w[1], w[2], w[3]);
     }
+    __syncthreads();   // the tile and the group states are reused by the next item
   }
 }
 
@@ -277,7 +264,16 @@ cudaError_t launch_merge(const MergeArgs& a, bool out_f32, cudaStream_t s) {
   // kernel has left); each block waits for that kernel to complete, and its
   // writes to be visible, before it reads a partial.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.merge_cap, kDCkv / merge_chunk(a.num_heads));
+  // a grid-stride loop over the plan's items: at most two blocks per SM
+  // (the kernel's registers allow two)
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 1;
+  }
+  const int cap_items = a.merge_cap * (kDCkv / merge_chunk(a.num_heads));
+  cfg.gridDim = dim3(cap_items < 2 * sms ? cap_items : 2 * sms);
   cfg.blockDim = dim3(kMergeThreads);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
