@@ -1,11 +1,12 @@
 """A device wait that runs out, on purpose, in a test build of the library.
 
 The test build (``-DMLA_STALL_TEST``, a separate shared library that the
-product never loads) gives every bounded wait of the decode kernel a 1 ms
-limit and has a knob that makes CTA 0's V producer leave out one copy.  The
-PV warp waiting for that copy gives up, the other roles of the cluster see
-the abort or run out of time on their own waits, drain what they issued, free
-TMEM and return: the kernel ends by itself.  The host then reads
+product never loads) gives every bounded wait of the decode kernels a 1 ms
+limit and has a knob per kernel that makes CTA 0's V producer leave out one
+copy (the one-CTA tcgen05 kernel and the CTA-pair kernel).  The PV issuer
+waiting for that copy gives up, the other roles of the cluster see the abort
+or run out of time on their own waits, drain what they issued, free TMEM and
+return: the kernel ends by itself.  The host then reads
 MLA_ERR_DEVICE_TIMEOUT from the plan's status word, and the next run of the
 same plan, knob off, must match the oracle (the kernel left no state behind).
 No trap, fault or endless loop is involved: the wait is bounded by design.
@@ -30,14 +31,19 @@ pytestmark = pytest.mark.gpu
 def testlib():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     lib = mla.bind_library(B.build_variant("stalltest", ["-DMLA_STALL_TEST"]))
-    lib.mla_test_set_stall.restype = ctypes.c_int
-    lib.mla_test_set_stall.argtypes = [ctypes.c_int]
+    for fn in (lib.mla_test_set_stall, lib.mla_test_set_pair_stall):
+        fn.restype = ctypes.c_int
+        fn.argtypes = [ctypes.c_int]
     return lib
 
 
-def _plan(lib, x, d):
+KNOBS = {"tcgen05": (mla.KERNEL_TCGEN05, "mla_test_set_stall"),
+         "pair": (mla.KERNEL_PAIR, "mla_test_set_pair_stall")}
+
+
+def _plan(lib, x, d, kernel):
     h = ctypes.c_void_p()
-    assert lib.mla_plan_create(x.batch, x.num_heads, mla.KERNEL_TCGEN05, ctypes.byref(h)) == mla.OK
+    assert lib.mla_plan_create(x.batch, x.num_heads, KNOBS[kernel][0], ctypes.byref(h)) == mla.OK
     indptr = np.ascontiguousarray(x.kv_indptr, np.int32)
     lens = np.ascontiguousarray(x.kv_len, np.int32)
     st = lib.mla_decode_plan(h, indptr.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
@@ -57,18 +63,20 @@ def _run(lib, h, x, d, out, lse):
     assert st == mla.OK
 
 
+@pytest.mark.parametrize("kernel", ["tcgen05", "pair"])
 @pytest.mark.parametrize("lens, chunk", [
     ([600, 300], 3),               # one unit per request
     ([9000, 40], 7),               # a request split over several units
 ])
-def test_expired_wait_is_reported_and_leaves_no_state(testlib, lens, chunk):
+def test_expired_wait_is_reported_and_leaves_no_state(testlib, kernel, lens, chunk):
     x = I.make_inputs("stall", lens, 128, 64, seed=31)
     d = to_device(x)
     out = torch.empty((x.batch, x.num_heads, 512), dtype=torch.float32, device="cuda")
     lse = torch.empty((x.batch, x.num_heads), dtype=torch.float32, device="cuda")
-    h = _plan(testlib, x, d)
+    h = _plan(testlib, x, d, kernel)
+    knob = getattr(testlib, KNOBS[kernel][1])
     try:
-        assert testlib.mla_test_set_stall(chunk) == 0
+        assert knob(chunk) == 0
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         _run(testlib, h, x, d, out, lse)
@@ -76,12 +84,12 @@ def test_expired_wait_is_reported_and_leaves_no_state(testlib, lens, chunk):
         assert time.perf_counter() - t0 < 5.0      # the kernel ended by itself
         assert testlib.mla_plan_check_status(h) == mla.OK   # the word was cleared
         # knob off: the same plan, no re-plan, runs clean and right
-        assert testlib.mla_test_set_stall(0) == 0
+        assert knob(0) == 0
         _run(testlib, h, x, d, out, lse)
         assert testlib.mla_plan_check_status(h) == mla.OK
         ref_out, ref_lse = O.mla_decode_inputs(x)
         assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
                       "after the expired wait")
     finally:
-        testlib.mla_test_set_stall(0)
+        knob(0)
         testlib.mla_plan_destroy(h)
