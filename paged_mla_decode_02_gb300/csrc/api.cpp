@@ -142,23 +142,24 @@ bool encode_2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int ele
 // (64, box_rows, box_panels) lands in shared memory panel by panel, each
 // panel box_rows x 128 bytes with the 128-byte swizzle -- the layout the MMA
 // reads -- in one copy instead of one per panel.
-// An e4m3 cache (one byte per element) is mapped the same way with 64-byte
-// panel rows and the 64-byte swizzle (16-byte chunk c of row r lands at
-// chunk c ^ ((r >> 1) & 3), so the kernel's row-per-lane reads are free of
-// bank conflicts); the kernel expands the bytes to the 128-byte-swizzled
-// bf16 layout itself.
+// An e4m3 cache (one byte per element) is mapped with either 64-element
+// panels and the 64-byte swizzle (16-byte chunk c of row r lands at chunk
+// c ^ ((r >> 1) & 3), so a kernel's row-per-lane reads are free of bank
+// conflicts) or, wide = true, 128-element panels of 128-byte rows and the
+// 128-byte swizzle, the MN-major layout an e4m3 MMA reads.
 bool encode_panels_3d(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows,
-                      uint32_t box_panels, bool fp8 = false) {
+                      uint32_t box_panels, bool fp8 = false, bool wide = false) {
   EncodeTiledFn fn = get_encode_fn();
   if (!fn) return false;
   const uint64_t eb = fp8 ? 1 : 2;
-  cuuint64_t dims[3] = {64, rows, kDCkv / 64};
-  cuuint64_t strides[2] = {kDCkv * eb, 64 * eb};
-  cuuint32_t box[3] = {64, box_rows, box_panels};
+  const uint64_t pw = fp8 && wide ? 128 : 64;   // elements per panel row
+  cuuint64_t dims[3] = {pw, rows, kDCkv / pw};
+  cuuint64_t strides[2] = {kDCkv * eb, pw * eb};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(pw), box_rows, box_panels};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  fp8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                  fp8 && !wide ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -183,8 +184,9 @@ bool mla::encode_tc_maps(TcMaps* maps, const void* q_nope, const void* ckv_cache
 }
 
 // The CTA-pair kernel's tensor maps: the query of 64 heads per box (one per
-// CTA of the pair), K panels of one page, V chunks of four 64-dim panels
-// (an fp8 cache: byte maps, 64-byte swizzle).
+// CTA of the pair), K panels of one page, V chunks of four 64-dim panels (an
+// fp8 cache: byte maps; K panels of 64-byte rows with the 64-byte swizzle, V
+// chunks of two 128-dim panels with the 128-byte swizzle).
 bool mla::encode_pair_maps(PairMaps* maps, const void* q_nope, const void* q_pe, const void* ckv_cache,
                            const void* kpe_cache, int batch, int num_heads, int page_size, int num_pages,
                            bool kv_fp8) {
@@ -198,8 +200,8 @@ bool mla::encode_pair_maps(PairMaps* maps, const void* q_nope, const void* q_pe,
          encode_2d(&maps->q_pe, q_pe, bf, 2, qrows, kDKpe, 64, 64) &&
          encode_2d(&maps->ckv_k, ckv_cache, kt, eb, kvrows, kDCkv, page_size, 64, ks) &&
          encode_2d(&maps->kpe_k, kpe_cache, kt, eb, kvrows, kDKpe, page_size, 64, ks) &&
-         encode_panels_3d(&maps->ckv_v, ckv_cache, kvrows, page_size >= kTcVChunkTok ? kTcVChunkTok : 16, 4,
-                          kv_fp8);
+         encode_panels_3d(&maps->ckv_v, ckv_cache, kvrows, page_size >= kTcVChunkTok ? kTcVChunkTok : 16,
+                          kv_fp8 ? 2 : 4, kv_fp8, true);
 }
 
 extern "C" {

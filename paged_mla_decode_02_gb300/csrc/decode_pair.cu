@@ -42,13 +42,18 @@
 // four threads of a head at the end (the output is divided by the latter,
 // the lse uses the former).
 //
-// fp8 (e4m3) caches (pages of 32 or 64 tokens): the copies land as codes in
-// the upper half of each ring slot and are expanded in place to f16 -- K
-// panels in the even CTA by the QK issuer while the previous MMAs run and in
-// the odd CTA by its warp 1, V chunks by the V producers one copy behind
-// their issue point -- and both products take f16 operands: the query
-// converted once per unit (a power-of-two scale per head row), P rounded to
-// f16.
+// fp8 (e4m3) caches (pages of 32 or 64 tokens): both products are e4m3
+// MMAs (kind::f8f6f4) straight from the copied codes -- K panels of 64 dims
+// (64-byte rows) and V chunks of 2 x 128 dims (128-byte rows, MN-major), in
+// 8 KB ring slots, so a ring holds twice the tokens of the bf16 one.  The
+// other operand of each product is split into two e4m3 terms, x = hi + lo
+// (hi = e4m3(x), lo = e4m3(x - hi)), and both terms multiply the same codes
+// into the same accumulator: the query once per unit under a power-of-two
+// scale per head row (its largest magnitude in [2^7, 2^8): hi + lo is then
+// the bf16 query exactly, but for elements below 2^-2 after the scaling), P
+// per tile as p = 2^(s - reference) * 2^6 with a reference that moves when
+// the tile maximum exceeds it by more than 2.5 (p <= 2^8.5 < 448); hi + lo
+// keeps 8 significant bits of p, as bf16 does.
 //
 // Every wait is bounded (2 s); on expiry the kernel records
 // MLA_ERR_DEVICE_TIMEOUT, lets its copies and MMAs land, frees TMEM and
@@ -80,9 +85,19 @@ constexpr int kFirstSoftmaxWarp = 2;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kVProducerWarp = 10;
 constexpr int kPvIssuerWarp = 11;
-constexpr int kKSlots = 4, kVSlots = 3;    // ring slots
+// Ring slots: 16 KB (bf16: a K panel of 128 tokens x 64 dims, a V chunk of
+// 32 tokens x 256 dims) or 8 KB (e4m3, the same tokens and dims); either
+// way 64 KB of K slots and 48 KB of V slots.
+template <bool kFp8>
+struct Ring {
+  static constexpr int kSlotBytes = kFp8 ? 8192 : 16384;
+  static constexpr int kKSlots = 65536 / kSlotBytes;
+  static constexpr int kVSlots = 49152 / kSlotBytes;
+  static constexpr int kVPanels = kFp8 ? 2 : 4;   // MN panels (128-byte rows) of a V chunk
+};
+constexpr int kKSlotsMax = 8, kVSlotsMax = 6;
+constexpr int kKRingBytes = 65536, kVRingBytes = 49152;
 constexpr int kPBufs = 1;                  // P buffers (2: by tile parity)
-constexpr int kSlotBytes = 16384;
 constexpr int kVChunkTok = kTcVChunkTok;   // 32 tokens per V chunk
 constexpr int kChunksPerTile = kT / kVChunkTok;
 static_assert(kVChunkTok == 32, "V chunk: two 16-token MMA slices");
@@ -90,7 +105,12 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-constexpr float kRescaleThreshold = 8.0f;   // log2 units: p stays below 2^8
+// log2 units: the reference moves when a tile's maximum exceeds it by more
+// than this; p = 2^(s - reference) stays below 2^8 (bf16), and e4m3 hi + lo
+// take p * 2^6 <= 2^8.5 (the largest code is 448; a power of two keeps a
+// lone token's p exact)
+constexpr float kRescaleThreshold = 8.0f, kRescaleThresholdFp8 = 2.5f;
+constexpr float kPOffsetFp8 = 6.0f, kPScaleFp8 = 64.0f;   // 2^kPOffsetFp8
 
 // shared memory (offsets from the 1024-byte aligned base)
 constexpr int kOffQ = 0;                          // 9 panels x (64 heads x 128 B)
@@ -99,8 +119,8 @@ constexpr int kOffP = kOffQ + 9 * kQPanel;        // P: 4 token panels x (64 hea
 constexpr int kPPanel = 64 * 128;
 constexpr int kPBuf = 4 * kPPanel;                // one P buffer: 32 KB
 constexpr int kOffKRing = kOffP + kPBufs * kPBuf;
-constexpr int kOffVRing = kOffKRing + kKSlots * kSlotBytes;
-constexpr int kOffRed = kOffVRing + kVSlots * kSlotBytes;  // maxima [2 parities][4 parts][64 heads] float
+constexpr int kOffVRing = kOffKRing + kKRingBytes;
+constexpr int kOffRed = kOffVRing + kVRingBytes;          // maxima [2 parities][4 parts][64 heads] float
 constexpr int kOffSum = kOffRed + 2 * 4 * 64 * 4;          // sums [4 parts][64 heads] float2
 constexpr int kOffQRed = kOffSum + 4 * 64 * 8;            // fp8: query row maxima [4 parts][64 heads] float
 constexpr int kOffFlags = kOffQRed + 4 * 64 * 4;          // abort, tmem slot
@@ -109,11 +129,11 @@ static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOffKRing % 1024 == 0 &&
               "swizzle atoms");
 
 enum Bar {
-  kKFull0 = 0,                   // [kKSlots] even CTA: K slot loaded in both CTAs (1 arrival + both CTAs' bytes)
-  kKEmpty0 = kKFull0 + kKSlots,  // [kKSlots] both: the MMAs reading the K slot completed
-  kVFull0 = kKEmpty0 + kKSlots,  // [kVSlots] even CTA: V slot loaded in both CTAs
-  kVEmpty0 = kVFull0 + kVSlots,  // [kVSlots] both
-  kQFull = kVEmpty0 + kVSlots,   // even CTA: both query halves loaded (1 arrival + bytes)
+  kKFull0 = 0,                      // [K slots] even CTA: K slot loaded in both CTAs (1 arrival + both CTAs' bytes)
+  kKEmpty0 = kKFull0 + kKSlotsMax,  // [K slots] both: the MMAs reading the K slot completed
+  kVFull0 = kKEmpty0 + kKSlotsMax,  // [V slots] even CTA: V slot loaded in both CTAs
+  kVEmpty0 = kVFull0 + kVSlotsMax,  // [V slots] both
+  kQFull = kVEmpty0 + kVSlotsMax,   // even CTA: both query halves loaded (1 arrival + bytes)
   kQFree,                        // both: the unit's last QK completed
   kSFull0,                       // [2] both: S buffer written
   kSFree0 = kSFull0 + 2,         // [2] even CTA: S buffer read by all 16 softmax warps
@@ -127,11 +147,9 @@ enum Bar {
   kFinal,                        // even CTA: every QK MMA completed
   kFinalPv,                      // even CTA: every PV MMA completed
   // fp8 caches only
-  kKLand0,                       // [kKSlots] this CTA's e4m3 K copy landed (1 arrival + bytes)
-  kVLand0 = kKLand0 + kKSlots,   // [kVSlots] this CTA's e4m3 V copy landed
-  kQLand = kVLand0 + kVSlots,    // this CTA's query landed (1 arrival + bytes)
+  kQLand,                        // this CTA's query landed (1 arrival + bytes)
   kQRed,                         // the 8 softmax warps posted their query row maxima
-  kQReady,                       // even CTA: both CTAs' query converted to f16 (16 arrivals)
+  kQReady,                       // even CTA: both CTAs' query split into e4m3 terms (16 arrivals)
   kNumBars
 };
 constexpr int kSmemBytes = kOffBar + 8 * kNumBars + 1024;   // + alignment slack
@@ -153,92 +171,35 @@ __device__ __forceinline__ void arrive_lead(uint32_t local_bar, int rank) {
 }
 
 // ---------------------------------------------------------------------------
-// fp8 (e4m3) caches.  The MMAs then take f16 operands: an e4m3 code converts
-// to f16 exactly in one instruction per pair (to bf16 it takes four), the
-// query is converted to f16 once per unit under a power-of-two scale per
-// head row (its largest magnitude lands in [2^14, 2^15): f16 keeps bf16's 8
-// significant bits and more), and P, in [0, 2^8], is rounded to f16.
+// fp8 (e4m3) caches: e4m3 x e4m3 -> f32 MMAs (kind::f8f6f4).  The instruction
+// descriptor has the layout of kind::f16's; the format code 0 of A and B
+// means e4m3 there.
 // ---------------------------------------------------------------------------
-__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn, bool b_mn) {
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4)                                   // D format: f32
-         | (static_cast<uint32_t>(a_mn) << 15)       // A, B format: f16 (0)
+         | (static_cast<uint32_t>(a_mn) << 15)       // A, B format: e4m3 (0)
          | (static_cast<uint32_t>(b_mn) << 16)
          | (static_cast<uint32_t>(N >> 3) << 17)
          | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Two e4m3 codes (the low byte of the 16-bit half first) -> two f16, the PTX
-// conversion instruction for this pair of formats (exact: every e4m3 value
-// is an f16).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t word, int half) {
-  uint16_t lo16, hi16;
-  asm("mov.b32 {%0, %1}, %2;" : "=h"(lo16), "=h"(hi16) : "r"(word));
-  uint32_t r;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(half ? hi16 : lo16));
-  return r;
+// Two floats -> two e4m3 codes (round to nearest even, saturating to +-448;
+// the first in the low byte), and back.
+__device__ __forceinline__ uint32_t to_e4m3x2(float x0, float x1) {
+  return __nv_cvt_float2_to_fp8x2(make_float2(x0, x1), __NV_SATFINITE, __NV_E4M3);
 }
-// 16 e4m3 codes -> 16 f16 (two 16-byte words).
-__device__ __forceinline__ void e4m3x16_to_f16x16(const uint4& in, uint4& lo, uint4& hi) {
-  const uint32_t w[4] = {in.x, in.y, in.z, in.w};
-  uint32_t o[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    o[2 * i] = e4m3x2_to_f16x2(w[i], 0);
-    o[2 * i + 1] = e4m3x2_to_f16x2(w[i], 1);
-  }
-  lo = make_uint4(o[0], o[1], o[2], o[3]);
-  hi = make_uint4(o[4], o[5], o[6], o[7]);
+__device__ __forceinline__ float2 from_e4m3x2(uint32_t codes) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(codes), __NV_E4M3);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
-
-// A copy lands as rows of 64 codes in the upper half of a 16 KB slot, 64-byte
-// swizzled (16-byte chunk c of row r at c ^ ((r >> 1) & 3)); a warp expands it
-// in place to the f16 rows of the 128-byte-swizzled panel the MMA reads
-// (chunk c of row r at c ^ (r & 7)), one lane per row.  Every step reads its
-// 32 rows before any lane writes, and its writes end below the rows later
-// steps read (f16 rows [32 t, 32 t + 32) end at byte 4096 (t + 1); the codes
-// of row 32 (t + 1) start at 8192 + 2048 (t + 1)).
-__device__ __forceinline__ void expand_row_f16(unsigned char* dst_row, int r, const uint4 (&q)[4]) {
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uint4 lo, hi;
-    e4m3x16_to_f16x16(q[k], lo, hi);
-    *reinterpret_cast<uint4*>(dst_row + (((2 * k) ^ (r & 7)) << 4)) = lo;
-    *reinterpret_cast<uint4*>(dst_row + (((2 * k + 1) ^ (r & 7)) << 4)) = hi;
-  }
-}
-// A slot is expanded by one warp: every lane first reads all its rows' codes
-// (16 chunks), then converts and writes them, so all reads precede all writes
-// and the loads are in flight together.
-// K panel: 128 token rows of 64 dims; lane l takes rows l, l + 32, l + 64, l + 96.
-__device__ __forceinline__ void expand_k_panel_f16(unsigned char* slot, int lane) {
-  uint4 q[4][4];
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const int r = 32 * t + lane;
-    const uint4* src = reinterpret_cast<const uint4*>(slot + 8192 + 64 * r);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) q[t][k] = src[k ^ ((r >> 1) & 3)];
-  }
-  __syncwarp();
-#pragma unroll
-  for (int t = 0; t < 4; ++t) expand_row_f16(slot + 128 * (32 * t + lane), 32 * t + lane, q[t]);
-  __syncwarp();
-}
-// V chunk: 4 panels of 32 token rows (codes of panel p at 8192 + 2048 p), lane
-// l takes row l of every panel; rows at and past rows_valid (beyond the
-// request's last token) become zeros.
-__device__ __forceinline__ void expand_v_chunk_f16(unsigned char* slot, int lane, int rows_valid) {
-  uint4 q[4][4];
-#pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const uint4* src = reinterpret_cast<const uint4*>(slot + 8192 + 2048 * p + 64 * lane);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) q[p][k] = lane < rows_valid ? src[k ^ ((lane >> 1) & 3)] : make_uint4(0, 0, 0, 0);
-  }
-  __syncwarp();
-#pragma unroll
-  for (int p = 0; p < 4; ++p) expand_row_f16(slot + 4096 * p + 128 * lane, lane, q[p]);
-  __syncwarp();
+// x = hi + lo, each an e4m3 term: hi = e4m3(x), lo = e4m3(x - hi) (x - hi is
+// exact in f32).  Two elements; returns (hi + lo) of both, added.
+__device__ __forceinline__ float split_e4m3x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = to_e4m3x2(x0, x1);
+  const float2 h = from_e4m3x2(hi);
+  lo = to_e4m3x2(x0 - h.x, x1 - h.y);
+  const float2 l = from_e4m3x2(lo);
+  return (h.x + l.x) + (h.y + l.y);
 }
 
 template <bool kOutF32, bool kFp8>
@@ -251,6 +212,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kOffFlags);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffFlags + 4);
 
+  constexpr int kKSlots = Ring<kFp8>::kKSlots, kVSlots = Ring<kFp8>::kVSlots;
+  constexpr int kSlotBytes = Ring<kFp8>::kSlotBytes, kVPanels = Ring<kFp8>::kVPanels;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int worker = blockIdx.x >> 1;
   const int rank = static_cast<int>(cluster_ctarank());
@@ -269,10 +232,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         cnt = 2 * kSoftmaxWarps;
       if (i == kRed0 || i == kRed0 + 1 || i == kSum || i == kQRed) cnt = kSoftmaxWarps;
       if (i == kQReady) cnt = 2 * kSoftmaxWarps;
-      // fp8: a K slot's full barrier counts the odd CTA's expansion (the even
-      // CTA's own is done by the QK issuer itself); a V slot's counts both
-      // CTAs' V producers
-      if (kFp8 && i >= kVFull0 && i < kVFull0 + kVSlots) cnt = 2;
       mbar_init(bar(base, i), cnt);
     }
     fence_barrier_init();
@@ -301,27 +260,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // completes on the even CTA's full barrier of its slot, where the even
     // CTA's producer announces the bytes of both (the odd CTA only issues
     // its copies: an arrive at cluster scope per slot would cost a fence
-    // each).  With an fp8 cache every copy lands as e4m3 codes in the upper
-    // half of its slot, on a barrier of this CTA (kKLand / kVLand), and is
-    // expanded to f16 before the MMAs read it: K panels by warp 1 (the QK
-    // issuer in the even CTA), V chunks by this warp, one copy behind.
+    // each).  An fp8 cache is copied as its e4m3 codes, which the MMAs read
+    // as they are.
     const bool is_k = warp == 0;
     int rp = 0;            // slots of this ring used so far
     int tail_uses = 0;
     bool ok = true;
-    // fp8 V: the chunk issued last, expanded once the next one is issued
-    int pend_rp = -1, pend_rows = 0;
-    auto expand_pending_v = [&]() -> bool {
-      if (pend_rp < 0) return true;
-      const int slot = pend_rp % kVSlots;
-      if (!(ok = mbar_wait_warp(bar(base, kVLand0 + slot), (pend_rp / kVSlots) & 1, abort_flag))) return false;
-      expand_v_chunk_f16(sm + kOffVRing + slot * kSlotBytes, lane, pend_rows);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) arrive_lead(bar(base, kVFull0 + slot), rank);
-      pend_rp = -1;
-      return true;
-    };
     int q_units = 0;       // query loads issued
     const int vbox = P >= kVChunkTok ? kVChunkTok : 16;
     const int nslots = is_k ? kKSlots : kVSlots;
@@ -355,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (q_units > 0 && !(ok = mbar_wait_warp(bar(base, kQFree), (q_units - 1) & 1, abort_flag))) return false;
       ++q_units;
       if constexpr (kFp8) {
-        // this CTA's query lands here; the softmax warps convert it to f16
+        // this CTA's query lands here; the softmax warps split it into e4m3
+        // terms
         if (lane == 0) mbar_arrive_expect_tx(bar(base, kQLand), 9 * kQPanel);
         __syncwarp();
         if (lane < 9) {
@@ -388,28 +333,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int nbox_both = nbox + (cnt1 + P - 1) / P;
       const int pb = (kHalfT * rank) / P;   // first page of this half within the tile
       const int page = __shfl_sync(0xffffffffu, pages, min(pb + lane, 31));
+      // a panel row: 64 dims, 128 bytes (bf16) or 64 (e4m3)
+      constexpr int row_bytes = kFp8 ? 64 : 128;
       for (int j = 0; j < 9; ++j) {
         int slot;
         if (!(ok = next_slot(slot))) return false;
-        if constexpr (kFp8) {
-          const uint32_t land = bar(base, kKLand0 + slot);
-          if (lane == 0) mbar_arrive_expect_tx(land, nbox * P * 64);
-          __syncwarp();
-          if (lane < nbox) {
-            const uint32_t dst = base + kOffKRing + slot * kSlotBytes + 8192 + lane * P * 64;
-            if (j < 8)
-              tma_load_2d(dst, &maps.ckv_k, 64 * j, page * P, land);
-            else
-              tma_load_2d(dst, &maps.kpe_k, 0, page * P, land);
-          }
-          continue;
-        }
         const uint32_t full = map_to_rank(bar(base, kKFull0 + slot), lead);
         if (lane == 0 && rank == 0)
-          mbar_arrive_expect_tx(bar(base, kKFull0 + slot), nbox_both * P * 128);
+          mbar_arrive_expect_tx(bar(base, kKFull0 + slot), nbox_both * P * row_bytes);
         __syncwarp();
         if (lane < nbox) {
-          const uint32_t dst = base + kOffKRing + slot * kSlotBytes + lane * P * 128;
+          const uint32_t dst = base + kOffKRing + slot * kSlotBytes + lane * P * row_bytes;
           if (j < 8)
             tma_load_2d_pair(dst, &maps.ckv_k, 64 * j, page * P, full);
           else
@@ -426,47 +360,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (rows <= 0) break;
         int slot;
         if (!(ok = next_slot(slot))) return false;
-        if constexpr (kFp8) {
-          // 32 rows of 4 x 64 codes (a page holds whole chunks: P >= 32); the
-          // previous chunk is expanded (rows past kv_len zeroed) while this
-          // one is in flight, then both CTAs' expansions count on the even
-          // CTA's full barrier
-          const uint32_t land = bar(base, kVLand0 + slot);
-          const int page = __shfl_sync(0xffffffffu, pages, (t - tok0) / P);
-          if (lane == 0) {
-            mbar_arrive_expect_tx(land, kVChunkTok * 4 * 64);
-            tma_load_3d(base + kOffVRing + slot * kSlotBytes + 8192, &maps.ckv_v, 0, page * P + (t % P), 4 * rank,
-                        land);
-          }
-          __syncwarp();
-          if (!expand_pending_v()) return false;
-          pend_rp = rp - 1;
-          pend_rows = rows;
-          continue;
-        }
         const uint32_t full = map_to_rank(bar(base, kVFull0 + slot), lead);
         if (stalled()) continue;
+        // one copy: vbox rows of kVPanels panels (128-byte rows), this CTA's
+        // 256 dims
         const int ncopy = (rows + vbox - 1) / vbox;
         const int tb = t + vbox * min(lane, ncopy - 1);
         const int page = __shfl_sync(0xffffffffu, pages, (tb - tok0) / P);
-        const uint32_t dst = base + kOffVRing + slot * kSlotBytes + lane * vbox * 4 * 128;
+        const int copy_bytes = vbox * kVPanels * 128;
+        const uint32_t dst = base + kOffVRing + slot * kSlotBytes + lane * copy_bytes;
         if (rows == kVChunkTok) {
-          if (lane == 0 && rank == 0) mbar_arrive_expect_tx(bar(base, kVFull0 + slot), 2 * ncopy * vbox * 4 * 128);
+          if (lane == 0 && rank == 0) mbar_arrive_expect_tx(bar(base, kVFull0 + slot), 2 * ncopy * copy_bytes);
           __syncwarp();
-          if (lane < ncopy) tma_load_3d_pair(dst, &maps.ckv_v, 0, page * P + (tb % P), 4 * rank, full);
+          if (lane < ncopy) tma_load_3d_pair(dst, &maps.ckv_v, 0, page * P + (tb % P), kVPanels * rank, full);
         } else {
           // last chunk of a request: rows past kv_len may hold anything (even
           // NaN) and p = 0 does not cancel NaN; copy locally, zero those
           // rows, then release the slot to the issuer
           const uint32_t tail = bar(base, kTail);
-          if (lane == 0) mbar_arrive_expect_tx(tail, ncopy * vbox * 4 * 128);
+          if (lane == 0) mbar_arrive_expect_tx(tail, ncopy * copy_bytes);
           __syncwarp();
-          if (lane < ncopy) tma_load_3d(dst, &maps.ckv_v, 0, page * P + (tb % P), 4 * rank, tail);
+          if (lane < ncopy) tma_load_3d(dst, &maps.ckv_v, 0, page * P + (tb % P), kVPanels * rank, tail);
           if (!(ok = mbar_wait_warp(tail, tail_uses & 1, abort_flag))) return false;
           unsigned char* sv = sm + kOffVRing + slot * kSlotBytes;
-          for (int q = lane; q < (kVChunkTok - rows) * 32; q += 32) {
-            const int rr = rows + q / 32, pnl = (q % 32) >> 3, c16 = q & 7;
-            const int off = vbox == kVChunkTok ? pnl * 4096 + rr * 128
+          // 16-byte chunks of the rows past the end: 8 per panel row
+          for (int q = lane; q < (kVChunkTok - rows) * kVPanels * 8; q += 32) {
+            const int rr = rows + q / (kVPanels * 8), pnl = (q % (kVPanels * 8)) >> 3, c16 = q & 7;
+            const int off = vbox == kVChunkTok ? pnl * (kVChunkTok * 128) + rr * 128
                                                : (rr >> 4) * 8192 + pnl * 2048 + (rr & 15) * 128;
             *reinterpret_cast<uint4*>(sv + off + c16 * 16) = make_uint4(0, 0, 0, 0);
           }
@@ -498,7 +418,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    if (kFp8 && !is_k && ok) expand_pending_v();
     if (!ok && lane == 0) report_error(a.err, kErrTimeout);
   } else if ((warp == 1 || warp == kPvIssuerWarp) && rank == 0) {
     // ================= MMA issuers (even CTA, whole warp, lane 0 issues) =================
@@ -510,14 +429,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t issue = lane == 0;
     bool ok = true;
     if (warp == 1) {
-      constexpr uint32_t id_qk = kFp8 ? idesc_f16_f32(128, 256, false, false) : idesc_bf16_f32(128, 256, false, false);
+      constexpr uint32_t id_qk = kFp8 ? idesc_e4m3_f32(128, 256, false, false) : idesc_bf16_f32(128, 256, false, false);
       const uint64_t q_desc0 = smem_desc(base + kOffQ, 16, 1024, kSw128);
-      const uint64_t k_desc0 = smem_desc(base + kOffKRing, 16, 1024, kSw128);
+      // K panels: 128-byte rows, 128-byte swizzle (bf16) or 64-byte rows and
+      // swizzle (e4m3); 8-row groups 1024 or 512 bytes apart
+      const uint64_t k_desc0 = kFp8 ? smem_desc(base + kOffKRing, 16, 512, kSw64)
+                                    : smem_desc(base + kOffKRing, 16, 1024, kSw128);
       int kc = 0, g = 0, unit_k = 0;
       for (int ui = u0; ui < u1 && ok; ++ui, ++unit_k) {
         const WorkUnit v = a.units[ui];
         const int n = tiles_of(v);
-        // the unit's query: loaded (bf16) or converted to f16 in both CTAs (fp8)
+        // the unit's query: loaded (bf16) or split into e4m3 terms in both CTAs (fp8)
         if (!(ok = kFp8 ? mbar_wait_cl_warp(bar(base, kQReady), unit_k & 1, abort_flag)
                         : mbar_wait_warp(bar(base, kQFull), unit_k & 1, abort_flag)))
           break;
@@ -529,24 +451,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 9; ++j, ++kc) {
             const int slot = kc % kKSlots;
             const uint32_t par = (kc / kKSlots) & 1;
-            if constexpr (kFp8) {
-              // this CTA's copy expanded here (while the previous panel's MMAs
-              // run), the odd CTA's by its warp 1
-              if (!(ok = mbar_wait_warp(bar(base, kKLand0 + slot), par, abort_flag))) break;
-              expand_k_panel_f16(sm + kOffKRing + slot * kSlotBytes, lane);
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (!(ok = mbar_wait_cl_warp(bar(base, kKFull0 + slot), par, abort_flag))) break;
-            } else if (!(ok = mbar_wait_warp(bar(base, kKFull0 + slot), par, abort_flag))) {
-              break;
-            }
+            if (!(ok = mbar_wait_warp(bar(base, kKFull0 + slot), par, abort_flag))) break;
             tc_fence_after();
             const uint64_t adesc = q_desc0 + static_cast<uint64_t>((j * kQPanel) >> 4);
             const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((slot * kSlotBytes) >> 4);
+            if constexpr (kFp8) {
+              // dims [64 j + 32 kk, + 32): the query's hi codes at byte 32 kk
+              // of its row, its lo codes at 64 + 32 kk, the K codes at 32 kk
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_pair(d, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2), id_qk,
-                       (j | kk) != 0, issue);
+              for (int kk = 0; kk < 2; ++kk) {
+                const uint64_t b = bdesc + static_cast<uint64_t>(kk * 2);
+                mma_pair_e4m3(d, adesc + static_cast<uint64_t>(kk * 2), b, id_qk, (j | kk) != 0, issue);
+                mma_pair_e4m3(d, adesc + static_cast<uint64_t>(4 + kk * 2), b, id_qk, 1u, issue);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_pair(d, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2), id_qk,
+                         (j | kk) != 0, issue);
+            }
             commit_pair(bar(base, kKEmpty0 + slot), 3, issue);
           }
           if (!ok) break;
@@ -561,9 +484,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_wait_cl_drain(bar(base, kFinal), 0);
       __syncwarp();
     } else {
-      constexpr uint32_t id_pv = kFp8 ? idesc_f16_f32(128, 256, false, true) : idesc_bf16_f32(128, 256, false, true);
+      constexpr uint32_t id_pv = kFp8 ? idesc_e4m3_f32(128, 256, false, true) : idesc_bf16_f32(128, 256, false, true);
       const uint64_t p_desc0 = smem_desc(base + kOffP, 16, 1024, kSw128);
       const bool v32 = P >= kVChunkTok;
+      // V chunks, MN-major: panels of 128-byte rows (64 bf16 or 128 e4m3
+      // dims), 128-byte swizzle, 8-row groups 1024 bytes apart
       const uint64_t v_desc0 = smem_desc(base + kOffVRing, v32 ? 4096 : 2048, 1024, kSw128);
       const uint32_t v_kstep = v32 ? 2048 : 8192, v_block = v32 ? 8192 : 4096;
       int vc = 0, g = 0, unit_k = 0;
@@ -581,24 +506,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < nch; ++c, ++vc) {
             const int slot = vc % kVSlots;
             const uint32_t par = (vc / kVSlots) & 1;
-            if constexpr (kFp8) {
-              // expanded in both CTAs by their V producers
-              if (!(ok = mbar_wait_cl_warp(bar(base, kVFull0 + slot), par, abort_flag))) break;
-            } else if (!(ok = mbar_wait_warp(bar(base, kVFull0 + slot), par, abort_flag))) {
-              break;
-            }
+            if (!(ok = mbar_wait_warp(bar(base, kVFull0 + slot), par, abort_flag))) break;
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-              const int t = kVChunkTok * c + 16 * kk;   // first token of the K step
-              const uint64_t adesc =
-                  p_desc0 + static_cast<uint64_t>((pbuf + (t >> 6) * kPPanel + (t & 63) * 2) >> 4);
+            if constexpr (kFp8) {
+              // tokens [32 c, 32 c + 32): P's hi codes at byte 32 (c & 1) of
+              // the rows of token panel c / 2, its lo codes 64 bytes further;
+              // V panel bb (128 dims) of the chunk for O columns [128 bb, ..)
+              const uint64_t a_hi =
+                  p_desc0 + static_cast<uint64_t>((pbuf + (c >> 1) * kPPanel + 32 * (c & 1)) >> 4);
 #pragma unroll
               for (int bb = 0; bb < 2; ++bb) {
                 const uint64_t bdesc =
-                    v_desc0 + static_cast<uint64_t>((slot * kSlotBytes + kk * v_kstep + bb * v_block) >> 4);
-                mma_pair(tmem + kColO + 128 * bb, adesc, bdesc, id_pv, (i == 0 && c == 0 && kk == 0) ? 0u : 1u,
-                         issue);
+                    v_desc0 + static_cast<uint64_t>((slot * kSlotBytes + bb * kVChunkTok * 128) >> 4);
+                mma_pair_e4m3(tmem + kColO + 128 * bb, a_hi, bdesc, id_pv, (i == 0 && c == 0) ? 0u : 1u, issue);
+                mma_pair_e4m3(tmem + kColO + 128 * bb, a_hi + 4, bdesc, id_pv, 1u, issue);
+              }
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 2; ++kk) {
+                const int t = kVChunkTok * c + 16 * kk;   // first token of the K step
+                const uint64_t adesc =
+                    p_desc0 + static_cast<uint64_t>((pbuf + (t >> 6) * kPPanel + (t & 63) * 2) >> 4);
+#pragma unroll
+                for (int bb = 0; bb < 2; ++bb) {
+                  const uint64_t bdesc =
+                      v_desc0 + static_cast<uint64_t>((slot * kSlotBytes + kk * v_kstep + bb * v_block) >> 4);
+                  mma_pair(tmem + kColO + 128 * bb, adesc, bdesc, id_pv, (i == 0 && c == 0 && kk == 0) ? 0u : 1u,
+                           issue);
+                }
               }
             }
             commit_pair(bar(base, kVEmpty0 + slot), 3, issue);
@@ -613,39 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
     }
   } else if (warp == 1 || warp == kPvIssuerWarp) {
-    // ================= odd CTA: fp8 expanders (else no role) =================
-    // Warp 1 expands this CTA's K copies in the order the even CTA's QK
-    // issuer consumes them, each then arriving on the even CTA's full barrier
-    // of the slot (V chunks are expanded by the V producers).
-    if (kFp8 && warp == 1) {
-      const bool is_k = true;
-      bool ok = true;
-      int cnt = 0;   // copies of this ring expanded
-      for (int ui = u0; ui < u1 && ok; ++ui) {
-        const WorkUnit v = a.units[ui];
-        const int n = tiles_of(v);
-        for (int i = 0; i < n && ok; ++i) {
-          const int valid = min(kT, v.tok_end - (v.tok_begin + i * kT));
-          const int per_tile = is_k ? 9 : (valid + kVChunkTok - 1) / kVChunkTok;
-          for (int c = 0; c < per_tile; ++c, ++cnt) {
-            const int nsl = is_k ? kKSlots : kVSlots;
-            const int slot = cnt % nsl;
-            if (!(ok = mbar_wait_warp(bar(base, (is_k ? kKLand0 : kVLand0) + slot), (cnt / nsl) & 1, abort_flag)))
-              break;
-            unsigned char* sl = sm + (is_k ? kOffKRing : kOffVRing) + slot * kSlotBytes;
-            const int rows = min(kVChunkTok, valid - kVChunkTok * c);
-            if (is_k)
-              expand_k_panel_f16(sl, lane);
-            else
-              expand_v_chunk_f16(sl, lane, rows);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(map_to_rank(bar(base, (is_k ? kKFull0 : kVFull0) + slot), lead));
-          }
-        }
-      }
-      if (!ok && lane == 0) report_error(a.err, kErrTimeout);
-    }
+    // odd CTA: no role (the even CTA issues the pair's MMAs)
   } else {
     // ================= softmax / epilogue (warps 2..9, both CTAs) =================
     const int sw = warp - kFirstSoftmaxWarp;
@@ -660,6 +563,81 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* red = reinterpret_cast<float*>(sm + kOffRed);
     float2* sums = reinterpret_cast<float2*>(sm + kOffSum);
     bool ok = true;
+    // fp8: a unit's query, split into e4m3 terms by these warps -- the
+    // first unit's at the start, every later unit's as soon as the previous
+    // unit's last P is written (its query has landed by then or soon after:
+    // it is loaded once the previous unit's last scores are done), so the
+    // split overlaps that unit's last P . V and epilogue, and the next
+    // scores can start meanwhile.  Returns false when a wait runs out; sets
+    // cq_next to the score scale of this thread's head.
+    float cq_next = c;
+    auto split_query = [&](uint32_t parity) -> bool {
+      // ---- the unit's query (this CTA's 64 heads) split in place into
+      // e4m3 terms: row hl is scaled by 2^e so that its largest magnitude
+      // lies in [2^7, 2^8) (then hi + lo is the scaled bf16 value exactly
+      // down to magnitudes of 2^-2), and the scores by 2^-e.  Each 128-byte
+      // row of a panel (64 bf16 dims) becomes the 64 hi codes followed by
+      // the 64 lo codes of the same dims, in the same row (128-byte
+      // swizzle).  The head's four threads take panels part, part + 4, ..
+      // of its 9, whole rows, so no thread reads what another writes ----
+      if (!mbar_wait_warp(bar(base, kQLand), parity, abort_flag)) return false;
+      auto qchunk = [&](int pj, int k) -> uint4* {
+        return reinterpret_cast<uint4*>(sm + kOffQ + pj * kQPanel + hl * 128 + ((k ^ (hl & 7)) << 4));
+      };
+      float mx = 0.f;
+      for (int pj = part; pj < 9; pj += 4) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = *qchunk(pj, k);
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int m = 0; m < 4; ++m)
+            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[m] << 16)), fabsf(__uint_as_float(w[m] & 0xffff0000u))));
+        }
+      }
+      float* qred = reinterpret_cast<float*>(sm + kOffQRed);
+      qred[part * 64 + hl] = mx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(base, kQRed));
+      if (!mbar_wait_warp(bar(base, kQRed), parity, abort_flag)) return false;
+      const float rm = fmaxf(fmaxf(qred[hl], qred[64 + hl]), fmaxf(qred[128 + hl], qred[192 + hl]));
+      // rows of zeros (heads past H) keep e = 0
+      int e = 0;
+      if (rm > 0.f && rm < INFINITY) e = min(max(7 - (((__float_as_int(rm) >> 23) & 0xff) - 127), -100), 100);
+      const float up = __int_as_float((127 + e) << 23);
+      for (int pj = part; pj < 9; pj += 4) {
+        uint32_t w[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v = *qchunk(pj, k);
+          w[4 * k] = v.x;
+          w[4 * k + 1] = v.y;
+          w[4 * k + 2] = v.z;
+          w[4 * k + 3] = v.w;
+        }
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {   // dims 4 m .. 4 m + 3
+          uint32_t h01, l01, h23, l23;
+          split_e4m3x2(__uint_as_float(w[2 * m] << 16) * up, __uint_as_float(w[2 * m] & 0xffff0000u) * up, h01,
+                       l01);
+          split_e4m3x2(__uint_as_float(w[2 * m + 1] << 16) * up, __uint_as_float(w[2 * m + 1] & 0xffff0000u) * up,
+                       h23, l23);
+          hi[m] = h01 | (h23 << 16);
+          lo[m] = l01 | (l23 << 16);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          *qchunk(pj, k) = make_uint4(hi[4 * k], hi[4 * k + 1], hi[4 * k + 2], hi[4 * k + 3]);
+          *qchunk(pj, 4 + k) = make_uint4(lo[4 * k], lo[4 * k + 1], lo[4 * k + 2], lo[4 * k + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) arrive_lead(bar(base, kQReady), rank);
+      cq_next = c * __int_as_float((127 - e) << 23);
+      return true;
+    };
     int g = 0, unit_k = 0;
     for (int ui = u0; ui < u1 && ok; ++ui, ++unit_k) {
       const WorkUnit u = a.units[ui];
@@ -668,51 +646,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float lx = 0.f, lr = 0.f;              // this thread's share of the row sums
       float cq = c;                          // score scale of this thread's head
       if constexpr (kFp8) {
-        // ---- the unit's query (this CTA's 64 heads) from bf16 to f16 in
-        // place: row hl is scaled by 2^e so that its largest magnitude lies
-        // in [2^14, 2^15), and the scores by 2^-e.  The head's four threads
-        // take 16-byte chunks part, part + 4, .. of the row's 72 (9 panels x
-        // 8, 128-byte swizzle) ----
-        if (!(ok = mbar_wait_warp(bar(base, kQLand), unit_k & 1, abort_flag))) break;
-        const unsigned char* qrow = sm + kOffQ + hl * 128;
-        auto qchunk = [&](int idx) -> uint4* {
-          return reinterpret_cast<uint4*>(const_cast<unsigned char*>(qrow) + (idx >> 3) * kQPanel +
-                                          (((idx & 7) ^ (hl & 7)) << 4));
-        };
-        float mx = 0.f;
-        for (int idx = part; idx < 72; idx += 4) {
-          const uint4 v = *qchunk(idx);
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            mx = fmaxf(mx, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xffff0000u))));
-        }
-        float* qred = reinterpret_cast<float*>(sm + kOffQRed);
-        qred[part * 64 + hl] = mx;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(base, kQRed));
-        if (!(ok = mbar_wait_warp(bar(base, kQRed), unit_k & 1, abort_flag))) break;
-        const float rm = fmaxf(fmaxf(qred[hl], qred[64 + hl]), fmaxf(qred[128 + hl], qred[192 + hl]));
-        // rows of zeros (heads past H) keep e = 0
-        int e = 0;
-        if (rm > 0.f && rm < INFINITY) e = min(max(14 - (((__float_as_int(rm) >> 23) & 0xff) - 127), -100), 100);
-        const float up = __int_as_float((127 + e) << 23);
-        for (int idx = part; idx < 72; idx += 4) {
-          uint4* ch = qchunk(idx);
-          const uint4 v = *ch;
-          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-          uint32_t o[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const __half2 h2 = __floats2half2_rn(__uint_as_float(w[k] << 16) * up, __uint_as_float(w[k] & 0xffff0000u) * up);
-            o[k] = *reinterpret_cast<const uint32_t*>(&h2);
-          }
-          *ch = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) arrive_lead(bar(base, kQReady), rank);
-        cq = c * __int_as_float((127 - e) << 23);
+        if (unit_k == 0 && !(ok = split_query(0))) break;
+        cq = cq_next;
       }
       for (int i = 0; i < n && ok; ++i, ++g) {
         const bool first = i == 0;
@@ -750,24 +685,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         float alpha = 1.f;
         if (first) {
           ref = mt;
-        } else if (mt > ref + kRescaleThreshold) {
+        } else if (mt > ref + (kFp8 ? kRescaleThresholdFp8 : kRescaleThreshold)) {
           alpha = exp2f(ref - mt);
           ref = mt;
         }
-        // ---- p = 2^(y - reference), rounded to bf16; row sums ----
+        // ---- p = 2^(y - reference) rounded to bf16, or 2^(y - reference)
+        // * 2^6 as e4m3 hi + lo terms (this thread's 64 tokens: hi codes in
+        // words 0..15, lo codes in words 16..31); row sums ----
         uint32_t pk[32];
         {
           float sx = 0.f, sr = 0.f;
+          if constexpr (kFp8) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float p0 = fast_exp2(y[2 * j] - ref), p1 = fast_exp2(y[2 * j + 1] - ref);
-            sx += p0 + p1;
-            if constexpr (kFp8) {
-              const __half2 h2 = __floats2half2_rn(p0, p1);
-              pk[j] = *reinterpret_cast<const uint32_t*>(&h2);
-              const float2 f2 = __half22float2(h2);
-              sr += f2.x + f2.y;
-            } else {
+            for (int m = 0; m < 16; ++m) {
+              const float p0 = fast_exp2(y[4 * m] - ref) * kPScaleFp8, p1 = fast_exp2(y[4 * m + 1] - ref) * kPScaleFp8;
+              const float p2 = fast_exp2(y[4 * m + 2] - ref) * kPScaleFp8;
+              const float p3 = fast_exp2(y[4 * m + 3] - ref) * kPScaleFp8;
+              sx += (p0 + p1) + (p2 + p3);
+              uint32_t h01, l01, h23, l23;
+              sr += split_e4m3x2(p0, p1, h01, l01) + split_e4m3x2(p2, p3, h23, l23);
+              pk[m] = h01 | (h23 << 16);
+              pk[16 + m] = l01 | (l23 << 16);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float p0 = fast_exp2(y[2 * j] - ref), p1 = fast_exp2(y[2 * j + 1] - ref);
+              sx += p0 + p1;
               const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
               const uint32_t w = *reinterpret_cast<const uint32_t*>(&b2);
               pk[j] = w;
@@ -800,7 +744,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st_wait();
         }
         // ---- P row of this head over this thread's 64 tokens: one 128-byte
-        // row of token panel 2 tq + ch (K-major, 128-byte swizzle) ----
+        // row of token panel 2 tq + ch (K-major, 128-byte swizzle; e4m3: the
+        // 64 hi codes, then the 64 lo codes) ----
         {
           unsigned char* prow = sm + kOffP + (g % kPBufs) * kPBuf + part * kPPanel + hl * 128;
 #pragma unroll
@@ -814,6 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
+      if (kFp8 && ui + 1 < u1 && !(ok = split_query((unit_k + 1) & 1))) break;
       // ================= epilogue of the unit =================
       {
         sums[part * 64 + hl] = make_float2(lx, lr);
@@ -827,7 +773,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           sx += s.x;
           sr += s.y;
         }
-        const float ls = (ref + log2f(sx)) * kLn2;
+        // (e4m3 P carries the factor 2^6, in both sums)
+        const float ls = (ref - (kFp8 ? kPOffsetFp8 : 0.f) + log2f(sx)) * kLn2;
         const float inv = a.kv_scale / sr;
         const bool split = u.out_slot >= 0;
         if (part == 0 && h < H) {

@@ -417,6 +417,20 @@ __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint6
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
       : "memory");
 }
+// The same with e4m3 operands (kind::f8f6f4; the instruction descriptor's A
+// and B formats 0 = e4m3).
+__device__ __forceinline__ void mma_pair_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate, uint32_t issue) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p, q;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "setp.ne.b32 q, %5, 0;\n"
+      "@q tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
 // One arrive, once every pair MMA issued so far by this thread has completed,
 // on the mbarrier at this shared-memory offset in each CTA of cta_mask.
 __device__ __forceinline__ void commit_pair(uint32_t bar, uint16_t cta_mask, uint32_t issue) {

@@ -1,15 +1,24 @@
-"""Why the fp8-cache path multiplies in bf16 (host only, no GPU).
+"""Which operands the fp8-cache products may take (host only, no GPU).
 
-An fp8 e4m3 cache could feed kind::f8f6f4 tensor-core products, but then both
-operands of each product are e4m3: the query (for the scores) and the
+An fp8 e4m3 cache feeds kind::f8f6f4 tensor-core products only if the other
+operand of each product is e4m3 too: the query (for the scores) and the
 probabilities P (for P . V).  This test emulates that arithmetic on an
 fp8-cache batch in float64, with the operands rounded as the MMA would see
 them, and compares it with the oracle (the exact attention over the
 dequantised cache) at the parity bar: max-abs <= 1e-2, relative L2 <= 5e-3,
-|delta lse| <= 1e-3.  bf16 operands (what the kernels use: every e4m3 code is
-exact in bf16) stay inside the bar; an e4m3 query (per-row scale to the e4m3
-range) or e4m3 P each break it.
+|delta lse| <= 1e-3.
+- bf16 operands (every e4m3 code is exact in bf16) stay inside the bar.
+- A single e4m3 query (per-row scale to the e4m3 range) or e4m3 P breaks it.
+- Two e4m3 terms per operand, x = hi + lo with hi = e4m3(x) and
+  lo = e4m3(x - hi), stay inside it, computed the way the CTA-pair kernel
+  does: the query scaled per row so that its largest magnitude lies in
+  [2^7, 2^8) (hi + lo is then the bf16 query exactly, but for elements
+  below 2^-2 after the scaling, which keep 2^-10), P in 256-token tiles
+  as 2^(s - reference) * 2^6 with a reference that moves when a tile's
+  maximum exceeds it by more than 2.5 (log2 units), the output divided by
+  the sum of the hi + lo values and the lse taken from the exact sum.
 """
+import math
 import numpy as np
 import pytest
 import torch
@@ -59,6 +68,58 @@ def _emulate(x, q_e4m3, p_e4m3):
     return np.stack(outs), np.stack(lses)
 
 
+def _f32(x):
+    return x.astype(np.float32).astype(np.float64)
+
+
+def _split(x):
+    hi = _e4m3(x)
+    return hi, _e4m3(_f32(x - hi))
+
+
+def _emulate_split(x, threshold=2.5, offset=6.0, tile=256):
+    qn, qp = O.decode_bf16(x.q_nope), O.decode_bf16(x.q_pe)
+    log2e = 1.0 / math.log(2.0)
+    outs, lses = [], []
+    for b in range(x.batch):
+        pages = x.kv_indices[x.kv_indptr[b]:x.kv_indptr[b + 1]]
+        L = int(x.kv_len[b])
+        C = O.decode_e4m3(x.ckv[pages].reshape(-1, 512))[:L]
+        R = O.decode_e4m3(x.kpe[pages].reshape(-1, 64))[:L]
+        q = np.concatenate([qn[b], qp[b]], axis=1)
+        K = np.concatenate([C, R], axis=1)
+        rm = np.abs(q).max(axis=1, keepdims=True)
+        e = np.where(rm > 0, 7 - np.floor(np.log2(np.where(rm > 0, rm, 1.0))), 0.0)
+        qs = q * 2.0 ** e
+        qh, ql = _split(qs)
+        # the bf16 query exactly from magnitude 2^-2 up; below, to 2^-10 (half
+        # the e4m3 subnormal step)
+        big = np.abs(qs) >= 0.25
+        assert np.array_equal((qh + ql)[big], qs[big])
+        assert np.abs(qh + ql - qs).max() <= 2.0 ** -10
+        y = _f32(_f32(qh @ K.T + ql @ K.T) * (x.sm_scale * x.kv_scale * log2e * 2.0 ** -e))
+        H = y.shape[0]
+        o, lx, lr, ref = np.zeros((H, 512)), np.zeros(H), np.zeros(H), None
+        for t0 in range(0, L, tile):
+            yt = y[:, t0:t0 + tile]
+            mt = yt.max(axis=1)
+            if ref is None:
+                ref, alpha = mt.copy(), np.ones(H)
+            else:
+                up = mt > ref + threshold
+                alpha = np.where(up, 2.0 ** (ref - mt), 1.0)
+                ref = np.where(up, mt, ref)
+            p = _f32(2.0 ** (yt - ref[:, None])) * 2.0 ** offset
+            assert p.max() < 448.0
+            ph, pl = _split(p)
+            lx = lx * alpha + p.sum(axis=1)
+            lr = lr * alpha + (ph + pl).sum(axis=1)
+            o = o * alpha[:, None] + (ph + pl) @ C[t0:t0 + tile]
+        outs.append(o / lr[:, None] * x.kv_scale)
+        lses.append((ref - offset + np.log2(lx)) * math.log(2.0))
+    return np.stack(outs), np.stack(lses)
+
+
 def _errors(out, lse, ref_out, ref_lse):
     err = out - ref_out
     return (float(np.abs(err).max()), float(np.linalg.norm(err) / np.linalg.norm(ref_out)),
@@ -80,3 +141,11 @@ def test_e4m3_operands_break_the_bar(batch, q_e4m3, p_e4m3):
     x, ref_out, ref_lse = batch
     e = _errors(*_emulate(x, q_e4m3, p_e4m3), ref_out, ref_lse)
     assert not _inside(e), e
+
+
+def test_split_e4m3_operands_meet_the_bar(batch):
+    x, ref_out, ref_lse = batch
+    e = _errors(*_emulate_split(x), ref_out, ref_lse)
+    assert _inside(e), e
+    # with margin: a tenth of the bar on the output, a hundredth on the lse
+    assert e[0] <= 1e-3 and e[1] <= 5e-4 and e[2] <= 1e-5, e
