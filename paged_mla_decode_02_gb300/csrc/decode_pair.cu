@@ -45,15 +45,15 @@
 // fp8 (e4m3) caches (pages of 32 or 64 tokens): both products are e4m3
 // MMAs (kind::f8f6f4) straight from the copied codes -- K panels of 64 dims
 // (64-byte rows) and V chunks of 2 x 128 dims (128-byte rows, MN-major), in
-// 8 KB ring slots, so a ring holds twice the tokens of the bf16 one.  The
-// other operand of each product is split into two e4m3 terms, x = hi + lo
-// (hi = e4m3(x), lo = e4m3(x - hi)), and both terms multiply the same codes
-// into the same accumulator: the query once per unit under a power-of-two
-// scale per head row (its largest magnitude in [2^7, 2^8): hi + lo is then
-// the bf16 query exactly, but for elements below 2^-2 after the scaling), P
-// per tile as p = 2^(s - reference) * 2^6 with a reference that moves when
-// the tile maximum exceeds it by more than 2.5 (p <= 2^8.5 < 448); hi + lo
-// keeps 8 significant bits of p, as bf16 does.
+// 8 KB ring slots.  The other operand of each product is split into two
+// e4m3 terms, x = hi + lo (hi = e4m3(x), lo = e4m3(x - hi)), and both terms
+// multiply the same codes into the same accumulator: the query once per
+// unit under a power-of-two scale per head row (its largest magnitude in
+// [2^7, 2^8): hi + lo is then the bf16 query exactly, but for elements
+// below 2^-2 after the scaling), P per tile as p = 2^(s - reference) * 2^5
+// with a reference that moves when the tile maximum exceeds it by more than
+// 3.5 (p <= 2^8.5 < 448); hi + lo keeps 8 significant bits of p, as bf16
+// does, down to 2^-2 (below, lo loses bits).  Two P buffers, by tile parity.
 //
 // Every wait is bounded (2 s); on expiry the kernel records
 // MLA_ERR_DEVICE_TIMEOUT, lets its copies and MMAs land, frees TMEM and
@@ -85,19 +85,6 @@ constexpr int kFirstSoftmaxWarp = 2;
 constexpr int kSoftmaxWarps = 8;
 constexpr int kVProducerWarp = 10;
 constexpr int kPvIssuerWarp = 11;
-// Ring slots: 16 KB (bf16: a K panel of 128 tokens x 64 dims, a V chunk of
-// 32 tokens x 256 dims) or 8 KB (e4m3, the same tokens and dims); either
-// way 64 KB of K slots and 48 KB of V slots.
-template <bool kFp8>
-struct Ring {
-  static constexpr int kSlotBytes = kFp8 ? 8192 : 16384;
-  static constexpr int kKSlots = 65536 / kSlotBytes;
-  static constexpr int kVSlots = 49152 / kSlotBytes;
-  static constexpr int kVPanels = kFp8 ? 2 : 4;   // MN panels (128-byte rows) of a V chunk
-};
-constexpr int kKSlotsMax = 8, kVSlotsMax = 6;
-constexpr int kKRingBytes = 65536, kVRingBytes = 49152;
-constexpr int kPBufs = 1;                  // P buffers (2: by tile parity)
 constexpr int kVChunkTok = kTcVChunkTok;   // 32 tokens per V chunk
 constexpr int kChunksPerTile = kT / kVChunkTok;
 static_assert(kVChunkTok == 32, "V chunk: two 16-token MMA slices");
@@ -107,26 +94,44 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // log2 units: the reference moves when a tile's maximum exceeds it by more
 // than this; p = 2^(s - reference) stays below 2^8 (bf16), and e4m3 hi + lo
-// take p * 2^6 <= 2^8.5 (the largest code is 448; a power of two keeps a
+// take p * 2^5 <= 2^8.5 (the largest code is 448; a power of two keeps a
 // lone token's p exact)
-constexpr float kRescaleThreshold = 8.0f, kRescaleThresholdFp8 = 2.5f;
-constexpr float kPOffsetFp8 = 6.0f, kPScaleFp8 = 64.0f;   // 2^kPOffsetFp8
+constexpr float kRescaleThreshold = 8.0f, kRescaleThresholdFp8 = 3.5f;
+constexpr float kPOffsetFp8 = 5.0f, kPScaleFp8 = 32.0f;   // 2^kPOffsetFp8
 
 // shared memory (offsets from the 1024-byte aligned base)
 constexpr int kOffQ = 0;                          // 9 panels x (64 heads x 128 B)
 constexpr int kQPanel = 64 * 128;
-constexpr int kOffP = kOffQ + 9 * kQPanel;        // P: 4 token panels x (64 heads x 128 B)
+constexpr int kOffP = kOffQ + 9 * kQPanel;        // P: 4 token panels x (64 heads x 128 B) per buffer
 constexpr int kPPanel = 64 * 128;
 constexpr int kPBuf = 4 * kPPanel;                // one P buffer: 32 KB
-constexpr int kOffKRing = kOffP + kPBufs * kPBuf;
-constexpr int kOffVRing = kOffKRing + kKRingBytes;
-constexpr int kOffRed = kOffVRing + kVRingBytes;          // maxima [2 parities][4 parts][64 heads] float
+constexpr int kPAndRings = 147456;                // P buffers + K ring + V ring: 144 KB
+constexpr int kOffRed = kOffP + kPAndRings;       // maxima [2 parities][4 parts][64 heads] float
 constexpr int kOffSum = kOffRed + 2 * 4 * 64 * 4;          // sums [4 parts][64 heads] float2
 constexpr int kOffQRed = kOffSum + 4 * 64 * 8;            // fp8: query row maxima [4 parts][64 heads] float
 constexpr int kOffFlags = kOffQRed + 4 * 64 * 4;          // abort, tmem slot
 constexpr int kOffBar = kOffFlags + 64;
-static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOffKRing % 1024 == 0 && kOffVRing % 1024 == 0,
-              "swizzle atoms");
+static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms");
+
+// The 144 KB after the query, per cache type:
+// - bf16: one P buffer (32 KB); 16 KB ring slots (a K panel of 128 tokens x
+//   64 dims, a V chunk of 32 tokens x 256 dims), 4 for K and 3 for V;
+// - e4m3: two P buffers (by tile parity: the softmax of a tile need not wait
+//   for the previous tile's P . V); 8 KB ring slots (the same tokens and
+//   dims), 5 for K and 5 for V.
+template <bool kFp8>
+struct Ring {
+  static constexpr int kPBufs = kFp8 ? 2 : 1;
+  static constexpr int kSlotBytes = kFp8 ? 8192 : 16384;
+  static constexpr int kKSlots = kFp8 ? 5 : 4;
+  static constexpr int kVSlots = kFp8 ? 5 : 3;
+  static constexpr int kVPanels = kFp8 ? 2 : 4;   // MN panels (128-byte rows) of a V chunk
+  static constexpr int kOffKRing = kOffP + kPBufs * kPBuf;
+  static constexpr int kOffVRing = kOffKRing + kKSlots * kSlotBytes;
+  static_assert(kOffVRing + kVSlots * kSlotBytes <= kOffRed, "rings fit before the reduction areas");
+  static_assert(kOffKRing % 1024 == 0 && kOffVRing % 1024 == 0, "swizzle atoms");
+};
+constexpr int kKSlotsMax = 5, kVSlotsMax = 5;
 
 enum Bar {
   kKFull0 = 0,                      // [K slots] even CTA: K slot loaded in both CTAs (1 arrival + both CTAs' bytes)
@@ -214,6 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   constexpr int kKSlots = Ring<kFp8>::kKSlots, kVSlots = Ring<kFp8>::kVSlots;
   constexpr int kSlotBytes = Ring<kFp8>::kSlotBytes, kVPanels = Ring<kFp8>::kVPanels;
+  constexpr int kPBufs = Ring<kFp8>::kPBufs;
+  constexpr int kOffKRing = Ring<kFp8>::kOffKRing, kOffVRing = Ring<kFp8>::kOffVRing;
+  static_assert(kKSlots <= kKSlotsMax && kVSlots <= kVSlotsMax, "barrier slots");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int worker = blockIdx.x >> 1;
   const int rank = static_cast<int>(cluster_ctarank());
@@ -690,7 +698,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ref = mt;
         }
         // ---- p = 2^(y - reference) rounded to bf16, or 2^(y - reference)
-        // * 2^6 as e4m3 hi + lo terms (this thread's 64 tokens: hi codes in
+        // * 2^5 as e4m3 hi + lo terms (this thread's 64 tokens: hi codes in
         // words 0..15, lo codes in words 16..31); row sums ----
         uint32_t pk[32];
         {
@@ -773,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           sx += s.x;
           sr += s.y;
         }
-        // (e4m3 P carries the factor 2^6, in both sums)
+        // (e4m3 P carries the factor 2^5, in both sums)
         const float ls = (ref - (kFp8 ? kPOffsetFp8 : 0.f) + log2f(sx)) * kLn2;
         const float inv = a.kv_scale / sr;
         const bool split = u.out_slot >= 0;

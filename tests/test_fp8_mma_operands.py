@@ -14,8 +14,8 @@ dequantised cache) at the parity bar: max-abs <= 1e-2, relative L2 <= 5e-3,
   does: the query scaled per row so that its largest magnitude lies in
   [2^7, 2^8) (hi + lo is then the bf16 query exactly, but for elements
   below 2^-2 after the scaling, which keep 2^-10), P in 256-token tiles
-  as 2^(s - reference) * 2^6 with a reference that moves when a tile's
-  maximum exceeds it by more than 2.5 (log2 units), the output divided by
+  as 2^(s - reference) * 2^5 with a reference that moves when a tile's
+  maximum exceeds it by more than 3.5 (log2 units), the output divided by
   the sum of the hi + lo values and the lse taken from the exact sum.
 """
 import math
@@ -77,7 +77,7 @@ def _split(x):
     return hi, _e4m3(_f32(x - hi))
 
 
-def _emulate_split(x, threshold=2.5, offset=6.0, tile=256):
+def _emulate_split(x, threshold=3.5, offset=5.0, tile=256):
     qn, qp = O.decode_bf16(x.q_nope), O.decode_bf16(x.q_pe)
     log2e = 1.0 / math.log(2.0)
     outs, lses = [], []
