@@ -113,11 +113,12 @@ class L2Flush:
 
 # DRAM traffic of the dominant kernel per launch on the deepseek workload, from
 # the committed ncu summaries: (summary, the sources the figure was taken of)
-PROFILES = {
-    "pair": ("decode_pair_deepseek.json",
-             ["decode_pair.cu", "tc_utils.cuh", "device_utils.cuh", "kernels.h", "mla_internal.h"]),
-    "tcgen05": ("decode_tc_deepseek.json",
-                ["decode_tc.cu", "tc_utils.cuh", "device_utils.cuh", "kernels.h", "mla_internal.h"]),
+PAIR_SOURCES = ["decode_pair.cu", "tc_utils.cuh", "device_utils.cuh", "kernels.h", "mla_internal.h"]
+PROFILES = {   # (kernel, workload) -> committed ncu figures and the sources they were taken from
+    ("pair", "deepseek"): ("decode_pair_deepseek.json", PAIR_SOURCES),
+    ("pair", "fp8"): ("decode_pair_fp8.json", PAIR_SOURCES),
+    ("tcgen05", "deepseek"): ("decode_tc_deepseek.json",
+                              ["decode_tc.cu", "tc_utils.cuh", "device_utils.cuh", "kernels.h", "mla_internal.h"]),
 }
 KERNEL_NAMES = {1: "tcgen05", 2: "mma_sync", 3: "pair"}   # mla_kernel_t values
 
@@ -137,9 +138,9 @@ def profiled_traffic(workload: str, kernel: str) -> float | None:
     kernel sources changed since it was taken (hash recorded beside the
     figure)."""
     import hashlib
-    if workload != "deepseek" or kernel not in PROFILES:
+    if (kernel, workload) not in PROFILES:
         return None
-    name, sources = PROFILES[kernel]
+    name, sources = PROFILES[(kernel, workload)]
     path = os.path.join(ROOT, "profiles", name)
     if not os.path.exists(path):
         return None

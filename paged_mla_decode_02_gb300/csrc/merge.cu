@@ -7,6 +7,8 @@
 // whose outputs were checked against plain attention in "[V1][Core]
 // FlashInfer attention backend for V1" (vLLM PR #14061, "Outstanding items").
 // A request with no tokens (n = 0) gets out = 0 and lse = -inf.
+// Two kernels: a flat one for many heads (one thread per request, head and
+// four dims) and a chunked one for few heads and many slots.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -184,6 +186,75 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
   }
 }
 
+// Many heads (H >= 64), the common split of a request into a few slots: one
+// thread per (merged request, head, 4 dims), looped over by the grid in
+// strides, each folding its slots four at a time (one memory round trip per
+// four slots) with no shared memory and no block-wide barrier, so several
+// blocks per SM keep many loads in flight.  Index i = ((e * 64 + d / 8) * H
+// + h) * 2 + half: consecutive threads read consecutive 16 bytes of a
+// partial; the two threads of (h, d / 8) join their halves through a shuffle
+// and the even one writes 8 output dims (16 bytes in bf16).
+constexpr int kFlatThreads = 256, kFlatBlocksPerSm = 4, kFlatAhead = 4;
+template <bool kOutF32>
+__global__ void __launch_bounds__(kFlatThreads, kFlatBlocksPerSm) merge_flat_kernel(const MergeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int H = a.num_heads;
+  const long long total = static_cast<long long>(a.params->n_merge) * (kDCkv / 8) * H * 2;
+  const long long stride = static_cast<long long>(gridDim.x) * kFlatThreads;
+  // every thread of a warp runs the same number of iterations (total is
+  // even and the stride a multiple of 32), so the shuffle below is uniform
+  for (long long i = static_cast<long long>(blockIdx.x) * kFlatThreads + threadIdx.x; i - (threadIdx.x & 31) < total;
+       i += stride) {
+    const bool live = i < total;
+    const int half = static_cast<int>(i & 1);
+    long long r = i >> 1;
+    const int h = static_cast<int>(r % H);
+    r /= H;
+    const int d8 = static_cast<int>(r % (kDCkv / 8));
+    const int e = static_cast<int>(r / (kDCkv / 8));
+    const int d = 8 * d8 + 4 * half;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float M = -INFINITY, W = 0.f;
+    MergeEntry me{0, 0, 0};
+    if (live) {
+      me = a.merge[e];
+      for (int i0 = 0; i0 < me.n_slots; i0 += kFlatAhead) {
+        float4 o[kFlatAhead];
+        float l[kFlatAhead];
+#pragma unroll
+        for (int j = 0; j < kFlatAhead; ++j)
+          if (i0 + j < me.n_slots) {
+            const int slot = me.first_slot + i0 + j;
+            o[j] = *reinterpret_cast<const float4*>(a.o_part + part_offset(slot, h, d, H));
+            l[j] = a.lse_part[lse_part_offset(slot, 0, h, H)];
+          }
+#pragma unroll
+        for (int j = 0; j < kFlatAhead; ++j)
+          if (i0 + j < me.n_slots) fold_state(M, W, acc, l[j], o[j]);
+      }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    const float4 v = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    // the odd thread's four dims, for the even one
+    const float4 u = make_float4(__shfl_down_sync(0xffffffffu, v.x, 1), __shfl_down_sync(0xffffffffu, v.y, 1),
+                                 __shfl_down_sync(0xffffffffu, v.z, 1), __shfl_down_sync(0xffffffffu, v.w, 1));
+    if (!live || half) continue;
+    const size_t row = static_cast<size_t>(me.req) * H + h;
+    if (kOutF32) {
+      float* dst = static_cast<float*>(a.out) + row * kDCkv + d;
+      *reinterpret_cast<float4*>(dst) = v;
+      *reinterpret_cast<float4*>(dst + 4) = u;
+    } else {
+      const __nv_bfloat162 b0 = __floats2bfloat162_rn(v.x, v.y), b1 = __floats2bfloat162_rn(v.z, v.w);
+      const __nv_bfloat162 b2 = __floats2bfloat162_rn(u.x, u.y), b3 = __floats2bfloat162_rn(u.z, u.w);
+      *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + row * kDCkv + d) =
+          make_uint4(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1),
+                     *reinterpret_cast<const uint32_t*>(&b2), *reinterpret_cast<const uint32_t*>(&b3));
+    }
+    if (d8 == 0) a.lse[row] = W > 0.f ? M + __logf(W) : -INFINITY;
+  }
+}
+
 // Two attention states of the same rows over disjoint token sets (a shared
 // prefix and a request's own suffix, say) combined into one: one warp per
 // row, 16 consecutive dims per lane (four 16-byte loads from each state), the
@@ -272,15 +343,28 @@ cudaError_t launch_merge(const MergeArgs& a, bool out_f32, cudaStream_t s) {
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       sms = 1;
   }
-  const int cap_items = a.merge_cap * (kDCkv / merge_chunk(a.num_heads));
-  cfg.gridDim = dim3(cap_items < 2 * sms ? cap_items : 2 * sms);
-  cfg.blockDim = dim3(kMergeThreads);
+  const bool flat = a.num_heads >= 64;
+  if (flat) {
+    // the flat kernel: a few blocks per SM, or fewer when the plan's capacity
+    // needs fewer threads
+    const long long cap_threads = static_cast<long long>(a.merge_cap) * (kDCkv / 8) * a.num_heads * 2;
+    const long long blocks = (cap_threads + kFlatThreads - 1) / kFlatThreads;
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks < kFlatBlocksPerSm * sms ? blocks : kFlatBlocksPerSm * sms));
+    cfg.blockDim = dim3(kFlatThreads);
+  } else {
+    const int cap_items = a.merge_cap * (kDCkv / merge_chunk(a.num_heads));
+    cfg.gridDim = dim3(cap_items < 2 * sms ? cap_items : 2 * sms);
+    cfg.blockDim = dim3(kMergeThreads);
+  }
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (flat)
+    return out_f32 ? cudaLaunchKernelEx(&cfg, merge_flat_kernel<true>, a)
+                   : cudaLaunchKernelEx(&cfg, merge_flat_kernel<false>, a);
   return out_f32 ? cudaLaunchKernelEx(&cfg, merge_kernel<true>, a) : cudaLaunchKernelEx(&cfg, merge_kernel<false>, a);
 }
 
