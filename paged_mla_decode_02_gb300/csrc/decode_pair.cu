@@ -22,17 +22,20 @@
 // scores were read" (the issuer may overwrite the S buffer) and "P is
 // written" (the issuer may start P . V).
 //
-// Per CTA: warp 0 K producer (the query once per unit, then the K panels of
-// every tile through a ring of 16 KB slots), warp 10 V producer (32-token V
-// chunks through a second ring); in the even CTA warp 1 issues every QK MMA
-// of the pair and warp 11 every PV MMA, so the softmax of tile g overlaps
-// the scores of tile g + 1 and the P . V of tile g - 1; warps 2..9 softmax
-// and epilogue: warp w reads TMEM lane quadrant w % 4 and column half
-// (w - 2) / 4, so each thread owns one head and 64 tokens of a tile, and the
-// four threads of a head combine their maxima through shared memory.
+// Per CTA: warp 0 K producer (the shared-memory part of the query once per
+// unit, then the K panels of every tile through a ring, two panels per slot
+// for bf16), warp 10 V producer (32-token V chunks through a second ring);
+// in the even CTA warp 1 issues every QK MMA of the pair and warp 11 every
+// PV MMA, so the softmax of tile g overlaps the scores of tile g + 1 and the
+// P . V of tile g - 1; warps 2..9 softmax and epilogue: warp w reads TMEM
+// lane quadrant w % 4 and column half (w - 2) / 4, so each thread owns one
+// head and 64 tokens of a tile, and the four threads of a head combine
+// their maxima through shared memory.  For bf16 the softmax warps also store
+// the query's dims [320, 576) into TMEM once per unit.
 //
-// TMEM columns: S double-buffered [0, 128) and [128, 256); O [256, 512)
-// (lane l < 64: dims [0, 256) of head 64 r + l; lane 64 + l: dims [256, 512)).
+// TMEM columns: S [0, 128); bf16: the query's dims [320, 576) [128, 256);
+// e4m3: a second S buffer [128, 256); O [256, 512) (lane l < 64: dims
+// [0, 256) of head 64 r + l; lane 64 + l: dims [256, 512)).
 //
 // Softmax, per tile and head: the exact maximum over the tile's 256 tokens,
 // a reference that moves only when that maximum exceeds it by more than 2^8
@@ -88,8 +91,12 @@ constexpr int kPvIssuerWarp = 11;
 constexpr int kVChunkTok = kTcVChunkTok;   // 32 tokens per V chunk
 constexpr int kChunksPerTile = kT / kVChunkTok;
 static_assert(kVChunkTok == 32, "V chunk: two 16-token MMA slices");
+// TMEM columns: S [0, 128) (e4m3: a second S buffer [128, 256)); bf16: the
+// query's dims [320, 576) as the QK A operand in [128, 256), row 64 r + l of
+// A in lanes l and 64 + l of CTA r; O [256, 512).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256;
+constexpr uint32_t kColS = 0, kColQT = 128, kColO = 256;
+constexpr int kQTDim0 = 320;               // first query dim held in TMEM (bf16)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // log2 units: the reference moves when a tile's maximum exceeds it by more
@@ -100,36 +107,45 @@ constexpr float kRescaleThreshold = 8.0f, kRescaleThresholdFp8 = 3.5f;
 constexpr float kPOffsetFp8 = 5.0f, kPScaleFp8 = 32.0f;   // 2^kPOffsetFp8
 
 // shared memory (offsets from the 1024-byte aligned base)
-constexpr int kOffQ = 0;                          // 9 panels x (64 heads x 128 B)
+constexpr int kOffQ = 0;                          // query panels x (64 heads x 128 B)
 constexpr int kQPanel = 64 * 128;
-constexpr int kOffP = kOffQ + 9 * kQPanel;        // P: 4 token panels x (64 heads x 128 B) per buffer
 constexpr int kPPanel = 64 * 128;
-constexpr int kPBuf = 4 * kPPanel;                // one P buffer: 32 KB
-constexpr int kPAndRings = 147456;                // P buffers + K ring + V ring: 144 KB
-constexpr int kOffRed = kOffP + kPAndRings;       // maxima [2 parities][4 parts][64 heads] float
+constexpr int kPBuf = 4 * kPPanel;                // one P buffer (4 token panels): 32 KB
+constexpr int kOffRed = 221184;                   // 216 KB: query, P and the rings before it
 constexpr int kOffSum = kOffRed + 2 * 4 * 64 * 4;          // sums [4 parts][64 heads] float2
 constexpr int kOffQRed = kOffSum + 4 * 64 * 8;            // fp8: query row maxima [4 parts][64 heads] float
 constexpr int kOffFlags = kOffQRed + 4 * 64 * 4;          // abort, tmem slot
 constexpr int kOffBar = kOffFlags + 64;
-static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms");
 
-// The 144 KB after the query, per cache type:
-// - bf16: one P buffer (32 KB); 16 KB ring slots (a K panel of 128 tokens x
-//   64 dims, a V chunk of 32 tokens x 256 dims), 4 for K and 3 for V;
-// - e4m3: two P buffers (by tile parity: the softmax of a tile need not wait
-//   for the previous tile's P . V); 8 KB ring slots (the same tokens and
-//   dims), 5 for K and 5 for V.
+// The 216 KB before the reduction areas, per cache type:
+// - bf16: the query's dims [0, 320) (5 panels, 40 KB; dims [320, 576) are
+//   in TMEM), one P buffer (32 KB), 3 K ring slots of two 16 KB K panels
+//   (128 tokens x 64 dims each: one barrier, one wait and one commit per two
+//   panels -- each wait before an MMA issue costs the issuing thread over a
+//   hundred cycles) and 3 V ring slots of 16 KB (a V chunk of 32 tokens x
+//   256 dims);
+// - e4m3: the whole query split into hi + lo terms (9 panels, 72 KB), two
+//   P buffers (by tile parity: the softmax of a tile need not wait for the
+//   previous tile's P . V), 8 KB ring slots (the same tokens and dims): 5
+//   for K, 5 for V.
 template <bool kFp8>
 struct Ring {
+  static constexpr bool kQTmem = !kFp8;   // part of the query in TMEM (then one S buffer)
+  static constexpr int kQSmemPanels = kQTmem ? kQTDim0 / 64 : 9;
+  static constexpr int kSBufs = kQTmem ? 1 : 2;
   static constexpr int kPBufs = kFp8 ? 2 : 1;
-  static constexpr int kSlotBytes = kFp8 ? 8192 : 16384;
-  static constexpr int kKSlots = kFp8 ? 5 : 4;
+  static constexpr int kPanelBytes = kFp8 ? 8192 : 16384;   // one K panel (128 rows)
+  static constexpr int kKPanelsPerSlot = kFp8 ? 1 : 2;
+  static constexpr int kKSlotBytes = kPanelBytes * kKPanelsPerSlot;
+  static constexpr int kVSlotBytes = kFp8 ? 8192 : 16384;   // one V chunk
+  static constexpr int kKSlots = kFp8 ? 5 : 3;
   static constexpr int kVSlots = kFp8 ? 5 : 3;
   static constexpr int kVPanels = kFp8 ? 2 : 4;   // MN panels (128-byte rows) of a V chunk
+  static constexpr int kOffP = kOffQ + kQSmemPanels * kQPanel;
   static constexpr int kOffKRing = kOffP + kPBufs * kPBuf;
-  static constexpr int kOffVRing = kOffKRing + kKSlots * kSlotBytes;
-  static_assert(kOffVRing + kVSlots * kSlotBytes <= kOffRed, "rings fit before the reduction areas");
-  static_assert(kOffKRing % 1024 == 0 && kOffVRing % 1024 == 0, "swizzle atoms");
+  static constexpr int kOffVRing = kOffKRing + kKSlots * kKSlotBytes;
+  static_assert(kOffVRing + kVSlots * kVSlotBytes <= kOffRed, "rings fit before the reduction areas");
+  static_assert(kOffP % 1024 == 0 && kOffKRing % 1024 == 0 && kOffVRing % 1024 == 0, "swizzle atoms");
 };
 constexpr int kKSlotsMax = 5, kVSlotsMax = 5;
 
@@ -218,8 +234,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffFlags + 4);
 
   constexpr int kKSlots = Ring<kFp8>::kKSlots, kVSlots = Ring<kFp8>::kVSlots;
-  constexpr int kSlotBytes = Ring<kFp8>::kSlotBytes, kVPanels = Ring<kFp8>::kVPanels;
-  constexpr int kPBufs = Ring<kFp8>::kPBufs;
+  constexpr int kVPanels = Ring<kFp8>::kVPanels;
+  constexpr int kPanelBytes = Ring<kFp8>::kPanelBytes, kKPanelsPerSlot = Ring<kFp8>::kKPanelsPerSlot;
+  constexpr int kKSlotBytes = Ring<kFp8>::kKSlotBytes, kVSlotBytes = Ring<kFp8>::kVSlotBytes;
+  constexpr int kPBufs = Ring<kFp8>::kPBufs, kSBufs = Ring<kFp8>::kSBufs;
+  constexpr int kQSmemPanels = Ring<kFp8>::kQSmemPanels;
+  constexpr bool kQTmem = Ring<kFp8>::kQTmem;
+  constexpr int kOffP = Ring<kFp8>::kOffP;
   constexpr int kOffKRing = Ring<kFp8>::kOffKRing, kOffVRing = Ring<kFp8>::kOffVRing;
   static_assert(kKSlots <= kKSlotsMax && kVSlots <= kVSlotsMax, "barrier slots");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -239,6 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (i == kSFree0 || i == kSFree0 + 1 || i == kPReady0 || i == kPReady0 + 1 || i == kOFree)
         cnt = 2 * kSoftmaxWarps;
       if (i == kRed0 || i == kRed0 + 1 || i == kSum || i == kQRed) cnt = kSoftmaxWarps;
+      // all 8 softmax warps of both CTAs: split the query (e4m3), store its
+      // TMEM part (bf16)
       if (i == kQReady) cnt = 2 * kSoftmaxWarps;
       mbar_init(bar(base, i), cnt);
     }
@@ -320,15 +343,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return true;
       }
-      if (lane == 0 && rank == 0) mbar_arrive_expect_tx(bar(base, kQFull), 2 * 9 * kQPanel);
+      // bf16: the query's dims [0, 320) into shared memory (the rest goes to
+      // TMEM, loaded by the softmax warps)
+      if (lane == 0 && rank == 0) mbar_arrive_expect_tx(bar(base, kQFull), 2 * kQSmemPanels * kQPanel);
       __syncwarp();
-      if (lane < 9) {
+      if (lane < kQSmemPanels) {
         const int row = v.req * H + 64 * rank;   // rows past the batch are zero-filled
-        if (lane < 8)
-          tma_load_2d_pair(base + kOffQ + lane * kQPanel, &maps.q_nope, 64 * lane, row,
-                           map_to_rank(bar(base, kQFull), lead));
-        else
-          tma_load_2d_pair(base + kOffQ + 8 * kQPanel, &maps.q_pe, 0, row, map_to_rank(bar(base, kQFull), lead));
+        tma_load_2d_pair(base + kOffQ + lane * kQPanel, &maps.q_nope, 64 * lane, row,
+                         map_to_rank(bar(base, kQFull), lead));
       }
       return true;
     };
@@ -340,18 +362,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int cnt1 = max(0, min(kHalfT, v.tok_end - (v.tok_begin + i * kT + kHalfT)));
       const int nbox_both = nbox + (cnt1 + P - 1) / P;
       const int pb = (kHalfT * rank) / P;   // first page of this half within the tile
-      const int page = __shfl_sync(0xffffffffu, pages, min(pb + lane, 31));
       // a panel row: 64 dims, 128 bytes (bf16) or 64 (e4m3)
       constexpr int row_bytes = kFp8 ? 64 : 128;
-      for (int j = 0; j < 9; ++j) {
+      // lane -> (panel jj of the slot, page box b): lanes [0, np * nbox)
+      const int b = lane % max(nbox, 1), jj = lane / max(nbox, 1);
+      const int page = __shfl_sync(0xffffffffu, pages, min(pb + b, 31));
+      for (int j0 = 0; j0 < 9; j0 += kKPanelsPerSlot) {
+        const int np = min(kKPanelsPerSlot, 9 - j0);   // panels j0 .. j0 + np - 1 in this slot
         int slot;
         if (!(ok = next_slot(slot))) return false;
         const uint32_t full = map_to_rank(bar(base, kKFull0 + slot), lead);
         if (lane == 0 && rank == 0)
-          mbar_arrive_expect_tx(bar(base, kKFull0 + slot), nbox_both * P * row_bytes);
+          mbar_arrive_expect_tx(bar(base, kKFull0 + slot), np * nbox_both * P * row_bytes);
         __syncwarp();
-        if (lane < nbox) {
-          const uint32_t dst = base + kOffKRing + slot * kSlotBytes + lane * P * row_bytes;
+        if (lane < np * nbox) {
+          const int j = j0 + jj;
+          const uint32_t dst = base + kOffKRing + slot * kKSlotBytes + jj * kPanelBytes + b * P * row_bytes;
           if (j < 8)
             tma_load_2d_pair(dst, &maps.ckv_k, 64 * j, page * P, full);
           else
@@ -376,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tb = t + vbox * min(lane, ncopy - 1);
         const int page = __shfl_sync(0xffffffffu, pages, (tb - tok0) / P);
         const int copy_bytes = vbox * kVPanels * 128;
-        const uint32_t dst = base + kOffVRing + slot * kSlotBytes + lane * copy_bytes;
+        const uint32_t dst = base + kOffVRing + slot * kVSlotBytes + lane * copy_bytes;
         if (rows == kVChunkTok) {
           if (lane == 0 && rank == 0) mbar_arrive_expect_tx(bar(base, kVFull0 + slot), 2 * ncopy * copy_bytes);
           __syncwarp();
@@ -390,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane < ncopy) tma_load_3d(dst, &maps.ckv_v, 0, page * P + (tb % P), kVPanels * rank, tail);
           if (!(ok = mbar_wait_warp(tail, tail_uses & 1, abort_flag))) return false;
-          unsigned char* sv = sm + kOffVRing + slot * kSlotBytes;
+          unsigned char* sv = sm + kOffVRing + slot * kVSlotBytes;
           // 16-byte chunks of the rows past the end: 8 per panel row
           for (int q = lane; q < (kVChunkTok - rows) * kVPanels * 8; q += 32) {
             const int rr = rows + q / (kVPanels * 8), pnl = (q % (kVPanels * 8)) >> 3, c16 = q & 7;
@@ -447,36 +473,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int ui = u0; ui < u1 && ok; ++ui, ++unit_k) {
         const WorkUnit v = a.units[ui];
         const int n = tiles_of(v);
-        // the unit's query: loaded (bf16) or split into e4m3 terms in both CTAs (fp8)
-        if (!(ok = kFp8 ? mbar_wait_cl_warp(bar(base, kQReady), unit_k & 1, abort_flag)
-                        : mbar_wait_warp(bar(base, kQFull), unit_k & 1, abort_flag)))
-          break;
+        // the unit's query: split into e4m3 terms in both CTAs (fp8), or its
+        // shared-memory part copied and its TMEM part stored (bf16)
+        if ((kFp8 || kQTmem) && !(ok = mbar_wait_cl_warp(bar(base, kQReady), unit_k & 1, abort_flag))) break;
+        if (!kFp8 && !(ok = mbar_wait_warp(bar(base, kQFull), unit_k & 1, abort_flag))) break;
         for (int i = 0; i < n && ok; ++i, ++g) {
-          if (g >= 2 && !(ok = mbar_wait_cl_warp(bar(base, kSFree0 + (g & 1)), ((g - 2) >> 1) & 1, abort_flag)))
+          // the S buffer this tile writes was read by the softmax
+          if (kSBufs == 2 && g >= 2 &&
+              !(ok = mbar_wait_cl_warp(bar(base, kSFree0 + (g & 1)), ((g - 2) >> 1) & 1, abort_flag)))
+            break;
+          if (kSBufs == 1 && g >= 1 && !(ok = mbar_wait_cl_warp(bar(base, kSFree0), (g - 1) & 1, abort_flag)))
             break;
           tc_fence_after();
-          const uint32_t d = tmem + kColS + 128 * (g & 1);
-          for (int j = 0; j < 9; ++j, ++kc) {
+          const uint32_t d = tmem + kColS + 128 * (kSBufs == 2 ? (g & 1) : 0);
+          for (int j0 = 0; j0 < 9; j0 += kKPanelsPerSlot, ++kc) {
             const int slot = kc % kKSlots;
             const uint32_t par = (kc / kKSlots) & 1;
             if (!(ok = mbar_wait_warp(bar(base, kKFull0 + slot), par, abort_flag))) break;
             tc_fence_after();
-            const uint64_t adesc = q_desc0 + static_cast<uint64_t>((j * kQPanel) >> 4);
-            const uint64_t bdesc = k_desc0 + static_cast<uint64_t>((slot * kSlotBytes) >> 4);
-            if constexpr (kFp8) {
-              // dims [64 j + 32 kk, + 32): the query's hi codes at byte 32 kk
-              // of its row, its lo codes at 64 + 32 kk, the K codes at 32 kk
+            for (int j = j0; j < j0 + kKPanelsPerSlot && j < 9; ++j) {
+              const uint64_t adesc = q_desc0 + static_cast<uint64_t>((j * kQPanel) >> 4);
+              const uint64_t bdesc =
+                  k_desc0 + static_cast<uint64_t>((slot * kKSlotBytes + (j - j0) * kPanelBytes) >> 4);
+              if constexpr (kFp8) {
+                // dims [64 j + 32 kk, + 32): the query's hi codes at byte 32 kk
+                // of its row, its lo codes at 64 + 32 kk, the K codes at 32 kk
 #pragma unroll
-              for (int kk = 0; kk < 2; ++kk) {
-                const uint64_t b = bdesc + static_cast<uint64_t>(kk * 2);
-                mma_pair_e4m3(d, adesc + static_cast<uint64_t>(kk * 2), b, id_qk, (j | kk) != 0, issue);
-                mma_pair_e4m3(d, adesc + static_cast<uint64_t>(4 + kk * 2), b, id_qk, 1u, issue);
+                for (int kk = 0; kk < 2; ++kk) {
+                  const uint64_t b = bdesc + static_cast<uint64_t>(kk * 2);
+                  mma_pair_e4m3(d, adesc + static_cast<uint64_t>(kk * 2), b, id_qk, (j | kk) != 0, issue);
+                  mma_pair_e4m3(d, adesc + static_cast<uint64_t>(4 + kk * 2), b, id_qk, 1u, issue);
+                }
+              } else if (j < kQSmemPanels) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_pair(d, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2), id_qk,
+                           (j | kk) != 0, issue);
+              } else {
+                // dims [64 j, 64 j + 64) of the query from TMEM: 8 columns per
+                // 16-dim K step
+                const uint32_t a_t = tmem + kColQT + (64 * j - kQTDim0) / 2;
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_pair_ts(d, a_t + 8 * kk, bdesc + static_cast<uint64_t>(kk * 2), id_qk, 1u, issue);
               }
-            } else {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_pair(d, adesc + static_cast<uint64_t>(kk * 2), bdesc + static_cast<uint64_t>(kk * 2), id_qk,
-                         (j | kk) != 0, issue);
             }
             commit_pair(bar(base, kKEmpty0 + slot), 3, issue);
           }
@@ -525,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int bb = 0; bb < 2; ++bb) {
                 const uint64_t bdesc =
-                    v_desc0 + static_cast<uint64_t>((slot * kSlotBytes + bb * kVChunkTok * 128) >> 4);
+                    v_desc0 + static_cast<uint64_t>((slot * kVSlotBytes + bb * kVChunkTok * 128) >> 4);
                 mma_pair_e4m3(tmem + kColO + 128 * bb, a_hi, bdesc, id_pv, (i == 0 && c == 0) ? 0u : 1u, issue);
                 mma_pair_e4m3(tmem + kColO + 128 * bb, a_hi + 4, bdesc, id_pv, 1u, issue);
               }
@@ -538,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int bb = 0; bb < 2; ++bb) {
                   const uint64_t bdesc =
-                      v_desc0 + static_cast<uint64_t>((slot * kSlotBytes + kk * v_kstep + bb * v_block) >> 4);
+                      v_desc0 + static_cast<uint64_t>((slot * kVSlotBytes + kk * v_kstep + bb * v_block) >> 4);
                   mma_pair(tmem + kColO + 128 * bb, adesc, bdesc, id_pv, (i == 0 && c == 0 && kk == 0) ? 0u : 1u,
                            issue);
                 }
@@ -646,10 +686,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       cq_next = c * __int_as_float((127 - e) << 23);
       return true;
     };
+    // bf16: the query's dims [320, 576) of this thread's head (request req)
+    // into TMEM columns [128, 256) of this thread's lane, where the QK MMAs
+    // read them as A (column half ch: dims [320 + 128 ch, + 128)).  Every
+    // row is held twice, in lanes hl and 64 + hl (quadrants q and q + 2 have
+    // the same heads): an M = 128 pair MMA reads A row 64 r + l from lane l
+    // for the D columns of this CTA's half of B and from lane 64 + l for the
+    // other CTA's half.  The previous unit's QK MMAs read the same columns:
+    // unless wait_parity < 0, wait for them (kQFree) first.  Returns false
+    // when the wait runs out.
+    auto load_query_tmem = [&](int req, int wait_parity) -> bool {
+      uint32_t w0[32], w1[32];
+      if (h < H) {
+        const size_t row = static_cast<size_t>(req) * H + h;
+        const uint4* src0 = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_nope) +
+                                                            row * kDCkv + kQTDim0 + 128 * ch);
+        // ch 0: dims [320, 448) of q_nope; ch 1: [448, 512) of q_nope, then q_pe
+        const uint4* src1 =
+            ch == 0 ? src0 + 8 : reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q_pe) + row * kDKpe);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint4 v0 = src0[k], v1 = src1[k];
+          w0[4 * k] = v0.x, w0[4 * k + 1] = v0.y, w0[4 * k + 2] = v0.z, w0[4 * k + 3] = v0.w;
+          w1[4 * k] = v1.x, w1[4 * k + 1] = v1.y, w1[4 * k + 2] = v1.z, w1[4 * k + 3] = v1.w;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) w0[k] = w1[k] = 0u;
+      }
+      if (wait_parity >= 0 && !mbar_wait_warp(bar(base, kQFree), static_cast<uint32_t>(wait_parity), abort_flag))
+        return false;
+      tc_fence_after();
+      tmem_st32(lane_addr + kColQT + 64 * ch, w0);
+      tmem_st32(lane_addr + kColQT + 64 * ch + 32, w1);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) arrive_lead(bar(base, kQReady), rank);
+      return true;
+    };
     int g = 0, unit_k = 0;
     for (int ui = u0; ui < u1 && ok; ++ui, ++unit_k) {
       const WorkUnit u = a.units[ui];
       const int n = tiles_of(u);
+      if (kQTmem && unit_k == 0 && !(ok = load_query_tmem(u.req, -1))) break;
       float ref = 0.f;                       // the head's reference (the same in its four threads)
       float lx = 0.f, lr = 0.f;              // this thread's share of the row sums
       float cq = c;                          // score scale of this thread's head
@@ -666,7 +746,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float mx = -INFINITY;
         {
           uint32_t v0[32], v1[32];
-          const uint32_t col = kColS + 128 * (g & 1) + 64 * ch;
+          const uint32_t col = kColS + 128 * (kSBufs == 2 ? (g & 1) : 0) + 64 * ch;
           tmem_ld32(lane_addr + col, v0);
           tmem_ld32(lane_addr + col + 32, v1);
           tmem_ld_wait();
@@ -681,7 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) arrive_lead(bar(base, kSFree0 + (g & 1)), rank);
+        if (lane == 0) arrive_lead(bar(base, kSFree0 + (kSBufs == 2 ? (g & 1) : 0)), rank);
         // ---- the head's maximum over the tile (its four threads) ----
         float* rd = red + (g & 1) * 4 * 64;
         rd[part * 64 + hl] = mx;
@@ -768,6 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       if (kFp8 && ui + 1 < u1 && !(ok = split_query((unit_k + 1) & 1))) break;
+      if (kQTmem && ui + 1 < u1 && !(ok = load_query_tmem(a.units[ui + 1].req, unit_k & 1))) break;
       // ================= epilogue of the unit =================
       {
         sums[part * 64 + hl] = make_float2(lx, lr);

@@ -417,6 +417,22 @@ __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint6
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
       : "memory");
 }
+// D[tmem] (+)= A[tmem] * B[smem]^T over the pair, A from TMEM: for M = 128,
+// row 64 r + l of A is read from lane l of CTA r (lanes 64..127 unused),
+// each 32-bit column holding two consecutive K elements (the first in the
+// low half).  Issued and predicated like mma_pair.
+__device__ __forceinline__ void mma_pair_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate, uint32_t issue) {
+  asm volatile(
+      "{\n"
+      ".reg .pred p, q;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "setp.ne.b32 q, %5, 0;\n"
+      "@q tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n"
+      "}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+      : "memory");
+}
 // The same with e4m3 operands (kind::f8f6f4; the instruction descriptor's A
 // and B formats 0 = e4m3).
 __device__ __forceinline__ void mma_pair_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
