@@ -105,6 +105,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 // lone token's p exact)
 constexpr float kRescaleThreshold = 8.0f, kRescaleThresholdFp8 = 3.5f;
 constexpr float kPOffsetFp8 = 5.0f, kPScaleFp8 = 32.0f;   // 2^kPOffsetFp8
+// The K copies of tile t wait until the V copies have reached chunk
+// 8 t - kKLeadChunks (8 chunks per tile): V re-reads the K rows from L2, and
+// a K stream far ahead of V pushes them out first (measured on long
+// requests at a high DRAM rate).
+constexpr int kKLeadChunks = 12;
 
 // shared memory (offsets from the 1024-byte aligned base)
 constexpr int kOffQ = 0;                          // query panels x (64 heads x 128 B)
@@ -114,7 +119,7 @@ constexpr int kPBuf = 4 * kPPanel;                // one P buffer (4 token panel
 constexpr int kOffRed = 221184;                   // 216 KB: query, P and the rings before it
 constexpr int kOffSum = kOffRed + 2 * 4 * 64 * 4;          // sums [4 parts][64 heads] float2
 constexpr int kOffQRed = kOffSum + 4 * 64 * 8;            // fp8: query row maxima [4 parts][64 heads] float
-constexpr int kOffFlags = kOffQRed + 4 * 64 * 4;          // abort, tmem slot
+constexpr int kOffFlags = kOffQRed + 4 * 64 * 4;          // abort, tmem slot, V tiles issued
 constexpr int kOffBar = kOffFlags + 64;
 
 // The 216 KB before the reduction areas, per cache type:
@@ -252,8 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int u0 = worker < prm.n_workers ? a.worker_ptr[worker] : 0;
   const int u1 = worker < prm.n_workers ? a.worker_ptr[worker + 1] : 0;
 
+  volatile int* v_tiles = reinterpret_cast<volatile int*>(sm + kOffFlags + 8);
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    *v_tiles = 0;
     for (int i = 0; i < kNumBars; ++i) {
       uint32_t cnt = 1;
       if (i == kTailReady) cnt = 2;
@@ -386,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     };
-    auto emit_v = [&](const WorkUnit& v, int i, int pages) -> bool {
+    auto emit_v = [&](const WorkUnit& v, int i, int pages, int vt) -> bool {
       const int tok0 = v.tok_begin + i * kT;
       for (int c = 0; c < kChunksPerTile; ++c) {
         const int t = tok0 + kVChunkTok * c;
@@ -395,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int slot;
         if (!(ok = next_slot(slot))) return false;
         const uint32_t full = map_to_rank(bar(base, kVFull0 + slot), lead);
+        if (lane == 0 && c > 0) *v_tiles = 8 * vt + c;   // chunks before this one issued
         if (stalled()) continue;
         // one copy: vbox rows of kVPanels panels (128-byte rows), this CTA's
         // 256 dims
@@ -439,16 +447,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       return true;
     };
+    int t = 0;   // tiles of this CTA so far
     for (int ui = u0; ui < u1 && ok; ++ui) {
       const WorkUnit v = a.units[ui];
       const int n = tiles_of(v);
-      for (int i = 0; i < n && ok; ++i) {
+      for (int i = 0; i < n && ok; ++i, ++t) {
         const int pages = tile_pages(v, i);
         if (is_k) {
           if (i == 0 && !emit_q(v)) break;
+          // at most kKLeadChunks V chunks ahead of the V copies (bounded wait)
+          if (8 * t > kKLeadChunks) {
+            const uint64_t t0 = globaltimer_ns();
+            while (*v_tiles < 8 * t - kKLeadChunks) {
+              if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
+                *abort_flag = 1;
+                ok = false;
+                break;
+              }
+              __nanosleep(64);
+            }
+            __syncwarp();
+            if (!(ok = __all_sync(0xffffffffu, ok))) break;
+          }
           if (!emit_k(v, i, pages)) break;
-        } else if (!emit_v(v, i, pages)) {
-          break;
+        } else {
+          if (!emit_v(v, i, pages, t)) break;
+          __syncwarp();
+          if (lane == 0) *v_tiles = 8 * (t + 1);   // a short tile counts as 8 chunks
         }
       }
     }
