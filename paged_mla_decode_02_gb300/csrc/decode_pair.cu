@@ -105,10 +105,11 @@ constexpr float kLn2 = 0.6931471805599453f;
 // lone token's p exact)
 constexpr float kRescaleThreshold = 8.0f, kRescaleThresholdFp8 = 3.5f;
 constexpr float kPOffsetFp8 = 5.0f, kPScaleFp8 = 32.0f;   // 2^kPOffsetFp8
-// The K copies of tile t wait until the V copies have reached chunk
+// bf16: the K copies of tile t wait until the V copies have reached chunk
 // 8 t - kKLeadChunks (8 chunks per tile): V re-reads the K rows from L2, and
 // a K stream far ahead of V pushes them out first (measured on long
-// requests at a high DRAM rate).
+// requests at a high DRAM rate; the e4m3 path, with half the bytes in
+// flight, gains nothing from the cap and pays for the count).
 constexpr int kKLeadChunks = 12;
 
 // shared memory (offsets from the 1024-byte aligned base)
@@ -402,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int slot;
         if (!(ok = next_slot(slot))) return false;
         const uint32_t full = map_to_rank(bar(base, kVFull0 + slot), lead);
-        if (lane == 0 && c > 0) *v_tiles = 8 * vt + c;   // chunks before this one issued
+        if (!kFp8 && lane == 0 && c > 0) *v_tiles = 8 * vt + c;   // chunks before this one issued
         if (stalled()) continue;
         // one copy: vbox rows of kVPanels panels (128-byte rows), this CTA's
         // 256 dims
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (is_k) {
           if (i == 0 && !emit_q(v)) break;
           // at most kKLeadChunks V chunks ahead of the V copies (bounded wait)
-          if (8 * t > kKLeadChunks) {
+          if (!kFp8 && 8 * t > kKLeadChunks) {
             const uint64_t t0 = globaltimer_ns();
             while (*v_tiles < 8 * t - kKLeadChunks) {
               if (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
           if (!emit_v(v, i, pages, t)) break;
           __syncwarp();
-          if (lane == 0) *v_tiles = 8 * (t + 1);   // a short tile counts as 8 chunks
+          if (!kFp8 && lane == 0) *v_tiles = 8 * (t + 1);   // a short tile counts as 8 chunks
         }
       }
     }
