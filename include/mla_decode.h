@@ -64,7 +64,7 @@ typedef enum {
   MLA_KERNEL_TCGEN05 = 1,     /* one-CTA tcgen05 / TMEM kernel (bf16 and fp8 caches) */
   MLA_KERNEL_MMA_SYNC = 2,    /* warp-level mma.sync kernel (legacy tensor path, for comparison) */
   MLA_KERNEL_PAIR = 3         /* tcgen05 kernel whose MMAs span a CTA pair (cta_group::2); bf16
-                                 caches, and fp8 caches with page_size >= 32 (f16 MMAs) */
+                                 caches, and fp8 caches with page_size >= 32 (e4m3 MMAs) */
 } mla_kernel_t;
 
 /* Plan statistics, filled by mla_plan_info. */
@@ -161,9 +161,13 @@ mla_status_t mla_decode_plan_multi(mla_plan_t plan, const int32_t* kv_indptr_hos
  * in bf16), and on the mma.sync kernel with any page size; with the tcgen05
  * kernel and 16-token pages the call returns MLA_ERR_UNSUPPORTED.  The
  * CTA-pair kernel (and so MLA_KERNEL_DEFAULT) takes fp8 caches with 32- or
- * 64-token pages: each copied tile is expanded to f16 in shared memory and
- * the query converted to f16 under a power-of-two scale per head row; with
- * 16-token pages it returns MLA_ERR_UNSUPPORTED.
+ * 64-token pages: e4m3 MMAs (kind::f8f6f4) read the copied codes as they
+ * are, against the query and the probabilities P each split into two e4m3
+ * terms (hi = e4m3(x), lo = e4m3(x - hi)); each query row is first scaled
+ * by a power of two so that its largest magnitude lies in [2^7, 2^8), which
+ * makes hi + lo the bf16 query exactly for magnitudes from 2^-2 up (after
+ * the scaling) and within 2^-10 below.  With 16-token pages it returns
+ * MLA_ERR_UNSUPPORTED.
  *   out       [batch, num_heads, 512]   out_dtype (BF16 or FP32)
  *   lse       [batch, num_heads]        fp32, natural log
  * Launches the decode kernel; with the tcgen05 kernel that is the only launch

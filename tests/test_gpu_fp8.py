@@ -1,8 +1,8 @@
 """fp8 (e4m3) caches on every kernel against the oracle on the dequantised
-values: the CTA-pair kernel expands each copied tile to f16 in shared memory
-and multiplies in f16 (the query converted once per unit under a
-power-of-two row scale, P rounded to f16), the one-CTA tcgen05 kernel expands
-to bf16 (every e4m3 value is exact in both), both fold kv_scale into the
+values: the CTA-pair kernel multiplies the copied codes as they are with
+e4m3 MMAs, against the query (scaled per row by a power of two) and P each
+split into two e4m3 terms; the one-CTA tcgen05 kernel expands each copied
+tile to bf16 (every e4m3 value is exact in it); both fold kv_scale into the
 scores and the output; the mma.sync kernel converts while staging."""
 from __future__ import annotations
 
@@ -58,9 +58,10 @@ def test_fp8_tensor_core_kernels_reject_16_token_pages(kernel):
 
 def test_fp8_pair_query_row_scales():
     """Query rows of very different magnitudes (2^-20 .. 2^4 times N(0,1), one
-    row of zeros): each row is converted to f16 under its own power-of-two
-    scale, so every row keeps its precision (unscaled, f16 would flush the
-    small rows' values below 2^-24 to zero)."""
+    row of zeros): each row is scaled by its own power of two (largest
+    magnitude into [2^7, 2^8)) before its split into two e4m3 terms, so every
+    row keeps its precision (unscaled, e4m3 would flush the small rows'
+    values below 2^-10 to zero)."""
     x = I.make_inputs("f8q", [700, 130], 128, 64, seed=43, kv_dtype="fp8_e4m3")
     rng = np.random.Generator(np.random.PCG64(7))
     exps = rng.integers(-20, 5, size=(x.batch, x.num_heads)).astype(np.float64)
