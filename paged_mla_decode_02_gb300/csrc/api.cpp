@@ -235,9 +235,10 @@ mla_status_t mla_plan_create(int max_batch, int num_heads, int kernel, mla_plan_
   if (!p) return MLA_ERR_CUDA;
   p->max_batch = max_batch;
   p->num_heads = num_heads;
-  // DEFAULT: the CTA-pair kernel for bf16 caches; fp8 caches run on the
+  // DEFAULT: the CTA-pair kernel for bf16 caches and for fp8 caches with
+  // pages of 32 or 64 tokens; an fp8 cache with 16-token pages goes to the
   // one-CTA tcgen05 kernel over the same partition (its 256-token unit
-  // boundaries are also 128-token tile boundaries)
+  // boundaries are also 128-token tile boundaries), which rejects it
   p->kernel_requested = kernel;
   p->kernel = kernel == MLA_KERNEL_DEFAULT ? MLA_KERNEL_PAIR : kernel;
   p->tile_tokens = p->kernel == MLA_KERNEL_MMA_SYNC ? kTileMma : p->kernel == MLA_KERNEL_PAIR ? kTilePair : kTileTc;
