@@ -78,6 +78,13 @@ template <int K, int N, bool kWRowsN, int kOutW>
 __global__ void __launch_bounds__(kProjThreads, 1)
     proj_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
                 __nv_bfloat16* __restrict__ c_out, int batch, int heads, int n_items, int a_rows) {
+  // launched as a programmatic dependent of the previous kernel on the
+  // stream: nothing is read before that kernel has completed and its writes
+  // are visible (a no-op in a plain launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next kernel on the stream may be scheduled now; it waits for this
+  // one to complete before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int KC = K < kKC ? K : kKC;
   constexpr int kChunks = K / KC;                   // pipeline stages per item
   constexpr int kSlices = kOutW / N;                // column slices per head
@@ -259,8 +266,19 @@ cudaError_t launch_proj(const CUtensorMap& a, const CUtensorMap& w, __nv_bfloat1
     return e;
   const int items = heads * (kOutW / N) * ((batch + kRows - 1) / kRows);
   const int grid = items < sms ? items : sms;
-  kernel<<<grid, kProjThreads, smem, s>>>(a, w, dst, batch, heads, items, batch < kRows ? batch : kRows);
-  return cudaGetLastError();
+  // a programmatic dependent launch: the grid is scheduled while the previous
+  // kernel drains, and waits for it at its first instruction
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kProjThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, a, w, dst, batch, heads, items, batch < kRows ? batch : kRows);
 }
 
 mla_status_t finish(cudaError_t e, int check_status, cudaStream_t s) {

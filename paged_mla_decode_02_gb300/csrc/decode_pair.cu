@@ -232,6 +232,13 @@ __device__ __forceinline__ float split_e4m3x2(float x0, float x1, uint32_t& hi, 
 template <bool kOutF32, bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_pair_kernel(const DecodeArgs a, const __grid_constant__ PairMaps maps) {
+  // launched as a programmatic dependent of the previous kernel on the
+  // stream: nothing is read before that kernel has completed and its writes
+  // are visible (a no-op in a plain launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next kernel on the stream may be scheduled now; it waits for this
+  // one to complete before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ unsigned char smem_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -1016,9 +1023,14 @@ cudaError_t launch_decode_pair(const DecodeArgs& a, const PairMaps& maps, bool o
   cudaError_t e = kv_fp8 ? (out_f32 ? set_pair_attributes<true, true>() : set_pair_attributes<false, true>())
                          : (out_f32 ? set_pair_attributes<true, false>() : set_pair_attributes<false, false>());
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config(a.n_workers, attr);
   cfg.stream = s;
+  // a programmatic dependent launch: the grid is scheduled while the previous
+  // kernel drains, and waits for it at its first instruction
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 2;
   if (kv_fp8)
     return out_f32 ? cudaLaunchKernelEx(&cfg, decode_pair_kernel<true, true>, a, maps)
                    : cudaLaunchKernelEx(&cfg, decode_pair_kernel<false, true>, a, maps);

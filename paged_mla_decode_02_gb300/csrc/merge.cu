@@ -52,6 +52,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const MergeArgs a)
   // launched as a programmatic dependent of the decode kernel: wait for it
   // (a no-op in a plain launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next kernel on the stream may be scheduled now; it waits for this
+  // one to complete before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int H = a.num_heads;
   const int C = merge_chunk(H);
   const int nchunk = kDCkv / C;
@@ -198,6 +201,9 @@ constexpr int kFlatThreads = 256, kFlatBlocksPerSm = 4, kFlatAhead = 4;
 template <bool kOutF32>
 __global__ void __launch_bounds__(kFlatThreads, kFlatBlocksPerSm) merge_flat_kernel(const MergeArgs a) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next kernel on the stream may be scheduled now; it waits for this
+  // one to complete before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int H = a.num_heads;
   const long long total = static_cast<long long>(a.params->n_merge) * (kDCkv / 8) * H * 2;
   const long long stride = static_cast<long long>(gridDim.x) * kFlatThreads;
