@@ -176,8 +176,12 @@ mla_status_t mla_decode_plan_multi(mla_plan_t plan, const int32_t* kv_indptr_hos
  * kernel), with the CTA-pair and mma.sync kernels a merge kernel follows.  The combination
  * order is fixed, so repeated runs give bit-identical results.
  * No allocation, no synchronisation, no host reads: capturable in a
- * CUDA graph (the graph keeps the pointers; re-planning with the same plan
- * between replays is allowed).  A page id outside [0, num_pages) found by the
+ * CUDA graph.  The graph keeps the pointers and the extent of the query and
+ * output arrays of the captured call (the batch planned then, times its
+ * heads): re-planning with the same plan between replays is allowed (new
+ * lengths, page table and split) for a batch no larger than the captured
+ * one; a replay after a re-plan to a larger batch would read the query rows
+ * past the captured extent as zeros.  A page id outside [0, num_pages) found by the
  * kernel is recorded and reported by mla_plan_check_status; that page is read
  * as zeros.
  */

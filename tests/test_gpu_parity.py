@@ -205,6 +205,46 @@ def test_nondefault_stream_and_graph_replay(kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
+def test_graph_replay_after_replan_to_a_smaller_batch(kernel):
+    """A run captured at batch 3 replays after the same plan is re-planned
+    for batch 2 (new lengths, pages and cache contents in the same buffers):
+    the captured query and output extents cover the smaller batch."""
+    x = I.make_inputs("g3", [700, 64, 1500], 128, 64, seed=31, pool_pages=48)
+    x2 = I.make_inputs("g2", [1300, 257], 128, 64, seed=32, pool_pages=48)
+    d, d2 = to_device(x), to_device(x2)
+    idx = torch.zeros(48, dtype=torch.int32, device="cuda")
+    idx[: len(x.kv_indices)].copy_(d["kv_indices"])
+    qn, qp, ckv, kpe = (d[k].clone() for k in ("q_nope", "q_pe", "ckv", "kpe"))
+    out = torch.empty((x.batch, x.num_heads, 512), dtype=torch.float32, device="cuda")
+    lse = torch.empty((x.batch, x.num_heads), dtype=torch.float32, device="cuda")
+    dec = mla.MLADecoder(x.batch, x.num_heads, kernel)
+    dec.plan(x.kv_indptr, idx, x.kv_len, x.page_size, x.sm_scale)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        dec.run(qn, qp, ckv, kpe, out, lse)
+    g.replay()
+    torch.cuda.synchronize()
+    dec.check_status()
+    ref_out, ref_lse = O.mla_decode_inputs(x)
+    assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse, "batch 3")
+    qn[:2].copy_(d2["q_nope"])
+    qp[:2].copy_(d2["q_pe"])
+    ckv.copy_(d2["ckv"])
+    kpe.copy_(d2["kpe"])
+    idx.zero_()
+    idx[: len(x2.kv_indices)].copy_(d2["kv_indices"])
+    dec.plan(x2.kv_indptr, idx, x2.kv_len, x2.page_size, x2.sm_scale)
+    g.replay()
+    torch.cuda.synchronize()
+    dec.check_status()
+    r2o, r2l = O.mla_decode_inputs(x2)
+    assert_parity(out[:2].double().cpu().numpy(), lse[:2].double().cpu().numpy(), r2o, r2l,
+                  "re-planned to batch 2")
+    dec.close()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 def test_run_host_entry_point(kernel):
     x = I.make_inputs("host", [100, 3000], 128, 64, seed=6)
     d = to_device(x)
