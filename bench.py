@@ -1,11 +1,13 @@
 """Benchmark of the paged MLA decode path on one GB300 (or N replicas).
 
-One step = one ``mla_decode_run`` (the tcgen05 decode kernel, split
-requests merged inside it) over one batch of the workload, inputs resident
-in HBM.  Default workload: DeepSeek-V3-shaped decode, batch 64, 128 heads,
-kv_len 4096 per request, page size 64, bf16 cache, pages randomly permuted
-over the pool.  Other modes (``--config``): deepseek_mtp2 (two query tokens
-per request), deepseek_absorbed (W_UK absorb + decode + W_UV projection),
+One step = one ``mla_decode_run`` (the CTA-pair decode kernel, then the
+merge kernel for split requests) over one batch of the workload, inputs
+resident in HBM.  Default workload: DeepSeek-V3-shaped decode, batch 64, 128
+heads, kv_len 4096 per request, page size 64, bf16 cache, pages randomly
+permuted over the pool.  Other modes (``--config``): ragged, long_b1,
+long_b4, fp8, deepseek_mtp2 (two query tokens per request), long_b4_mtp4
+(four query tokens per request of 16 heads, packed into one request's
+rows), deepseek_absorbed (W_UK absorb + decode + W_UV projection),
 deepseek_cascade (shared prefix + own suffix + state merge).
 
 Prints one JSON line.  ``value`` is microseconds per batch (device time of

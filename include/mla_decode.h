@@ -135,11 +135,18 @@ mla_status_t mla_decode_plan(mla_plan_t plan, const int32_t* kv_indptr_host,
  *   mla_decode_run then takes
  *     q_nope [batch, q_len, num_heads, 512],  q_pe [batch, q_len, num_heads, 64],
  *     out    [batch, q_len, num_heads, 512],  lse  [batch, q_len, num_heads].
- *   Each query token is planned as its own request over a prefix of its
- *   request's pages, so a step reads each request's cache q_len times.
- *   Consecutive queries of a request sit next to each other in the work
- *   list, so those reads are mostly served by L2.
- *   q_len = 1 plans exactly what mla_decode_plan plans.
+ *   With the CTA-pair kernel (MLA_KERNEL_DEFAULT or MLA_KERNEL_PAIR) and
+ *   q_len * num_heads <= 128, the q_len query tokens of a request share
+ *   the rows of one request (row j * num_heads + h of the [batch, q_len *
+ *   num_heads] view of the query and output arrays, each row masked to its
+ *   own prefix), so a step reads each request's cache once;
+ *   mla_plan_info then reports batch requests.  Otherwise each query token
+ *   is planned as its own request over a prefix of its request's pages
+ *   (mla_plan_info reports batch * q_len), so a step reads each request's
+ *   cache q_len times; consecutive queries of a request sit next to each
+ *   other in the work list, so those reads are mostly served by L2.
+ *   q_len = 1 plans exactly what mla_decode_plan plans.  A graph captured
+ *   from a run of such a plan replays re-plans with the same q_len.
  */
 mla_status_t mla_decode_plan_multi(mla_plan_t plan, const int32_t* kv_indptr_host,
                                    const int32_t* kv_indices_dev, const int32_t* kv_len_host,

@@ -34,6 +34,7 @@ struct mla_plan_s {
   int units_cap = 0;
   int slots_cap = 0;
   int merge_cap = 0;
+  size_t part_rows_cap = 0;          // rows (head x share) of the partial-share buffers
 
   // One device blob: PlanDev | units | worker_ptr | merge (16-byte aligned parts).
   void* d_blob = nullptr;
@@ -280,8 +281,14 @@ mla_status_t mla_plan_create(int max_batch, int num_heads, int kernel, mla_plan_
   p->off_wptr = align16(p->off_units + sizeof(WorkUnit) * p->units_cap);
   p->off_merge = align16(p->off_wptr + sizeof(int32_t) * (p->n_workers + 1));
   p->blob_bytes = align16(p->off_merge + sizeof(MergeEntry) * p->merge_cap);
-  const size_t o_bytes = sizeof(float) * static_cast<size_t>(p->slots_cap) * num_heads * kDCkv;
-  const size_t l_bytes = sizeof(float) * static_cast<size_t>(p->slots_cap) * kLsePartCopies * num_heads;
+  // Partial shares: a row per (share, head).  A CTA-pair plan may pack up
+  // to 128 rows per request (several query tokens), whose split units take
+  // at most n_workers x 128 + max_batch x num_heads rows in all.
+  p->part_rows_cap = static_cast<size_t>(p->slots_cap) * num_heads;
+  if (p->kernel == MLA_KERNEL_PAIR)
+    p->part_rows_cap = static_cast<size_t>(p->n_workers) * kMaxHeads + static_cast<size_t>(max_batch) * num_heads;
+  const size_t o_bytes = sizeof(float) * p->part_rows_cap * kDCkv;
+  const size_t l_bytes = sizeof(float) * p->part_rows_cap * kLsePartCopies;
   const size_t c_bytes = sizeof(int32_t) * static_cast<size_t>(max_batch) * 8;
   if ((e = cudaMalloc(&p->d_blob, p->blob_bytes)) != cudaSuccess ||
       (e = cudaMallocHost(&p->h_blob, p->blob_bytes)) != cudaSuccess ||
@@ -315,13 +322,17 @@ namespace {
 
 // Partition and upload for n_req requests given by the position of their
 // first page id in kv_indices (page_base) and their token counts (the
-// caller validated both).
+// caller validated both).  num_heads is the rows per request the kernels
+// see: the plan's heads, or q_len x heads when q_len > 1 query tokens of a
+// request share its rows (heads_per_token = the plan's heads); each partial
+// share of a request takes that many rows of the share buffers.
 mla_status_t plan_requests(mla_plan_t plan, const int32_t* page_base, const int32_t* len, int n_req,
                            const int32_t* kv_indices_dev, int num_heads, int page_size,
-                           float sm_scale, void* stream) {
+                           float sm_scale, void* stream, int q_len = 1, int heads_per_token = 0) {
   Partition part;
   partition_batch(page_base, len, n_req, plan->n_workers, plan->tile_tokens, &part);
   if (static_cast<int>(part.units.size()) > plan->units_cap || part.n_slots > plan->slots_cap ||
+      static_cast<size_t>(part.n_slots) * num_heads > plan->part_rows_cap ||
       static_cast<int>(part.merge.size()) > plan->merge_cap)
     return fail(plan, MLA_ERR_CAPACITY, "partition exceeds plan buffers");
 
@@ -339,6 +350,8 @@ mla_status_t plan_requests(mla_plan_t plan, const int32_t* page_base, const int3
   prm.page_size = page_size;
   prm.sm_scale = sm_scale;
   prm.n_slots = part.n_slots;
+  prm.q_len = q_len;
+  prm.heads_per_token = heads_per_token > 0 ? heads_per_token : num_heads;
   char* h = static_cast<char*>(plan->h_blob);
   std::memcpy(h, &prm, sizeof(prm));
   if (!part.units.empty())
@@ -413,9 +426,21 @@ mla_status_t mla_decode_plan_multi(mla_plan_t plan, const int32_t* kv_indptr_hos
     if (kv_len_host[b] < q_len)
       return fail(plan, MLA_ERR_INVALID_ARG,
                   "every request must hold its q_len query tokens in the cache (kv_len >= q_len)");
-  // Query j of request b sees the first kv_len - q_len + 1 + j tokens: it is
-  // planned as its own request over a prefix of b's pages, at row b * q_len + j
-  // of the [batch * q_len, heads] query and output arrays.
+  // Query j of request b sees the first kv_len - q_len + 1 + j tokens.  On
+  // the CTA-pair kernel, when q_len x heads <= 128, the q_len query tokens of
+  // a request share its MMA rows (row j * heads + h of the [batch, q_len *
+  // heads] view of the query and output arrays, each row masked to its own
+  // prefix), so its pages are read once (the plan's share buffers hold any
+  // such partition; should one not fit, the form below is used).
+  if (plan->kernel == MLA_KERNEL_PAIR && q_len > 1 && q_len * num_heads <= kMaxHeads) {
+    st = plan_requests(plan, kv_indptr_host, kv_len_host, batch, kv_indices_dev, q_len * num_heads,
+                       page_size, sm_scale, stream, q_len, num_heads);
+    if (st != MLA_ERR_CAPACITY) return st;
+    plan->last_error.clear();
+  }
+  // Otherwise query j of request b is planned as its own request over a
+  // prefix of b's pages, at row b * q_len + j of the [batch * q_len, heads]
+  // query and output arrays.
   std::vector<int32_t> base(static_cast<size_t>(batch) * q_len), len(base.size());
   for (int b = 0; b < batch; ++b)
     for (int j = 0; j < q_len; ++j) {
@@ -469,7 +494,7 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
   a.counters = plan->d_counters;
   a.err = plan->d_err;
   a.num_pages = num_pages;
-  a.num_heads = plan->num_heads;
+  a.num_heads = plan->params.num_heads;   // rows per request (q_len x heads when packed)
   a.kv_scale = fp8 ? kv_scale : 1.f;   // the dequantisation scale of fp8 codes only
   a.units_cap = plan->units_cap;
   a.n_workers = plan->n_workers;
@@ -489,7 +514,7 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
       return fail(plan, MLA_ERR_UNSUPPORTED,
                   "the CTA-pair kernel takes fp8 caches with page_size >= 32; use MLA_KERNEL_MMA_SYNC");
     PairMaps maps;
-    if (!encode_pair_maps(&maps, q_nope, q_pe, ckv_cache, kpe_cache, plan->params.batch, plan->num_heads,
+    if (!encode_pair_maps(&maps, q_nope, q_pe, ckv_cache, kpe_cache, plan->params.batch, plan->params.num_heads,
                           plan->params.page_size, num_pages, fp8))
       return fail(plan, MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     e = launch_decode_pair(a, maps, out_f32, fp8, s);
@@ -498,7 +523,7 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
       return fail(plan, MLA_ERR_UNSUPPORTED,
                   "the tcgen05 kernel takes fp8 caches with page_size >= 32; use MLA_KERNEL_MMA_SYNC");
     TcMaps maps;
-    if (!encode_tc_maps(&maps, q_nope, ckv_cache, kpe_cache, plan->params.batch, plan->num_heads,
+    if (!encode_tc_maps(&maps, q_nope, ckv_cache, kpe_cache, plan->params.batch, plan->params.num_heads,
                         plan->params.page_size, num_pages, fp8))
       return fail(plan, MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     e = launch_decode_tc(a, maps, out_f32, fp8, s);
@@ -517,7 +542,7 @@ mla_status_t mla_decode_run(mla_plan_t plan, const void* q_nope, const void* q_p
   m.lse_part = plan->d_lse_part;
   m.out = out;
   m.lse = lse;
-  m.num_heads = plan->num_heads;
+  m.num_heads = plan->params.num_heads;
   m.merge_cap = plan->merge_cap;
   e = launch_merge(m, out_f32, s);
   if (e != cudaSuccess) return cuda_fail(plan, e, "merge kernel launch");
@@ -534,7 +559,7 @@ mla_status_t mla_decode_run_host(mla_plan_t plan, const void* q_nope_host, const
     return fail(plan, MLA_ERR_INVALID_ARG, "NULL host pointer");
   if (out_dtype != MLA_DTYPE_BF16 && out_dtype != MLA_DTYPE_FP32)
     return fail(plan, MLA_ERR_UNSUPPORTED, "out_dtype must be BF16 or FP32");
-  const size_t rows = static_cast<size_t>(plan->params.batch) * plan->num_heads;
+  const size_t rows = static_cast<size_t>(plan->params.batch) * plan->params.num_heads;
   const size_t qn = rows * kDCkv * 2, qp = rows * kDKpe * 2;
   const size_t ob = rows * kDCkv * (out_dtype == MLA_DTYPE_FP32 ? 4 : 2), lb = rows * 4;
   cudaError_t e;
@@ -633,8 +658,8 @@ mla_status_t mla_plan_info(mla_plan_t plan, mla_plan_info_t* info) {
   info->kernel = plan->kernel;
   info->tile_tokens = plan->tile_tokens;
   info->workspace_bytes = static_cast<int64_t>(plan->blob_bytes) +
-                          static_cast<int64_t>(sizeof(float)) * plan->slots_cap *
-                              plan->num_heads * (kDCkv + 1);
+                          static_cast<int64_t>(sizeof(float)) * static_cast<int64_t>(plan->part_rows_cap) *
+                              (kDCkv + kLsePartCopies);
   return MLA_OK;
 }
 

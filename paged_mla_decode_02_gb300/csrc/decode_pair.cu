@@ -641,6 +641,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int part = 2 * tq + ch;            // which of the head's four threads this is
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(q * 32) << 16);
     const float c = prm.sm_scale * a.kv_scale * kLog2e;
+    // several query tokens packed into the rows: this row's token j sees all
+    // but the request's last q_len - 1 - j tokens (0 with one token per row)
+    const int row_hide = prm.q_len > 1 && prm.heads_per_token > 0 && h < H
+                             ? prm.q_len - 1 - h / prm.heads_per_token
+                             : 0;
     float* red = reinterpret_cast<float*>(sm + kOffRed);
     float2* sums = reinterpret_cast<float2*>(sm + kOffSum);
     bool ok = true;
@@ -783,7 +788,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(lane_addr + col, v0);
           tmem_ld32(lane_addr + col + 32, v1);
           tmem_ld_wait();
-          const int nvalid = u.tok_end - (u.tok_begin + i * kT + kHalfT * tq + 64 * ch);
+          const int row_end = min(u.tok_end, u.kv_len - row_hide);
+          const int nvalid = row_end - (u.tok_begin + i * kT + kHalfT * tq + 64 * ch);
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             y[j] = j < nvalid ? __uint_as_float(v0[j]) * cq : -INFINITY;
@@ -812,16 +818,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ---- p = 2^(y - reference) rounded to bf16, or 2^(y - reference)
         // * 2^5 as e4m3 hi + lo terms (this thread's 64 tokens: hi codes in
-        // words 0..15, lo codes in words 16..31); row sums ----
+        // words 0..15, lo codes in words 16..31); row sums.  A packed row
+        // with no visible token so far keeps the reference -inf and p = 0
+        // (its y are all -inf; the exponent then uses 0) ----
         uint32_t pk[32];
         {
+          const float rexp = ref == -INFINITY ? 0.f : ref;
           float sx = 0.f, sr = 0.f;
           if constexpr (kFp8) {
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
-              const float p0 = fast_exp2(y[4 * m] - ref) * kPScaleFp8, p1 = fast_exp2(y[4 * m + 1] - ref) * kPScaleFp8;
-              const float p2 = fast_exp2(y[4 * m + 2] - ref) * kPScaleFp8;
-              const float p3 = fast_exp2(y[4 * m + 3] - ref) * kPScaleFp8;
+              const float p0 = fast_exp2(y[4 * m] - rexp) * kPScaleFp8, p1 = fast_exp2(y[4 * m + 1] - rexp) * kPScaleFp8;
+              const float p2 = fast_exp2(y[4 * m + 2] - rexp) * kPScaleFp8;
+              const float p3 = fast_exp2(y[4 * m + 3] - rexp) * kPScaleFp8;
               sx += (p0 + p1) + (p2 + p3);
               uint32_t h01, l01, h23, l23;
               sr += split_e4m3x2(p0, p1, h01, l01) + split_e4m3x2(p2, p3, h23, l23);
@@ -831,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              const float p0 = fast_exp2(y[2 * j] - ref), p1 = fast_exp2(y[2 * j + 1] - ref);
+              const float p0 = fast_exp2(y[2 * j] - rexp), p1 = fast_exp2(y[2 * j + 1] - rexp);
               sx += p0 + p1;
               const __nv_bfloat162 b2 = __floats2bfloat162_rn(p0, p1);
               const uint32_t w = *reinterpret_cast<const uint32_t*>(&b2);
@@ -897,7 +906,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // (e4m3 P carries the factor 2^5, in both sums)
         const float ls = (ref - (kFp8 ? kPOffsetFp8 : 0.f) + log2f(sx)) * kLn2;
-        const float inv = a.kv_scale / sr;
+        const float inv = sr > 0.f ? a.kv_scale / sr : 0.f;   // a row with no visible token: out 0
         const bool split = u.out_slot >= 0;
         if (part == 0 && h < H) {
           if (split)

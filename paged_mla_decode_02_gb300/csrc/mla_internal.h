@@ -51,8 +51,15 @@ struct PlanDev {
   int32_t page_size;
   float sm_scale;
   int32_t n_slots;
+  // Several query tokens of a request packed into the rows of one request
+  // (CTA-pair kernel, q_len * heads_per_token <= 128): row h is query token
+  // h / heads_per_token of its request and sees the request's first
+  // kv_len - (q_len - 1 - h / heads_per_token) tokens.  q_len <= 1: one
+  // query token per request (every row sees kv_len tokens).
+  int32_t q_len;
+  int32_t heads_per_token;
 };
-static_assert(sizeof(PlanDev) == 32, "PlanDev layout");
+static_assert(sizeof(PlanDev) == 40, "PlanDev layout");
 
 // Device error codes (same values as mla_status_t).
 constexpr int kErrTimeout = 5;

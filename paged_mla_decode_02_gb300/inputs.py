@@ -217,6 +217,7 @@ CONFIGS = {
     "ragged": dict(kv_len=_ragged_lengths, num_heads=128, page_size=16),
     "long_b1": dict(kv_len=[131072], num_heads=16, page_size=64, key_scale=3.0),
     "long_b4": dict(kv_len=[131072] * 4, num_heads=16, page_size=64, key_scale=3.0),
+    "long_b4_mtp4": dict(kv_len=[131072] * 4, num_heads=16, page_size=64, key_scale=3.0, q_len=4),
     "fp8": dict(kv_len=_lognormal_lengths, num_heads=128, page_size=64,
                 kv_dtype="fp8_e4m3", kv_scale=1.0),
 }
@@ -228,6 +229,7 @@ CONFIG_DESCRIPTIONS = {
     "ragged": "B128 H128 P16 L~U[1,8192] bf16",
     "long_b1": "B1 H16 P64 L131072 bf16 keys x3",
     "long_b4": "B4 H16 P64 L131072 bf16 keys x3",
+    "long_b4_mtp4": "B4 H16 P64 L131072 bf16 keys x3, 4 query tokens per request",
     "fp8": "B256 H128 P64 L~lognormal(2048,0.8)<=16384 fp8-e4m3",
 }
 

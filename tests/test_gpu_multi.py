@@ -85,3 +85,68 @@ def test_multi_token_plan_rejects_bad_arguments(bad, status):
         assert ei.value.status == status
     finally:
         dec.close()
+
+
+# ---------------------------------------------------------------------------
+# the CTA-pair kernel packs the query tokens of a request into its MMA rows
+# (q_len x heads <= 128): one plan request per request, each row masked to
+# its own prefix
+# ---------------------------------------------------------------------------
+
+def _run_multi_dec(x, d, kernel, max_batch=None):
+    dec = mla.MLADecoder(max_batch or x.batch * x.q_len, x.num_heads, kernel)
+    dec.plan(x.kv_indptr, d["kv_indices"], x.kv_len, x.page_size, x.sm_scale, q_len=x.q_len)
+    out, lse = dec.run(d["q_nope"], d["q_pe"], d["ckv"], d["kpe"], kv_scale=x.kv_scale,
+                       out_dtype=torch.float32)
+    dec.check_status()
+    return dec, out, lse
+
+
+def _oracle_x(x):
+    return O.mla_decode_multi(x.q_nope, x.q_pe, x.ckv, x.kpe, x.kv_indptr, x.kv_indices,
+                              x.kv_len, x.page_size, x.sm_scale, x.kv_dtype, x.kv_scale)
+
+
+@pytest.mark.parametrize("lens, heads, P, Q, kv_dtype", [
+    ([20000, 4, 777], 16, 64, 4, "bf16"),     # a request split over many workers; one of exactly Q tokens
+    ([40000], 16, 64, 8, "bf16"),             # 128 rows, one request over every worker
+    ([300, 257, 9], 32, 32, 3, "bf16"),       # 96 rows: the odd CTA's last 32 rows unused
+    ([5000, 700, 2], 16, 64, 2, "fp8_e4m3"),  # e4m3 cache (hi + lo query and P)
+])
+def test_packed_query_tokens_match_oracle(lens, heads, P, Q, kv_dtype):
+    x = I.make_inputs("mqp", lens, heads, P, seed=47, q_len=Q, poison=True, slack_pages=3,
+                      kv_dtype=kv_dtype)
+    d = to_device(x)
+    dec, out, lse = _run_multi_dec(x, d, "pair")
+    try:
+        assert dec.info()["batch"] == x.batch      # one plan request per request: packed
+        ref_out, ref_lse = _oracle_x(x)
+        assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
+                      f"packed Q={Q} H={heads} {lens} {kv_dtype}")
+        # split shares are combined in slot order: repeated runs are bit-identical
+        out2, lse2 = dec.run(d["q_nope"], d["q_pe"], d["ckv"], d["kpe"], kv_scale=x.kv_scale,
+                             out_dtype=torch.float32)
+        dec.check_status()
+        assert torch.equal(out, out2) and torch.equal(lse, lse2)
+    finally:
+        dec.close()
+
+
+@pytest.mark.parametrize("kernel, heads, Q, packed", [
+    ("pair", 16, 8, True),
+    ("pair", 64, 2, True),
+    ("pair", 128, 2, False),      # 256 rows do not fit one pair MMA: one plan request per token
+    ("tcgen05", 16, 4, False),
+    ("mma_sync", 16, 4, False),
+])
+def test_which_plans_pack(kernel, heads, Q, packed):
+    x = I.make_inputs("mqw", [600, 64], heads, 64, seed=3, q_len=Q)
+    d = to_device(x)
+    dec, out, lse = _run_multi_dec(x, d, kernel)
+    try:
+        assert dec.info()["batch"] == (x.batch if packed else x.batch * Q)
+        ref_out, ref_lse = _oracle_x(x)
+        assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
+                      f"{kernel} H={heads} Q={Q}")
+    finally:
+        dec.close()
