@@ -150,3 +150,18 @@ def test_which_plans_pack(kernel, heads, Q, packed):
                       f"{kernel} H={heads} Q={Q}")
     finally:
         dec.close()
+
+
+def test_packed_full_size_long_b4_mtp4():
+    """The bench's long_b4_mtp4 workload (4 x 131072 tokens, 16 heads, 4 query
+    tokens per request, packed) against the oracle, every request."""
+    x = I.make_config("long_b4_mtp4")
+    d = to_device(x)
+    dec, out, lse = _run_multi_dec(x, d, "default")
+    try:
+        assert dec.info()["batch"] == x.batch
+        ref_out, ref_lse = _oracle_x(x)
+        assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse,
+                      "long_b4_mtp4")
+    finally:
+        dec.close()
