@@ -359,6 +359,9 @@ const char* mla_plan_last_error(mla_plan_t plan);
  *          (n_slots = 0 for an empty request: out = 0, lse = -inf)
  *   counts [3] int32: {num_units, num_partial_slots, num_merge}
  * Returns MLA_ERR_CAPACITY when units_cap or merge_cap is too small.
+ * This is the default-cost partition.  A CTA-pair plan may instead keep a
+ * partition with fewer split requests when its estimated step (slowest
+ * worker plus the merge pass over the split shares) is shorter.
  */
 mla_status_t mla_plan_partition_host(const int32_t* kv_indptr_host, const int32_t* kv_len_host,
                                      int batch, int head_dim_ckv, int head_dim_kpe,

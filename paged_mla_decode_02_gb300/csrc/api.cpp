@@ -330,7 +330,10 @@ mla_status_t plan_requests(mla_plan_t plan, const int32_t* page_base, const int3
                            const int32_t* kv_indices_dev, int num_heads, int page_size,
                            float sm_scale, void* stream, int q_len = 1, int heads_per_token = 0) {
   Partition part;
-  partition_batch(page_base, len, n_req, plan->n_workers, plan->tile_tokens, &part);
+  if (plan->kernel == MLA_KERNEL_PAIR)
+    partition_batch_pair(page_base, len, n_req, plan->n_workers, num_heads, &part);
+  else
+    partition_batch(page_base, len, n_req, plan->n_workers, plan->tile_tokens, &part);
   if (static_cast<int>(part.units.size()) > plan->units_cap || part.n_slots > plan->slots_cap ||
       static_cast<size_t>(part.n_slots) * num_heads > plan->part_rows_cap ||
       static_cast<int>(part.merge.size()) > plan->merge_cap)

@@ -88,8 +88,8 @@ constexpr int tiles_of(int32_t len, int tile_tokens) { return (len + tile_tokens
 // `units` is non-null.  Returns the number of units, or -1 when the batch
 // needs more than n_workers workers at this budget.
 int fill_workers(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int n_workers,
-                 int tile_tokens, long long budget, WorkUnit* units, int32_t* worker_ptr) {
-  const PlanCosts c = plan_costs(tile_tokens);
+                 int tile_tokens, const PlanCosts& c, long long budget, WorkUnit* units,
+                 int32_t* worker_ptr) {
   int w = 0, nu = 0;
   long long used = 0;   // cost taken by worker w
   if (worker_ptr) worker_ptr[0] = 0;
@@ -149,13 +149,18 @@ int fill_workers(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int
 
 int partition_units(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int n_workers,
                     int tile_tokens, WorkUnit* units, int32_t* worker_ptr) {
+  return partition_units(kv_indptr, kv_len, batch, n_workers, tile_tokens, plan_costs(tile_tokens),
+                         units, worker_ptr);
+}
+
+int partition_units(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int n_workers,
+                    int tile_tokens, const PlanCosts& c, WorkUnit* units, int32_t* worker_ptr) {
   // Smallest budget the greedy fill meets.  Whether the fill succeeds is not
   // monotone in the budget (where a request is cut depends on it), so a
   // bisection finds a feasible budget `hi` only; the smallest one is then
   // looked for upward from the lower bound every partition obeys (the work
   // spread evenly), at most kMaxScan budgets.  One worker holding everything
   // always fits.
-  const PlanCosts c = plan_costs(tile_tokens);
   long long total = 0, nonempty = 0;
   for (int b = 0; b < batch; ++b) {
     total += tiles_of(kv_len[b], tile_tokens);
@@ -165,7 +170,7 @@ int partition_units(const int32_t* kv_indptr, const int32_t* kv_len, int batch, 
   long long hi = c.tile * total + static_cast<long long>(c.unit + c.split) * (batch + n_workers);
   while (lo + 1 < hi) {
     const long long mid = lo + (hi - lo) / 2;
-    if (fill_workers(kv_indptr, kv_len, batch, n_workers, tile_tokens, mid, nullptr, nullptr) >= 0)
+    if (fill_workers(kv_indptr, kv_len, batch, n_workers, tile_tokens, c, mid, nullptr, nullptr) >= 0)
       hi = mid;
     else
       lo = mid;
@@ -173,11 +178,11 @@ int partition_units(const int32_t* kv_indptr, const int32_t* kv_len, int batch, 
   constexpr long long kMaxScan = 4096;
   const long long bound = (c.tile * total + c.unit * nonempty + n_workers - 1) / n_workers;
   for (long long b = std::max(bound, hi - kMaxScan); b < hi; ++b)
-    if (fill_workers(kv_indptr, kv_len, batch, n_workers, tile_tokens, b, nullptr, nullptr) >= 0) {
+    if (fill_workers(kv_indptr, kv_len, batch, n_workers, tile_tokens, c, b, nullptr, nullptr) >= 0) {
       hi = b;
       break;
     }
-  return fill_workers(kv_indptr, kv_len, batch, n_workers, tile_tokens, hi, units, worker_ptr);
+  return fill_workers(kv_indptr, kv_len, batch, n_workers, tile_tokens, c, hi, units, worker_ptr);
 }
 
 int assign_slots(WorkUnit* units, int n_units, const int32_t* kv_len, int batch, int tile_tokens,
@@ -210,18 +215,59 @@ int assign_slots(WorkUnit* units, int n_units, const int32_t* kv_len, int batch,
 
 void partition_batch(const int32_t* kv_indptr, const int32_t* kv_len, int batch,
                      int n_workers, int tile_tokens, Partition* out) {
+  partition_batch(kv_indptr, kv_len, batch, n_workers, tile_tokens, plan_costs(tile_tokens), out);
+}
+
+void partition_batch(const int32_t* kv_indptr, const int32_t* kv_len, int batch,
+                     int n_workers, int tile_tokens, const PlanCosts& c, Partition* out) {
   out->units.resize(max_units(n_workers, batch));
   out->worker_ptr.assign(n_workers + 1, 0);
   out->merge.resize(batch);
   long long total = 0;
   for (int b = 0; b < batch; ++b) total += tiles_of(kv_len[b], tile_tokens);
   out->total_tiles = static_cast<int>(total);
-  const int nu = partition_units(kv_indptr, kv_len, batch, n_workers, tile_tokens,
+  const int nu = partition_units(kv_indptr, kv_len, batch, n_workers, tile_tokens, c,
                                  out->units.data(), out->worker_ptr.data());
   out->units.resize(nu);
   int nm = 0;
   out->n_slots = assign_slots(out->units.data(), nu, kv_len, batch, tile_tokens, out->merge.data(), &nm);
   out->merge.resize(nm);
+}
+
+long long partition_makespan(const Partition& p, int tile_tokens) {
+  const PlanCosts c = plan_costs(tile_tokens);
+  long long worst = 0;
+  for (size_t w = 0; w + 1 < p.worker_ptr.size(); ++w) {
+    long long used = 0;
+    for (int i = p.worker_ptr[w]; i < p.worker_ptr[w + 1]; ++i) {
+      const WorkUnit& u = p.units[i];
+      used += c.unit + static_cast<long long>(c.tile) * tiles_of(u.tok_end - u.tok_begin, tile_tokens) +
+              (u.n_slots > 0 ? c.split : 0);
+    }
+    worst = std::max(worst, used);
+  }
+  return worst;
+}
+
+double pair_step_estimate_us(const Partition& p, int rows) {
+  constexpr double kTileUs = 3.9;            // one 256-token tile of a CTA pair
+  constexpr double kMergeFixedUs = 2.5;      // a merge pass that combines something
+  constexpr double kMergeBytesPerUs = 2.75e6;
+  double us = partition_makespan(p, kTilePair) * (kTileUs / 4.0);
+  if (p.n_slots > 0)
+    us += kMergeFixedUs + static_cast<double>(p.n_slots) * rows * kDCkv * sizeof(float) / kMergeBytesPerUs;
+  return us;
+}
+
+void partition_batch_pair(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int n_workers,
+                          int rows, Partition* out) {
+  partition_batch(kv_indptr, kv_len, batch, n_workers, kTilePair, out);
+  if (out->n_slots == 0) return;
+  Partition whole;
+  PlanCosts few = plan_costs(kTilePair);
+  few.split = kFewSplitsCost;
+  partition_batch(kv_indptr, kv_len, batch, n_workers, kTilePair, few, &whole);
+  if (pair_step_estimate_us(whole, rows) < pair_step_estimate_us(*out, rows)) *out = std::move(whole);
 }
 
 }  // namespace mla

@@ -44,6 +44,9 @@ constexpr PlanCosts plan_costs(int tile_tokens) {
 // nothing.
 int partition_units(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int n_workers,
                     int tile_tokens, WorkUnit* units, int32_t* worker_ptr);
+// The same under explicit costs.
+int partition_units(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int n_workers,
+                    int tile_tokens, const PlanCosts& c, WorkUnit* units, int32_t* worker_ptr);
 
 // Gives the units of every split request consecutive partial slots and
 // writes one merge entry per split request and per empty request (at most
@@ -51,9 +54,30 @@ int partition_units(const int32_t* kv_indptr, const int32_t* kv_len, int batch, 
 int assign_slots(WorkUnit* units, int n_units, const int32_t* kv_len, int batch, int tile_tokens,
                  MergeEntry* merge, int* n_merge);
 
-// Both steps into growable arrays.
+// Both steps into growable arrays (default or explicit costs).
 void partition_batch(const int32_t* kv_indptr, const int32_t* kv_len, int batch,
                      int n_workers, int tile_tokens, Partition* out);
+void partition_batch(const int32_t* kv_indptr, const int32_t* kv_len, int batch,
+                     int n_workers, int tile_tokens, const PlanCosts& c, Partition* out);
+
+// The largest worker cost of a partition under the default costs.
+long long partition_makespan(const Partition& p, int tile_tokens);
+
+// The CTA-pair kernel's partition (256-token tiles, `rows` query rows per
+// request).  A split request costs its workers the stores of its shares (the
+// `split` cost), and the whole step one merge pass over all the shares,
+// which no per-worker cost expresses.  So when the default partition splits
+// requests, a second one that splits only where a worker cannot hold a
+// request whole (a split unit costs kFewSplitsCost quarter tiles) is built
+// as well, and the one with the smaller estimated step kept: the makespan at
+// ~3.9 us per tile, plus, with shares, ~2.5 us and their bytes (rows x 2 KB
+// each) at ~2.75 TB/s.  (Measured on 128-head batches: two query tokens per
+// request of 64 x 4096 tokens, 156.7 -> 148.6 us per step without splits;
+// ragged and fp8 batches keep their splits.)
+constexpr int kFewSplitsCost = 12;
+double pair_step_estimate_us(const Partition& p, int rows);
+void partition_batch_pair(const int32_t* kv_indptr, const int32_t* kv_len, int batch, int n_workers,
+                          int rows, Partition* out);
 
 // Upper bounds of the partition sizes, used to size plan buffers at creation:
 // a request is cut only where a worker ends, so each worker adds at most one
