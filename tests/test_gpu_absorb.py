@@ -89,6 +89,66 @@ def test_absorbed_chain_matches_unabsorbed_attention(lens, heads, P):
     assert rel <= 1e-2, f"absorbed chain rel-L2 {rel:.2e}"
 
 
+def test_chain_back_to_back_equals_synchronised_chain():
+    """absorb -> decode (+ merge) -> project launched back to back on one
+    stream, each kernel a programmatic dependent launch of the one before it
+    (it waits for that kernel at its first instruction), eagerly and from a
+    CUDA graph: the same bits as the chain with a synchronisation after
+    every call.  The intermediate and output buffers hold NaN before each
+    run, so a kernel that read its input early would show."""
+    x = I.make_inputs("abs_b2b", [2000, 90, 30000], 128, 64, seed=18)   # the last request split
+    d = to_device(x)
+    rng = np.random.Generator(np.random.PCG64(19))
+    _, q_raw = _bf16(rng, (x.batch, 128, 128))
+    _, w_uk = _bf16(rng, (128, 512, 128), 1.0 / math.sqrt(128))
+    _, w_uv = _bf16(rng, (128, 512, 128), 1.0 / math.sqrt(512))
+    q_nope = torch.empty((x.batch, 128, 512), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((x.batch, 128, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((x.batch, 128), dtype=torch.float32, device="cuda")
+    o = torch.empty((x.batch, 128, 128), dtype=torch.bfloat16, device="cuda")
+    dec = mla.MLADecoder(x.batch, 128)
+    try:
+        dec.plan(x.kv_indptr, d["kv_indices"], x.kv_len, 64, x.sm_scale)
+        torch.cuda.synchronize()
+        assert dec.info()["num_partial_slots"] > 0      # the merge kernel has work
+
+        def poison():
+            for t in (q_nope, out, lse, o):
+                t.fill_(float("nan"))
+
+        def chain(sync):
+            mla.mla_absorb_q(q_raw, w_uk, q_nope)
+            if sync:
+                torch.cuda.synchronize()
+            dec.run(q_nope, d["q_pe"], d["ckv"], d["kpe"], out, lse)
+            if sync:
+                torch.cuda.synchronize()
+            mla.mla_project_out(out, w_uv, o)
+            if sync:
+                torch.cuda.synchronize()
+
+        poison()
+        chain(True)
+        ref_o, ref_lse = o.clone(), lse.clone()
+        assert not torch.isnan(ref_o).any()
+        for _ in range(3):
+            poison()
+            chain(False)
+            torch.cuda.synchronize()
+            assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            chain(False)
+        for _ in range(3):
+            poison()
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(o, ref_o) and torch.equal(lse, ref_lse)
+        dec.check_status()
+    finally:
+        dec.close()
+
+
 def test_projection_arguments_are_checked():
     q = torch.zeros((2, 3, 96), dtype=torch.bfloat16, device="cuda")
     w = torch.zeros((3, 512, 96), dtype=torch.bfloat16, device="cuda")
