@@ -177,3 +177,43 @@ def test_packed_full_size_long_b4_mtp4():
                       "long_b4_mtp4")
     finally:
         dec.close()
+
+
+def test_packed_plan_graph_replay_after_replan():
+    """A packed run (3 query tokens x 32 heads = 96 rows per request) captured
+    in a CUDA graph replays after a re-plan with the same q_len, new lengths,
+    pages and cache contents in the same buffers."""
+    Q, H, P = 3, 32, 64
+    x = I.make_inputs("mqg1", [900, 3, 5000], H, P, seed=51, q_len=Q, pool_pages=100)
+    x2 = I.make_inputs("mqg2", [4100, 777, 64], H, P, seed=52, q_len=Q, pool_pages=100)
+    d, d2 = to_device(x), to_device(x2)
+    idx = torch.zeros(100, dtype=torch.int32, device="cuda")
+    idx[: len(x.kv_indices)].copy_(d["kv_indices"])
+    qn, qp, ckv, kpe = (d[k].clone() for k in ("q_nope", "q_pe", "ckv", "kpe"))
+    out = torch.empty((x.batch, Q, H, 512), dtype=torch.float32, device="cuda")
+    lse = torch.empty((x.batch, Q, H), dtype=torch.float32, device="cuda")
+    dec = mla.MLADecoder(x.batch * Q, H, "default")
+    try:
+        dec.plan(x.kv_indptr, idx, x.kv_len, P, x.sm_scale, q_len=Q)
+        assert dec.info()["batch"] == x.batch
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            dec.run(qn, qp, ckv, kpe, out, lse)
+        g.replay()
+        torch.cuda.synchronize()
+        dec.check_status()
+        ref_out, ref_lse = _oracle_x(x)
+        assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), ref_out, ref_lse, "captured")
+        for k, t in (("q_nope", qn), ("q_pe", qp), ("ckv", ckv), ("kpe", kpe)):
+            t.copy_(d2[k])
+        idx.zero_()
+        idx[: len(x2.kv_indices)].copy_(d2["kv_indices"])
+        dec.plan(x2.kv_indptr, idx, x2.kv_len, P, x2.sm_scale, q_len=Q)
+        g.replay()
+        torch.cuda.synchronize()
+        dec.check_status()
+        r2o, r2l = _oracle_x(x2)
+        assert_parity(out.double().cpu().numpy(), lse.double().cpu().numpy(), r2o, r2l, "re-planned")
+    finally:
+        dec.close()
