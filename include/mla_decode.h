@@ -182,8 +182,8 @@ mla_status_t mla_decode_plan_multi(mla_plan_t plan, const int32_t* kv_indptr_hos
  * of its last-finishing unit, requests with kv_len 0 are filled by the same
  * kernel), with the CTA-pair and mma.sync kernels a merge kernel follows.  The combination
  * order is fixed, so repeated runs give bit-identical results.
- * The decode and merge kernels (like the projection kernels below) are
- * programmatic dependent launches: each may be scheduled while the kernel
+ * The decode and merge kernels (like the projection and state-merge kernels
+ * below) are programmatic dependent launches: each may be scheduled while the kernel
  * before it on the stream drains, and waits for that kernel to complete
  * before it reads anything; each lets the next kernel on the stream be
  * scheduled early.  A caller kernel launched after them with programmatic

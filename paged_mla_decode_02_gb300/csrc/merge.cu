@@ -272,6 +272,10 @@ template <bool kOutF32>
 __global__ void __launch_bounds__(32 * kStatesWarps)
     merge_states_kernel(const float* o_a, const float* lse_a, const float* o_b, const float* lse_b,
                         void* out, float* lse_out, int rows) {
+  // a programmatic dependent launch: wait for the kernel before it on the
+  // stream (a no-op in a plain launch), then let the next one be scheduled
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int row = blockIdx.x * kStatesWarps + (threadIdx.x >> 5);
   if (row >= rows) return;
   const int lane = threadIdx.x & 31;
@@ -326,12 +330,17 @@ cudaError_t launch_merge_states(const float* o_a, const float* lse_a, const floa
                                 const float* lse_b, void* out, bool out_f32, float* lse_out,
                                 int rows, cudaStream_t s) {
   if (rows <= 0) return cudaSuccess;
-  const int grid = (rows + kStatesWarps - 1) / kStatesWarps;
-  if (out_f32)
-    merge_states_kernel<true><<<grid, 32 * kStatesWarps, 0, s>>>(o_a, lse_a, o_b, lse_b, out, lse_out, rows);
-  else
-    merge_states_kernel<false><<<grid, 32 * kStatesWarps, 0, s>>>(o_a, lse_a, o_b, lse_b, out, lse_out, rows);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((rows + kStatesWarps - 1) / kStatesWarps);
+  cfg.blockDim = dim3(32 * kStatesWarps);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return out_f32 ? cudaLaunchKernelEx(&cfg, merge_states_kernel<true>, o_a, lse_a, o_b, lse_b, out, lse_out, rows)
+                 : cudaLaunchKernelEx(&cfg, merge_states_kernel<false>, o_a, lse_a, o_b, lse_b, out, lse_out, rows);
 }
 
 cudaError_t launch_merge(const MergeArgs& a, bool out_f32, cudaStream_t s) {
